@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 SpMV library on the 3D 7-point Laplacian 128^3.
+
+One step = one y = A x (every kernel of the handle's apply plan) over the matrix
+already resident in HBM; the format is built once before timing (build time is
+reported separately).  Headline: float64; float32 is measured in the same run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  GFLOP/s = 2 nnz / t; effective GB/s uses the
+algorithmic bytes nnz (value + int32 index) + (n + 1) int32 row pointers + n
+values of x + n values of y.  Multi-GPU runs are independent replicas (one
+process per GPU, no collective on the data path); ``value`` is the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SpMV GFLOP/s and effective HBM GB/s (fraction of GB300 peak), fp64 & fp32"
+UNIT = "GFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129e6
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+# --------------------------------------------------------------------------- #
+# host-side helpers (also exercised by the CPU tests)
+# --------------------------------------------------------------------------- #
+
+
+def effective_bytes(n: int, nnz: int, value_bytes: int) -> int:
+    """Algorithmic bytes of one y = A x: matrix values + int32 indices, int32 row
+    pointers, x read once, y written once."""
+    return nnz * (value_bytes + 4) + (n + 1) * 4 + 2 * n * value_bytes
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, init_method="env://")
+    return dist
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device_index=None):
+    if world <= 1:
+        return
+    import torch.distributed as dist
+
+    if dist.get_backend() == "nccl" and device_index is not None:
+        dist.barrier(device_ids=[device_index])
+    else:
+        dist.barrier()
+
+
+def aggregate_rate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank in at most max_seconds."""
+    return units_per_rank * world / max_seconds
+
+
+def load_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def apply_source_sha() -> str:
+    src = os.path.join(ROOT, "sparse_matrix_vector_csr_gb300", "csrc", "apply.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(workload: str, dtype: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(PROFILE_DIR, "traffic.json")
+    try:
+        with open(path) as f:
+            rows = json.load(f)
+    except Exception:
+        return None
+    for r in rows:
+        if r.get("workload") == workload and r.get("dtype") == dtype and r.get("kernel") == kernel:
+            if r.get("apply_cu_sha") == apply_source_sha():
+                return r.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while a region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.marks = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if t0 <= ts <= t1] or [p for _, p in rows[-3:]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for name, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][1]),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+
+
+def _gpu_id(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def measure_device(torch, spmv, csr, x_np, steps, warmup, sampler=None, fmt="auto"):
+    """Build once, then time `steps` back-to-back applies with CUDA events on the stream."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rp = torch.from_numpy(csr.row_ptr).to(dev)
+    ci = torch.from_numpy(csr.col_idx).to(dev)
+    vv = torch.from_numpy(csr.vals).to(dev)
+    x = torch.from_numpy(x_np).to(dev)
+    y = torch.empty_like(x)
+    torch.cuda.synchronize()
+    t_b = time.perf_counter()
+    A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=fmt)
+    build_ms = (time.perf_counter() - t_b) * 1e3
+    desc = A.describe()
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        A.apply(x, y)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark()
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(steps):
+        A.apply(x, y)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    region_ms = e0.elapsed_time(e1)
+    # per-kernel split of one apply (separate, event-bracketed launches)
+    splits = [A.apply_profiled(x, y) for _ in range(20)]
+    per_kernel = [statistics.median(s[i] for s in splits) for i in range(len(splits[0]))]
+    # cold: L2 flushed before every apply (flush outside the events)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    cold = []
+    for _ in range(30):
+        flush.fill_(1.0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        A.apply(x, y)
+        b.record(stream)
+        b.synchronize()
+        cold.append(a.elapsed_time(b))
+    del flush
+    A.close()
+    return {"region_ms": region_ms, "t0": t0, "t1": t1, "build_ms": build_ms, "desc": desc,
+            "per_kernel_ms": per_kernel, "cold_ms": statistics.median(cold)}
+
+
+def measure_e2e(torch, spmv, csr, x_np, steps):
+    """Public API with host buffers: H2D of x, apply, D2H of y every step (wall clock)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rp = torch.from_numpy(csr.row_ptr).to(dev)
+    ci = torch.from_numpy(csr.col_idx).to(dev)
+    vv = torch.from_numpy(csr.vals).to(dev)
+    with spmv.SpmvMatrix.from_csr(rp, ci, vv) as A:
+        xh = torch.from_numpy(x_np).pin_memory().numpy()
+        yh = torch.empty(csr.n, dtype=torch.from_numpy(x_np).dtype).pin_memory().numpy()
+        for _ in range(3):
+            A.apply_host(xh, yh)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            A.apply_host(xh, yh)
+        t = time.perf_counter() - t0
+    return t
+
+
+def cpu_baseline(csr, x_np, budget_s=8.0):
+    """The oracle as it stands (single thread, long double) on a row prefix sized to the budget."""
+    import numpy as np
+
+    import oracle
+
+    probe = min(csr.n, 20000)
+    t0 = time.perf_counter()
+    oracle.spmv(csr, x_np, rows=np.arange(probe))
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rows = int(min(csr.n, max(probe, probe * budget_s / dt)))
+    t0 = time.perf_counter()
+    oracle.spmv(csr, x_np, rows=np.arange(rows))
+    dt = time.perf_counter() - t0
+    nnz = int(csr.row_ptr[rows])
+    return {"value": 2.0 * nnz / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the workload ({nnz} nonzeros), one pass, "
+                      f"single-threaded long double (LDBL_MANT_DIG={oracle.ldbl_mant_dig()})",
+            "seconds": dt}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+    from workloads import WORKLOADS, make_workload
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev_index = torch.cuda.current_device()
+
+    csr64, x64 = make_workload(args.workload, dtype=np.float64)
+    csr32, x32 = csr64.astype(np.float32), x64.astype(np.float32)
+    n, nnz = csr64.n, csr64.nnz
+
+    sampler = ClockSampler(_gpu_id(torch)) if rank == 0 else None
+    results = {}
+    for tag, csr, x in (("f64", csr64, x64), ("f32", csr32, x32)):
+        barrier(world, dev_index)
+        r = measure_device(torch, spmv, csr, x, args.steps, args.warmup, sampler if tag == "f64" else None,
+                           fmt=args.format)
+        barrier(world, dev_index)
+        r["region_ms_max"] = reduce_max(r["region_ms"], world, device=torch.device("cuda", dev_index))
+        results[tag] = r
+    if sampler:
+        sampler.stop()
+    clocks = sampler.summary(results["f64"]["t0"], results["f64"]["t1"]) if sampler else None
+
+    e2e_steps = min(args.steps, 500)
+    e2e_t = measure_e2e(torch, spmv, csr64, x64, e2e_steps)
+    e2e_t = reduce_max(e2e_t, world, device=torch.device("cuda", dev_index))
+
+    if rank != 0:
+        return
+    peak, peak_kind = load_peaks()
+
+    def summarize(tag, sv):
+        r = results[tag]
+        sec = r["region_ms_max"] / 1e3
+        steps = args.steps
+        gflops = aggregate_rate(2.0 * nnz * steps, world, sec) / 1e9
+        beff = effective_bytes(n, nnz, sv)
+        eff_gbs = aggregate_rate(beff * steps, world, sec) / 1e9
+        kernels = r["desc"]["kernels"]
+        pk = r["per_kernel_ms"]
+        dom = max(range(len(pk)), key=lambda i: pk[i]) if pk else 0
+        if len(kernels) == 1:
+            kernel_ms = r["region_ms"] / steps
+            note = "single-kernel plan: launch duration = timed region / steps"
+        else:
+            share = pk[dom] / sum(pk)
+            kernel_ms = r["region_ms"] / steps * share
+            note = f"{kernels[dom]} share {share:.3f} of the event-timed apply"
+        achieved = beff / (kernel_ms / 1e3) / 1e9
+        traffic = committed_traffic(args.workload, tag, kernels[dom] if kernels else "")
+        return {
+            "value": gflops, "effective_gbs": eff_gbs, "ms_per_step": r["region_ms_max"] / steps,
+            "cold_ms_per_step": r["cold_ms"], "cold_effective_gbs": beff / (r["cold_ms"] / 1e3) / 1e9,
+            "build_ms": r["build_ms"],
+            "format": {k: r["desc"][k] for k in ("format", "C", "sigma", "K", "slots", "padded_entries",
+                                                 "n_long_rows", "segment", "kernels")},
+            "per_kernel_ms": pk,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": kernels[dom] if kernels else None,
+                         "algorithmic_bytes_per_launch": beff, "peak_source": f"{peak_kind} (hbm_gbs)",
+                         "note": note},
+        }
+
+    s64 = summarize("f64", 8)
+    s32 = summarize("f32", 4)
+    e2e_value = aggregate_rate(2.0 * nnz * e2e_steps, world, e2e_t) / 1e9
+    line = {
+        "metric": METRIC, "value": s64["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": s64["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {
+            "workload": WORKLOADS[args.workload]["desc"] + f" (nnz={nnz}), float64 headline, float32 beside it",
+            "n": n, "nnz": nnz, "format": s64["format"]["format"], "parallelism": "replicas" if world > 1 else "single",
+            "l2": (f"inputs larger than L2: one apply streams {effective_bytes(n, nnz, 8) / 1e6:.0f} MB (f64) / "
+                   f"{effective_bytes(n, nnz, 4) / 1e6:.0f} MB (f32) > {L2_BYTES / 1e6:.0f} MB L2, applies back to "
+                   "back; cold_* fields flush L2 before every apply"),
+        },
+        "effective_gbs": s64["effective_gbs"],
+        "roofline": s64["roofline"],
+        "gpu_launches": args.steps * len(s64["format"]["kernels"]),
+        "e2e": {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
+                "h2d_bytes_per_step": n * 8, "d2h_bytes_per_step": n * 8,
+                "note": "spmv_apply_host: pinned x -> device, apply, y -> pinned host, stream sync each step"},
+        "clocks": clocks,
+        "detail_f64": {k: v for k, v in s64.items() if k not in ("roofline",)},
+        "fp32": s32,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(csr64, x64)
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# reference arm: the oracle on host cores
+# --------------------------------------------------------------------------- #
+
+
+def run_reference(args):
+    import numpy as np
+
+    import oracle
+    from workloads import WORKLOADS, make_workload
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    csr, x = make_workload(args.workload, dtype=np.float64)
+    total_steps = args.steps + args.warmup
+    budget = 90.0
+    probe = min(csr.n, 20000)
+    t0 = time.perf_counter()
+    oracle.spmv(csr, x, rows=np.arange(probe))
+    per_row = max(time.perf_counter() - t0, 1e-6) / probe
+    rows = int(max(1, min(csr.n, budget / total_steps / per_row)))
+    sample = np.arange(rows)
+    nnz_s = int(csr.row_ptr[rows])
+    for _ in range(args.warmup):
+        oracle.spmv(csr, x, rows=sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.spmv(csr, x, rows=sample)
+    dt = time.perf_counter() - t0
+    value = 2.0 * nnz_s * args.steps / dt / 1e9
+    sample_desc = (f"each step: rows 0..{rows - 1} ({nnz_s} nonzeros) of the workload, single-threaded long double "
+                   f"oracle (LDBL_MANT_DIG={oracle.ldbl_mant_dig()})")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOADS[args.workload]["desc"] + f" (nnz={csr.nnz}), float64", "n": csr.n,
+                   "nnz": csr.nnz},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="lap3d_128")
+    ap.add_argument("--format", default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * spmv.h -- C interface of the GB300 (sm_103a) sparse matrix-vector product library.
+ *
+ * The library computes y = A x for a square n x n sparse matrix A handed over in
+ * compressed sparse row (CSR) form: row_ptr[n+1], col_idx[nnz], vals[nnz].
+ * Problem statement: "Sparse matrix-vector multiplication (spMVM) is often the
+ * dominating component" of iterative solvers -- GPGPU spMVM paper (arXiv 1112.5588),
+ * introduction; the CSR arrays are the Ap/Aj/Ax of "Development of Krylov and AMG
+ * linear solvers for large-scale sparse matrices on GPUs", matrix formats, Figure 3.
+ *
+ * A build call converts the CSR input, on the device, into one of the storage
+ * formats the pages describe and returns an opaque handle; apply calls reuse it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named row_ptr, col_idx, vals, x, y, perm, slice_ptr are DEVICE
+ *    pointers of the current CUDA device, unless the name ends in _host.
+ *  - Indices are int32; n < 2^31 and nnz < 2^31.  row_ptr[0] = 0, row_ptr is
+ *    non-decreasing, row_ptr[n] = nnz, every column lies in [0, n).  Entries of a
+ *    row may come in any order; duplicate columns are kept and summed; explicit
+ *    zeros are kept as entries.
+ *  - Values and vectors use the handle's value type: SPMV_F64 (double) or
+ *    SPMV_F32 (float).  x and y have n elements and must not overlap.
+ *  - Streams are cudaStream_t values passed as void*; NULL is the legacy default stream.
+ *  - Errors: functions returning int return an spmv_status (0 = success); functions
+ *    returning a handle return NULL on failure.  In both cases spmv_last_error()
+ *    and spmv_last_error_message() describe the failure for the calling thread.
+ *    No entry point traps or aborts on bad input.
+ */
+#ifndef SPMV_GB300_H
+#define SPMV_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPMV_API __attribute__((visibility("default")))
+#else
+#define SPMV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spmv_handle_s *spmv_handle_t;
+
+/* value type of the matrix, x and y */
+typedef enum { SPMV_F64 = 0, SPMV_F32 = 1 } spmv_dtype;
+
+/*
+ * Storage formats.
+ *  SPMV_FMT_CSR_VECTOR  CSR kept as given; a group of g lanes (g = 2..32, chosen per
+ *      row-length bin) works on one row and combines its partial sums with warp
+ *      shuffles.  Source: "Load-balancing Sparse Matrix Vector Product Kernels on
+ *      GPUs" (scite report), quoted "Sparse Linear Algebra on AMD and NVIDIA GPUs",
+ *      the subwarp-per-row CSR algorithm; row-length classes from the Trilinos issue
+ *      "Tpetra::CrsMatrix::unpackAndCombine: Optimize GPU unpack for few long rows".
+ *  SPMV_FMT_ELL_R       ELLPACK-R: rows shifted left into an n x max-row-length
+ *      rectangle stored column by column (leading dimension a multiple of 32) plus a
+ *      row-length array, one thread per row that stops at its row's end.  GPGPU
+ *      spMVM paper, ELLPACK-R section, Figs. 1-2.
+ *  SPMV_FMT_SELL        SELL-C-sigma: rows sorted by length inside windows of sigma
+ *      rows, cut into slices of C rows, each slice padded to its longest row and
+ *      stored column by column.  sigma = n is pJDS (GPGPU spMVM paper, pJDS section,
+ *      Fig. 1 "sort" and "pad"), sigma = 1 keeps the natural order; SELL-P is the
+ *      sliced ELL of the scite report's abstract.
+ *  SPMV_FMT_HYB         ELL part of width K plus a spill holding the rest of each
+ *      row, as COO (HYB) or CSR (HEC); the ELL part is computed first and writes y,
+ *      the spill adds into y.  Krylov/AMG paper, matrix formats, Figs. 1-3 and the
+ *      HEC SpMV algorithm.
+ *  SPMV_FMT_AUTO        the builder picks one of the above from the row lengths.
+ * In every format, rows longer than the long-row threshold are taken out and
+ * handled by a load-balanced merge-path pass (the "very long rows" class of the
+ * Trilinos issue; merge-path split as the Trilinos issue attributes to the vendor
+ * library), so no single thread walks a very long row.
+ */
+typedef enum {
+    SPMV_FMT_AUTO = 0,
+    SPMV_FMT_CSR_VECTOR = 1,
+    SPMV_FMT_ELL_R = 2,
+    SPMV_FMT_SELL = 3,
+    SPMV_FMT_HYB = 4
+} spmv_format;
+
+/*
+ * Tuning parameters; a negative value (or 0 where noted) means "choose automatically".
+ *   C                   SELL slice height: 32 or 64 (warp-size multiple).
+ *   sigma               SELL sort window in rows: 1 = no sort, >= n = global sort (pJDS).
+ *   K                   HYB ELL width.  Automatic: the smallest K with
+ *                       (value_bytes + 8) * #{rows longer than K} <= ld * (value_bytes + 4).
+ *   spill_csr           HYB spill kind: 1 = CSR (HEC), 0 = COO (HYB).  Automatic = CSR.
+ *   long_row_threshold  rows with more entries go to the merge-path pass.  0 = never.
+ *   subwarp             CSR-vector lanes per row (2, 4, 8, 16 or 32) for every row;
+ *                       automatic = per row-length bin.
+ */
+typedef struct {
+    int32_t C;
+    int64_t sigma;
+    int32_t K;
+    int32_t spill_csr;
+    int32_t long_row_threshold;
+    int32_t subwarp;
+} spmv_format_params;
+
+typedef enum {
+    SPMV_OK = 0,
+    SPMV_ERR_INVALID_ARG = -1, /* NULL pointer, bad size, bad enum value */
+    SPMV_ERR_BAD_CSR = -2,     /* row_ptr not monotone / wrong ends, column out of range */
+    SPMV_ERR_CUDA = -3,        /* a CUDA runtime call failed (message has the CUDA error) */
+    SPMV_ERR_OOM = -4,         /* device allocation failed */
+    SPMV_ERR_TOO_LARGE = -5,   /* the requested layout would exceed the library's size limits */
+    SPMV_ERR_UNSUPPORTED = -6, /* parameter combination not supported */
+    SPMV_ERR_TIMEOUT = -7      /* reserved: a bounded device wait ran out */
+} spmv_status;
+
+/* Fill *p with "all automatic" values.  Returns SPMV_OK or SPMV_ERR_INVALID_ARG. */
+SPMV_API int spmv_default_params(spmv_format_params *p);
+
+/*
+ * Build a handle from a device CSR matrix.
+ *   n, nnz    matrix order and number of stored entries (0 allowed for both).
+ *   row_ptr   int32[n+1], col_idx int32[nnz], vals double/float[nnz]: device memory,
+ *             only read; the handle keeps its own copies, so the caller may free or
+ *             overwrite them once the call returns.
+ *   dtype     spmv_dtype; format: spmv_format.
+ * The work runs on the legacy default stream and the call returns after it has
+ * finished; inputs written on other streams must be complete before the call.
+ * The CSR is validated on the device; a malformed matrix returns NULL with
+ * SPMV_ERR_BAD_CSR.  A fixed format whose storage would not fit returns NULL with
+ * SPMV_ERR_TOO_LARGE or SPMV_ERR_OOM; there is never a silent change of format.
+ */
+SPMV_API spmv_handle_t spmv_build_from_csr(int64_t n, int64_t nnz, const int32_t *row_ptr,
+                                  const int32_t *col_idx, const void *vals, int dtype, int format);
+
+/* As spmv_build_from_csr, with tuning parameters (NULL = automatic) and a stream
+ * (the build is ordered after earlier work on that stream and synchronises it). */
+SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int32_t *row_ptr,
+                                     const int32_t *col_idx, const void *vals, int dtype,
+                                     int format, const spmv_format_params *params, void *stream);
+
+/*
+ * y = A x, overwriting y (no scaling, no accumulation into the old y).
+ * x and y are device arrays of n elements of the handle's value type, in the
+ * caller's original row order (any row permutation of the format is internal).
+ * Asynchronous on `stream`: returns after enqueueing 1 to 4 kernel launches.
+ * The handle holds a small scratch array for the merge-path pass, so two applies
+ * of the SAME handle must not run concurrently (on different streams); applies of
+ * different handles may.  Empty rows give +0.
+ */
+SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
+
+/*
+ * y_host = A x_host with host arrays: copies x to the device, applies, copies y
+ * back and waits for the stream.  Page-locked (pinned) host buffers give the full
+ * copy bandwidth.  The device staging buffers are allocated by the first call on
+ * a handle and kept until spmv_destroy.
+ */
+SPMV_API int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *stream);
+
+/*
+ * As spmv_apply, but records CUDA events around each kernel it launches, waits for
+ * them and writes each launch's device time in milliseconds to kernel_ms[0..cap).
+ * Returns the number of kernels launched (>= 0) or a negative spmv_status.  Meant
+ * for measurement, not for the hot loop.
+ */
+SPMV_API int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, float *kernel_ms,
+                        int cap);
+
+/* Release every device buffer of the handle.  NULL is accepted and ignored. */
+SPMV_API void spmv_destroy(spmv_handle_t h);
+
+/* Status of the last failing call on this thread (SPMV_OK if none) and its message. */
+SPMV_API int spmv_last_error(void);
+SPMV_API const char *spmv_last_error_message(void);
+/* Static description of a status code. */
+SPMV_API const char *spmv_error_string(int status);
+
+/*
+ * Rebuild the CSR held by the handle, in the caller's row order and in the input's
+ * in-row order: row_ptr int32[n+1], col_idx int32[nnz], vals[nnz] (device memory
+ * owned by the caller).  Every format stores exactly the input entries, so the
+ * result equals the build input array for array.  Synchronises `stream`.
+ */
+SPMV_API int spmv_to_csr(spmv_handle_t h, int32_t *row_ptr, int32_t *col_idx, void *vals, void *stream);
+
+/*
+ * Write a JSON object describing the handle (format, resolved parameters, padded
+ * and allocated slots, long rows, spill size, kernels launched per apply, bytes
+ * streamed per apply) into json[0..cap).  Returns SPMV_OK, or SPMV_ERR_INVALID_ARG
+ * when cap is too small (the text is then truncated but NUL-terminated).
+ */
+SPMV_API int spmv_describe(spmv_handle_t h, char *json, size_t cap);
+
+/*
+ * Copy layout arrays of the sliced part (SELL, ELL-R or the HYB ELL part):
+ *   perm       int32[n]: perm[p] = original row stored at sorted position p
+ *              (the identity when the format keeps the natural order);
+ *   slice_ptr  int64[n_slices + 1]: start of every slice in the slot arrays.
+ * Either pointer may be NULL.  Sizes are in spmv_describe ("n_slices").  Returns
+ * SPMV_ERR_UNSUPPORTED for a handle without a sliced part.  Synchronises `stream`.
+ */
+SPMV_API int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPMV_GB300_H */

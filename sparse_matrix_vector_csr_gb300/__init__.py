@@ -1,0 +1,139 @@
+"""GB300 (sm_103a) sparse matrix-vector product, y = A x, for CSR input.
+
+The computation lives in the CUDA library ``libspmv_gb300.so`` (C interface in
+``include/spmv.h``); this package is its Python binding.  ``_abi`` mirrors the C
+entry points one to one; :class:`SpmvMatrix` wraps a handle for torch tensors.
+
+    import torch, sparse_matrix_vector_csr_gb300 as spmv
+    A = spmv.SpmvMatrix.from_csr(row_ptr, col_idx, vals)        # CUDA tensors
+    y = A @ x                                                   # or A.apply(x, y)
+"""
+from __future__ import annotations
+
+from . import _abi
+from ._abi import (  # noqa: F401
+    FORMATS,
+    SpmvError,
+    spmv_apply,
+    spmv_apply_host,
+    spmv_apply_profiled,
+    spmv_build_from_csr,
+    spmv_build_from_csr_ex,
+    spmv_default_params,
+    spmv_describe,
+    spmv_destroy,
+    spmv_error_string,
+    spmv_get_layout,
+    spmv_last_error,
+    spmv_last_error_message,
+    spmv_to_csr,
+)
+
+__all__ = ["SpmvMatrix", "SpmvError", "FORMATS"] + [n for n in _abi.EXPORTS]
+
+
+class SpmvMatrix:
+    """A square sparse matrix held by the CUDA library in one storage format."""
+
+    def __init__(self, handle: int, n: int, nnz: int, dtype):
+        self._h = handle
+        self.n = n
+        self.nnz = nnz
+        self.dtype = dtype
+
+    @classmethod
+    def from_csr(cls, row_ptr, col_idx, vals, format: str = "auto", stream=None, **params) -> "SpmvMatrix":
+        """Build from device CSR tensors (int32 row_ptr/col_idx, float64/float32 vals).
+
+        ``params``: C, sigma, K, spill_csr, long_row_threshold, subwarp (see spmv.h).
+        """
+        import torch
+
+        for name, t in (("row_ptr", row_ptr), ("col_idx", col_idx), ("vals", vals)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous CUDA tensor")
+        if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+            raise TypeError("row_ptr and col_idx must be int32")
+        n = row_ptr.numel() - 1
+        nnz = col_idx.numel()
+        if vals.numel() != nnz:
+            raise ValueError("vals and col_idx differ in length")
+        code = _abi.dtype_code(vals.dtype)
+        h = spmv_build_from_csr_ex(n, nnz, row_ptr, col_idx, vals, code, format, params, stream)
+        return cls(h, n, nnz, vals.dtype)
+
+    def _check_vec(self, v, name):
+        import torch
+
+        if not (isinstance(v, torch.Tensor) and v.is_cuda and v.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous CUDA tensor")
+        if v.dtype != self.dtype or v.numel() != self.n:
+            raise ValueError(f"{name} must hold {self.n} values of {self.dtype}")
+
+    def apply(self, x, y=None, stream=None):
+        """y = A x on the current (or given) stream; allocates y when not given."""
+        import torch
+
+        self._check_vec(x, "x")
+        if y is None:
+            y = torch.empty_like(x)
+        self._check_vec(y, "y")
+        spmv_apply(self._h, x, y, stream)
+        return y
+
+    __matmul__ = apply
+
+    def apply_host(self, x_host, y_host=None):
+        """y = A x for numpy host arrays (pinned memory recommended)."""
+        import numpy as np
+
+        if y_host is None:
+            y_host = np.empty_like(x_host)
+        spmv_apply_host(self._h, x_host, y_host)
+        return y_host
+
+    def apply_profiled(self, x, y, stream=None):
+        """Per-kernel device times (ms) of one apply."""
+        return spmv_apply_profiled(self._h, x, y, stream)
+
+    def to_csr(self):
+        """The stored CSR (original row order and in-row order) as CUDA tensors."""
+        import torch
+
+        dev = torch.device("cuda", torch.cuda.current_device())
+        rp = torch.empty(self.n + 1, dtype=torch.int32, device=dev)
+        ci = torch.empty(self.nnz, dtype=torch.int32, device=dev)
+        vv = torch.empty(self.nnz, dtype=self.dtype, device=dev)
+        spmv_to_csr(self._h, rp, ci, vv)
+        return rp, ci, vv
+
+    def describe(self) -> dict:
+        return spmv_describe(self._h)
+
+    def layout(self):
+        """(perm, slice_ptr) of the sliced part as CUDA tensors."""
+        import torch
+
+        d = self.describe()
+        dev = torch.device("cuda", torch.cuda.current_device())
+        perm = torch.empty(self.n, dtype=torch.int32, device=dev)
+        sp = torch.empty(d["n_slices"] + 1, dtype=torch.int64, device=dev)
+        spmv_get_layout(self._h, perm, sp)
+        return perm, sp
+
+    def close(self):
+        if self._h:
+            spmv_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

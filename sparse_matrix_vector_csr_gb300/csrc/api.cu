@@ -1,0 +1,948 @@
+// C-ABI entry points of the sm_103a SpMV library (declared in include/spmv.h):
+// argument checks, format selection, the build sequence, apply dispatch, and the
+// inspection helpers used by tests and the bench.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "spmv_internal.cuh"
+
+namespace spmv {
+
+namespace {
+thread_local int g_last_error = SPMV_OK;
+thread_local char g_last_msg[1024] = "";
+}  // namespace
+
+int set_error(int status, const std::string &msg) {
+    g_last_error = status;
+    std::snprintf(g_last_msg, sizeof(g_last_msg), "%s", msg.c_str());
+    return status;
+}
+
+int set_cuda_error(cudaError_t err, const char *what) {
+    const int st = (err == cudaErrorMemoryAllocation) ? SPMV_ERR_OOM : SPMV_ERR_CUDA;
+    (void)cudaGetLastError();  // clear a non-sticky error so later calls start clean
+    return set_error(st, std::string(what) + ": " + cudaGetErrorString(err));
+}
+
+namespace {
+
+void clear_error() {
+    g_last_error = SPMV_OK;
+    g_last_msg[0] = '\0';
+}
+
+// ---------------------------------------------------------------------------
+// memory helpers
+// ---------------------------------------------------------------------------
+int dev_alloc(spmv_handle_t h, void **p, size_t bytes) {
+    *p = nullptr;
+    if (bytes == 0) return SPMV_OK;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        return set_cuda_error(e, "cudaMalloc");
+    }
+    h->allocations.push_back(*p);
+    return SPMV_OK;
+}
+
+template <class T>
+int dev_alloc_n(spmv_handle_t h, T **p, int64_t count) {
+    void *q = nullptr;
+    int st = dev_alloc(h, &q, static_cast<size_t>(count) * sizeof(T));
+    *p = static_cast<T *>(q);
+    return st;
+}
+
+void dev_free(spmv_handle_t h, void *p) {
+    if (!p) return;
+    auto it = std::find(h->allocations.begin(), h->allocations.end(), p);
+    if (it != h->allocations.end()) h->allocations.erase(it);
+    cudaFree(p);
+}
+
+// Temporary device buffers of one build call, released when it returns.
+struct Temp {
+    std::vector<void *> ptrs;
+    ~Temp() {
+        for (void *p : ptrs) cudaFree(p);
+    }
+    template <class T>
+    int get(T **p, int64_t count) {
+        *p = nullptr;
+        if (count <= 0) count = 1;
+        void *q = nullptr;
+        cudaError_t e = cudaMalloc(&q, static_cast<size_t>(count) * sizeof(T));
+        if (e != cudaSuccess) return set_cuda_error(e, "cudaMalloc (build temporary)");
+        ptrs.push_back(q);
+        *p = static_cast<T *>(q);
+        return SPMV_OK;
+    }
+};
+
+int check_device_pointer(const void *p, const char *name) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return set_error(SPMV_ERR_INVALID_ARG, std::string(name) + " is not a CUDA pointer");
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return set_error(SPMV_ERR_INVALID_ARG, std::string(name) + " is not device memory");
+    return SPMV_OK;
+}
+
+int bits_for(uint64_t v) {
+    int b = 0;
+    while (v) {
+        ++b;
+        v >>= 1;
+    }
+    return b;
+}
+
+int check_fits(double bytes, const char *what) {
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SPMV_OK;
+    }
+    if (bytes > 0.9 * static_cast<double>(free_b))
+        return set_error(SPMV_ERR_TOO_LARGE, std::string(what) + ": layout needs " +
+                                                 std::to_string(static_cast<long long>(bytes)) +
+                                                 " bytes, more than the free device memory allows");
+    return SPMV_OK;
+}
+
+const char *format_name(int f) {
+    switch (f) {
+        case SPMV_FMT_AUTO: return "auto";
+        case SPMV_FMT_CSR_VECTOR: return "csr_vector";
+        case SPMV_FMT_ELL_R: return "ell_r";
+        case SPMV_FMT_SELL: return "sell";
+        case SPMV_FMT_HYB: return "hyb";
+        default: return "?";
+    }
+}
+
+// default long-row threshold: keeps every sequential per-thread sum short enough for
+// the per-row error bound (about 4096 fp64 / 128 fp32 terms per thread)
+int32_t default_threshold(int format, int dtype) {
+    if (format == SPMV_FMT_CSR_VECTOR) return dtype == SPMV_F64 ? 8192 : 4096;
+    return dtype == SPMV_F64 ? 4096 : 128;
+}
+
+// ---------------------------------------------------------------------------
+// build context
+// ---------------------------------------------------------------------------
+struct BuildCtx {
+    spmv_handle_t h;
+    cudaStream_t s;
+    const int32_t *row_ptr;  // caller's
+    const int32_t *col;      // caller's
+    const void *val;         // caller's
+    int32_t *len = nullptr;  // [n] row lengths (temporary)
+    std::vector<int64_t> hist;
+    int64_t n_long = 0, long_nnz = 0;
+    int32_t max_short = 0;
+    int32_t threshold = -1;  // -1 = no long-row cut
+    Temp temp;
+};
+
+int sync(cudaStream_t s) {
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    SPMV_TRY_CUDA(cudaGetLastError());
+    return SPMV_OK;
+}
+
+// Stable partition of rows by a small bucket id (one 8-bit counting pass).
+// rows_out gets the row ids grouped by bucket; bucket_start[b] = first index of bucket b.
+int partition_rows(BuildCtx &c, int mode, int32_t a, int32_t forced_g, int32_t *rows_out,
+                   std::vector<int64_t> &bucket_start) {
+    const int64_t n = c.h->n;
+    uint32_t *keys = nullptr, *keys_out = nullptr;
+    int64_t *counts = nullptr, *offsets = nullptr, *scan_tmp = nullptr;
+    const int64_t nb = radix_blocks(n);
+    SPMV_TRY(c.temp.get(&keys, n));
+    SPMV_TRY(c.temp.get(&keys_out, n));
+    SPMV_TRY(c.temp.get(&counts, 256 * nb + 1));
+    SPMV_TRY(c.temp.get(&offsets, 256 * nb + 1));
+    SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(256 * nb)));
+    int32_t *vals_in = nullptr;
+    SPMV_TRY(c.temp.get(&vals_in, n));
+    SPMV_TRY_CUDA(launch_bucket_keys(n, c.len, mode, a, forced_g, keys, vals_in, c.s));
+    SPMV_TRY_CUDA(launch_radix_pass(keys, vals_in, n, 0, keys_out, rows_out, counts, offsets, scan_tmp, c.s));
+    // offsets[b * nb] is where bucket b starts
+    bucket_start.assign(9, n);
+    std::vector<int64_t> host(8);
+    for (int b = 0; b < 8; ++b)
+        SPMV_TRY_CUDA(cudaMemcpyAsync(&host[b], offsets + static_cast<int64_t>(b) * nb, sizeof(int64_t),
+                                      cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY(sync(c.s));
+    for (int b = 0; b < 8; ++b) bucket_start[b] = host[b];
+    bucket_start[8] = n;
+    return SPMV_OK;
+}
+
+// Compact CSR of the listed rows, entries from in-row position `offset` on.
+int build_segment(BuildCtx &c, const int32_t *rows_dev, int64_t m, int32_t offset, int kind, int accumulate) {
+    spmv_handle_t h = c.h;
+    Segmented &sg = h->seg;
+    sg = Segmented();
+    if (m <= 0) return SPMV_OK;
+    sg.kind = kind;
+    sg.n_rows = m;
+    sg.accumulate = accumulate;
+    sg.dst_offset = offset;
+    SPMV_TRY(dev_alloc_n(h, &sg.rows, m));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(sg.rows, rows_dev, sizeof(int32_t) * m, cudaMemcpyDeviceToDevice, c.s));
+    int64_t *sizes = nullptr, *cptr = nullptr, *scan_tmp = nullptr;
+    SPMV_TRY(c.temp.get(&sizes, m));
+    SPMV_TRY(c.temp.get(&cptr, m + 1));
+    SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(m)));
+    SPMV_TRY_CUDA(launch_compact_sizes(m, sg.rows, c.len, offset, sizes, c.s));
+    SPMV_TRY_CUDA(launch_exclusive_scan(sizes, m, cptr, scan_tmp, c.s));
+    int64_t total = 0;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&total, cptr + m, sizeof(int64_t), cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY(sync(c.s));
+    sg.nnz = total;
+    const size_t vb = value_bytes(h->dtype);
+    SPMV_TRY(check_fits(static_cast<double>(total) * static_cast<double>(vb + 8) + 8.0 * m, "segmented part"));
+    SPMV_TRY(dev_alloc_n(h, &sg.ptr, m + 1));
+    SPMV_TRY_CUDA(launch_int64_to_int32(cptr, m + 1, sg.ptr, c.s));
+    SPMV_TRY(dev_alloc_n(h, &sg.col, total));
+    SPMV_TRY(dev_alloc(h, &sg.val, static_cast<size_t>(total) * vb));
+    if (kind == 2) SPMV_TRY(dev_alloc_n(h, &sg.coo_row, total));
+    SPMV_TRY_CUDA(launch_compact_copy(h->dtype, m, sg.rows, c.row_ptr, offset, c.col, c.val, cptr, sg.col, sg.val,
+                                      sg.coo_row, c.s));
+    sg.n_cta = (kind == 1) ? merge_ctas(m, total) : coo_ctas(total);
+    if (sg.n_cta > 0) {
+        SPMV_TRY(dev_alloc_n(h, &sg.carry_row, sg.n_cta));
+        SPMV_TRY(dev_alloc_n(h, &sg.carry_val, sg.n_cta));
+    }
+    return SPMV_OK;
+}
+
+// Long rows (len > threshold) leave the main format for the merge-path pass.
+int build_long_rows(BuildCtx &c, int accumulate) {
+    if (c.n_long <= 0) return SPMV_OK;
+    int32_t *rows = nullptr;
+    SPMV_TRY(c.temp.get(&rows, c.h->n));
+    std::vector<int64_t> start;
+    SPMV_TRY(partition_rows(c, 0, c.threshold, 0, rows, start));
+    const int64_t m = start[2] - start[1];
+    if (m != c.n_long) return set_error(SPMV_ERR_CUDA, "long-row partition count mismatch");
+    return build_segment(c, rows + start[1], m, 0, 1, accumulate);
+}
+
+// ---------------------------------------------------------------------------
+// sliced part (SELL-C-sigma, ELLPACK-R, HYB's ELL)
+// ---------------------------------------------------------------------------
+
+// Plan: order, per-position lengths, slice widths and offsets.  `lens` are the
+// lengths to store (long rows already 0).  ell_ld > 0 selects the single-slice
+// ELL addressing with that leading dimension and width = max length.
+int plan_sliced(BuildCtx &c, const int32_t *lens, int32_t C, int64_t sigma, int64_t ell_ld, int32_t max_len) {
+    spmv_handle_t h = c.h;
+    const int64_t n = h->n;
+    Sliced &sl = h->sliced;
+    sl = Sliced();
+    sl.present = true;
+    sl.sigma = sigma;
+    if (ell_ld > 0) {
+        sl.C = static_cast<int32_t>(std::min<int64_t>(ell_ld, INT32_MAX));
+        sl.ld = ell_ld;
+        sl.n_pos = ell_ld;
+        sl.log2C = 31;
+        sl.cmask = 0x7fffffffu;
+        sl.stride = ell_ld;
+        sl.n_slices = 1;
+        sl.sigma = 1;
+    } else {
+        sl.C = C;
+        sl.n_pos = ceil_div(n, C) * C;
+        sl.log2C = bits_for(static_cast<uint64_t>(C)) - 1;
+        sl.cmask = static_cast<uint32_t>(C - 1);
+        sl.stride = C;
+        sl.n_slices = sl.n_pos / C;
+    }
+    // order
+    int32_t *perm_tmp = nullptr;
+    if (sl.sigma > 1 && n > 1) {
+        SPMV_TRY(c.temp.get(&perm_tmp, n));
+        const int64_t sig = std::min<int64_t>(sl.sigma, n);
+        if (sig <= kWindowSortMax) {
+            SPMV_TRY_CUDA(launch_window_sort(lens, n, sig, perm_tmp, c.s));
+        } else {
+            const int64_t windows = ceil_div(n, sig);
+            const int wbits = bits_for(static_cast<uint64_t>(windows - 1));
+            const int lbits = bits_for(static_cast<uint64_t>(max_len));
+            if (wbits + lbits > 32)
+                return set_error(SPMV_ERR_UNSUPPORTED, "SELL sort key does not fit 32 bits for this sigma");
+            const int total_bits = wbits + lbits;
+            uint32_t *k0 = nullptr, *k1 = nullptr;
+            int32_t *v0 = nullptr, *v1 = nullptr;
+            int64_t *counts = nullptr, *offsets = nullptr, *scan_tmp = nullptr;
+            const int64_t nb = radix_blocks(n);
+            SPMV_TRY(c.temp.get(&k0, n));
+            SPMV_TRY(c.temp.get(&k1, n));
+            SPMV_TRY(c.temp.get(&v0, n));
+            SPMV_TRY(c.temp.get(&v1, n));
+            SPMV_TRY(c.temp.get(&counts, 256 * nb + 1));
+            SPMV_TRY(c.temp.get(&offsets, 256 * nb + 1));
+            SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(256 * nb)));
+            SPMV_TRY_CUDA(launch_sort_keys(lens, n, sig, lbits, max_len, k0, v0, c.s));
+            int passes = std::max(1, (total_bits + 7) / 8);
+            for (int p = 0; p < passes; ++p) {
+                SPMV_TRY_CUDA(launch_radix_pass(k0, v0, n, 8 * p, k1, v1, counts, offsets, scan_tmp, c.s));
+                std::swap(k0, k1);
+                std::swap(v0, v1);
+            }
+            perm_tmp = v0;
+        }
+        SPMV_TRY(dev_alloc_n(h, &sl.perm, sl.n_pos));
+    }
+    SPMV_TRY(dev_alloc_n(h, &sl.len, sl.n_pos));
+    SPMV_TRY_CUDA(launch_gather_sorted(lens, perm_tmp, n, sl.n_pos, sl.len, sl.perm, c.s));
+    // widths and offsets
+    SPMV_TRY(dev_alloc_n(h, &sl.width, sl.n_slices));
+    SPMV_TRY(dev_alloc_n(h, &sl.slice_ptr, sl.n_slices + 1));
+    std::vector<int32_t> widths(static_cast<size_t>(sl.n_slices));
+    if (ell_ld > 0) {
+        widths[0] = max_len;
+        SPMV_TRY_CUDA(cudaMemcpyAsync(sl.width, widths.data(), sizeof(int32_t), cudaMemcpyHostToDevice, c.s));
+        const int64_t sp[2] = {0, ell_ld * static_cast<int64_t>(max_len)};
+        SPMV_TRY_CUDA(cudaMemcpyAsync(sl.slice_ptr, sp, sizeof(sp), cudaMemcpyHostToDevice, c.s));
+        SPMV_TRY(sync(c.s));
+        sl.slots = sp[1];
+        sl.padded_entries = n * static_cast<int64_t>(max_len);
+        sl.max_width = max_len;
+    } else {
+        int64_t *sizes = nullptr, *scan_tmp = nullptr;
+        SPMV_TRY(c.temp.get(&sizes, sl.n_slices));
+        SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(sl.n_slices)));
+        SPMV_TRY_CUDA(launch_slice_widths(sl.len, sl.n_slices, sl.C, sl.width, sizes, c.s));
+        SPMV_TRY_CUDA(launch_exclusive_scan(sizes, sl.n_slices, sl.slice_ptr, scan_tmp, c.s));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(widths.data(), sl.width, sizeof(int32_t) * sl.n_slices,
+                                      cudaMemcpyDeviceToHost, c.s));
+        SPMV_TRY(sync(c.s));
+        int64_t slots = 0, padded = 0;
+        int32_t mw = 0;
+        for (int64_t s = 0; s < sl.n_slices; ++s) {
+            const int64_t rows_here = std::min<int64_t>(sl.C, n - s * sl.C);
+            slots += static_cast<int64_t>(widths[s]) * sl.C;
+            padded += static_cast<int64_t>(widths[s]) * rows_here;
+            mw = std::max(mw, widths[s]);
+        }
+        sl.slots = slots;
+        sl.padded_entries = padded;
+        sl.max_width = mw;
+    }
+    return SPMV_OK;
+}
+
+int fill_sliced(BuildCtx &c) {
+    spmv_handle_t h = c.h;
+    Sliced &sl = h->sliced;
+    const size_t vb = value_bytes(h->dtype);
+    SPMV_TRY(check_fits(static_cast<double>(sl.slots) * static_cast<double>(vb + 4), "sliced part"));
+    SPMV_TRY(dev_alloc_n(h, &sl.col, sl.slots));
+    SPMV_TRY(dev_alloc(h, &sl.val, static_cast<size_t>(sl.slots) * vb));
+    SPMV_TRY_CUDA(launch_fill_sliced(h->dtype, sl, c.row_ptr, c.col, c.val, c.s));
+    return SPMV_OK;
+}
+
+void release_sliced(spmv_handle_t h) {
+    Sliced &sl = h->sliced;
+    dev_free(h, sl.perm);
+    dev_free(h, sl.len);
+    dev_free(h, sl.width);
+    dev_free(h, sl.slice_ptr);
+    dev_free(h, sl.col);
+    dev_free(h, sl.val);
+    sl = Sliced();
+}
+
+// ---------------------------------------------------------------------------
+// per-format builds
+// ---------------------------------------------------------------------------
+int build_sell_like(BuildCtx &c, int format, int32_t C, int64_t sigma) {
+    spmv_handle_t h = c.h;
+    int32_t *clip = nullptr;
+    SPMV_TRY(c.temp.get(&clip, h->n));
+    SPMV_TRY_CUDA(launch_clip_long(h->n, c.len, c.threshold, clip, c.s));
+    if (format == SPMV_FMT_ELL_R) {
+        const int64_t ld = ceil_div(std::max<int64_t>(h->n, 1), 32) * 32;
+        SPMV_TRY(check_fits(static_cast<double>(ld) * c.max_short * static_cast<double>(value_bytes(h->dtype) + 4),
+                            "ELLPACK-R"));
+        SPMV_TRY(plan_sliced(c, clip, 0, 1, ld, c.max_short));
+    } else {
+        SPMV_TRY(plan_sliced(c, clip, C, sigma, 0, c.max_short));
+    }
+    h->sliced.stored_entries = h->nnz - c.long_nnz;
+    SPMV_TRY(fill_sliced(c));
+    SPMV_TRY(build_long_rows(c, 1));
+    h->kernels.push_back(format == SPMV_FMT_ELL_R ? "ell_r" : "sell");
+    return SPMV_OK;
+}
+
+int build_hyb(BuildCtx &c, int32_t K, int spill_csr) {
+    spmv_handle_t h = c.h;
+    const int64_t n = h->n;
+    h->K = K;
+    int32_t *ell_len = nullptr;
+    SPMV_TRY(c.temp.get(&ell_len, n));
+    SPMV_TRY_CUDA(launch_min_len(n, c.len, K, ell_len, c.s));
+    const int64_t ld = ceil_div(std::max<int64_t>(n, 1), 256) * 256;
+    const int32_t width = std::min<int32_t>(K, h->max_len);
+    SPMV_TRY(check_fits(static_cast<double>(ld) * width * static_cast<double>(value_bytes(h->dtype) + 4),
+                        "HYB ELL part"));
+    SPMV_TRY(plan_sliced(c, ell_len, 0, 1, ld, width));
+    SPMV_TRY(fill_sliced(c));
+    // spill rows: len > K
+    int32_t *rows = nullptr;
+    SPMV_TRY(c.temp.get(&rows, n));
+    std::vector<int64_t> start;
+    SPMV_TRY(partition_rows(c, 1, K, 0, rows, start));
+    const int64_t m = start[2] - start[1];
+    SPMV_TRY(build_segment(c, rows + start[1], m, K, spill_csr ? 1 : 2, 1));
+    h->sliced.stored_entries = h->nnz - h->seg.nnz;
+    h->kernels.push_back("hyb_ell");
+    return SPMV_OK;
+}
+
+int build_csr_vector(BuildCtx &c, int32_t forced_g) {
+    spmv_handle_t h = c.h;
+    const int64_t n = h->n;
+    const size_t vb = value_bytes(h->dtype);
+    SPMV_TRY(dev_alloc_n(h, &h->csr_col, h->nnz));
+    SPMV_TRY(dev_alloc(h, &h->csr_val, static_cast<size_t>(h->nnz) * vb));
+    if (h->nnz > 0) {
+        SPMV_TRY_CUDA(cudaMemcpyAsync(h->csr_col, c.col, sizeof(int32_t) * h->nnz, cudaMemcpyDeviceToDevice, c.s));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(h->csr_val, c.val, vb * h->nnz, cudaMemcpyDeviceToDevice, c.s));
+    }
+    // bin sizes from the histogram (bins: <=2, <=4, <=8, <=16, longer)
+    const int gs[5] = {2, 4, 8, 16, 32};
+    std::vector<int64_t> cnt(5, 0);
+    const int64_t n_short = n - c.n_long;
+    if (forced_g > 0) {
+        int b = 0;
+        while (gs[b] != forced_g) ++b;
+        cnt[b] = n_short;
+    } else {
+        const int32_t thr = c.threshold;
+        for (int l = 0; l < kHistCap; ++l) {
+            if (thr >= 0 && l > thr) continue;  // long row
+            const int b = l <= 2 ? 0 : l <= 4 ? 1 : l <= 8 ? 2 : l <= 16 ? 3 : 4;
+            cnt[b] += c.hist[l];
+        }
+        // the top bucket holds every row of kHistCap or more entries
+        if (thr < 0)
+            cnt[4] += c.hist[kHistCap];
+        else if (thr >= kHistCap)
+            cnt[4] += c.hist[kHistCap] - c.n_long;
+    }
+    int nonempty = 0;
+    for (int b = 0; b < 5; ++b) nonempty += cnt[b] > 0;
+    if (nonempty <= 1 && c.n_long == 0) {
+        for (int b = 0; b < 5; ++b)
+            if (cnt[b] > 0) h->bins.push_back(Bin{gs[b], cnt[b], 0});
+        h->bin_rows = nullptr;
+    } else {
+        SPMV_TRY(dev_alloc_n(h, &h->bin_rows, n));
+        std::vector<int64_t> start;
+        SPMV_TRY(partition_rows(c, 2, c.threshold, forced_g, h->bin_rows, start));
+        for (int b = 0; b < 5; ++b) {
+            const int64_t count = start[b + 1] - start[b];
+            if (count != cnt[b]) return set_error(SPMV_ERR_CUDA, "row-bin count mismatch");
+            if (count > 0) h->bins.push_back(Bin{gs[b], count, start[b]});
+        }
+        if (c.n_long > 0) {
+            if (start[7] - start[6] != c.n_long) return set_error(SPMV_ERR_CUDA, "long-row bin count mismatch");
+            SPMV_TRY(build_segment(c, h->bin_rows + start[6], c.n_long, 0, 1, 0));
+        }
+    }
+    for (const Bin &b : h->bins) h->kernels.push_back("csr_vector_g" + std::to_string(b.g));
+    return SPMV_OK;
+}
+
+// Padded slot count of SELL-32 in natural order (sigma = 1), for the AUTO choice.
+int probe_sigma1_slots(BuildCtx &c, int64_t *slots) {
+    const int64_t n = c.h->n;
+    const int64_t ns = ceil_div(n, 32);
+    int32_t *clip = nullptr, *len_pad = nullptr, *width = nullptr;
+    int64_t *sizes = nullptr, *sp = nullptr, *scan_tmp = nullptr;
+    SPMV_TRY(c.temp.get(&clip, n));
+    SPMV_TRY(c.temp.get(&len_pad, ns * 32));
+    SPMV_TRY(c.temp.get(&width, ns));
+    SPMV_TRY(c.temp.get(&sizes, ns));
+    SPMV_TRY(c.temp.get(&sp, ns + 1));
+    SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(ns)));
+    SPMV_TRY_CUDA(launch_clip_long(n, c.len, c.threshold, clip, c.s));
+    SPMV_TRY_CUDA(launch_gather_sorted(clip, nullptr, n, ns * 32, len_pad, nullptr, c.s));
+    SPMV_TRY_CUDA(launch_slice_widths(len_pad, ns, 32, width, sizes, c.s));
+    SPMV_TRY_CUDA(launch_exclusive_scan(sizes, ns, sp, scan_tmp, c.s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(slots, sp + ns, sizeof(int64_t), cudaMemcpyDeviceToHost, c.s));
+    return sync(c.s);
+}
+
+int32_t hyb_auto_width(const BuildCtx &c, int dtype, int64_t n, int32_t cap) {
+    // smallest K with (vb + 8) * #{len > K} <= ld * (vb + 4)
+    const int64_t vb = static_cast<int64_t>(value_bytes(dtype));
+    const int64_t ld = ceil_div(std::max<int64_t>(n, 1), 256) * 256;
+    int64_t longer = n;  // #{len > K} for K = -1
+    int32_t K = 0;
+    longer -= c.hist[0];
+    while (K < cap && K < kHistCap && (vb + 8) * longer > ld * (vb + 4)) {
+        ++K;
+        longer -= c.hist[K];
+    }
+    return std::min(K, cap);
+}
+
+int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
+    spmv_handle_t h = c.h;
+    const int64_t n = h->n, nnz = h->nnz;
+
+    SPMV_TRY(dev_alloc_n(h, &h->row_ptr, n + 1));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(h->row_ptr, c.row_ptr, sizeof(int32_t) * (n + 1), cudaMemcpyDeviceToDevice, c.s));
+
+    // a1: validate + lengths
+    int32_t *status = nullptr;
+    SPMV_TRY(c.temp.get(&c.len, n));
+    SPMV_TRY(c.temp.get(&status, 3));
+    SPMV_TRY_CUDA(cudaMemsetAsync(status, 0, sizeof(int32_t) * 3, c.s));
+    SPMV_TRY_CUDA(launch_validate(n, nnz, c.row_ptr, c.col, c.len, status, c.s));
+    int32_t st_host[3] = {0, 0, 0};
+    SPMV_TRY_CUDA(cudaMemcpyAsync(st_host, status, sizeof(st_host), cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY(sync(c.s));
+    if (st_host[0]) return set_error(SPMV_ERR_BAD_CSR, "row_ptr is not a valid CSR row pointer (row_ptr[0] != 0, "
+                                                       "decreasing entries, or row_ptr[n] != nnz)");
+    if (st_host[1]) return set_error(SPMV_ERR_BAD_CSR, "a column index lies outside [0, n)");
+    h->max_len = st_host[2];
+    h->mean_len = n ? static_cast<double>(nnz) / static_cast<double>(n) : 0.0;
+
+    // a2: parameters
+    int32_t thr = prm.long_row_threshold;
+    const int fmt_for_thr = (format == SPMV_FMT_AUTO) ? SPMV_FMT_SELL : format;
+    if (thr < 0) thr = default_threshold(fmt_for_thr, h->dtype);
+    if (prm.long_row_threshold == 0) thr = -1;  // 0 = never cut
+    if (format == SPMV_FMT_HYB) thr = -1;         // the spill takes every long tail
+    c.threshold = thr;
+
+    int64_t *hist_d = nullptr, *stats_d = nullptr;
+    SPMV_TRY(c.temp.get(&hist_d, kHistCap + 1));
+    SPMV_TRY(c.temp.get(&stats_d, 3));
+    SPMV_TRY_CUDA(launch_histogram(n, c.len, thr, hist_d, stats_d, c.s));
+    c.hist.assign(kHistCap + 1, 0);
+    int64_t stats[3] = {0, 0, 0};
+    SPMV_TRY_CUDA(cudaMemcpyAsync(c.hist.data(), hist_d, sizeof(int64_t) * (kHistCap + 1), cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(stats, stats_d, sizeof(stats), cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY(sync(c.s));
+    c.n_long = stats[0];
+    c.long_nnz = stats[1];
+    c.max_short = static_cast<int32_t>(stats[2]);
+    h->n_long_rows = c.n_long;
+    h->long_nnz = c.long_nnz;
+
+    int32_t C = prm.C > 0 ? prm.C : 32;
+    if (C < 32 || C > 1024 || (C & (C - 1)))
+        return set_error(SPMV_ERR_INVALID_ARG, "SELL slice height C must be a power of two in [32, 1024]");
+    int64_t sigma = prm.sigma > 0 ? prm.sigma : 1;
+
+    if (format == SPMV_FMT_AUTO) {
+        // natural-order SELL-32 when it pads little, else sorted windows of 256 rows,
+        // else one subwarp group per row
+        int64_t slots1 = 0;
+        SPMV_TRY(probe_sigma1_slots(c, &slots1));
+        const int64_t stored = nnz - c.long_nnz;
+        if (static_cast<double>(slots1) <= 1.10 * static_cast<double>(stored) + 32.0 * 64) {
+            format = SPMV_FMT_SELL;
+            C = 32;
+            sigma = 1;
+        } else {
+            format = SPMV_FMT_SELL;
+            C = 32;
+            sigma = 256;
+            int32_t *clip = nullptr;
+            SPMV_TRY(c.temp.get(&clip, n));
+            SPMV_TRY_CUDA(launch_clip_long(n, c.len, c.threshold, clip, c.s));
+            SPMV_TRY(plan_sliced(c, clip, C, sigma, 0, c.max_short));
+            const bool good = static_cast<double>(h->sliced.slots) <= 1.10 * static_cast<double>(stored) + 32.0 * 64;
+            release_sliced(h);
+            if (!good) {
+                format = SPMV_FMT_CSR_VECTOR;
+                thr = prm.long_row_threshold < 0 ? default_threshold(format, h->dtype) : thr;
+                if (thr != c.threshold) {
+                    c.threshold = thr;
+                    SPMV_TRY_CUDA(launch_histogram(n, c.len, thr, hist_d, stats_d, c.s));
+                    SPMV_TRY_CUDA(cudaMemcpyAsync(stats, stats_d, sizeof(stats), cudaMemcpyDeviceToHost, c.s));
+                    SPMV_TRY(sync(c.s));
+                    c.n_long = stats[0];
+                    c.long_nnz = stats[1];
+                    c.max_short = static_cast<int32_t>(stats[2]);
+                    h->n_long_rows = c.n_long;
+                    h->long_nnz = c.long_nnz;
+                }
+            }
+        }
+    }
+    h->format = format;
+    h->params = prm;
+    h->params.C = C;
+    h->params.sigma = sigma;
+    h->params.long_row_threshold = c.threshold;
+
+    switch (format) {
+        case SPMV_FMT_CSR_VECTOR: {
+            int32_t g = prm.subwarp > 0 ? prm.subwarp : 0;
+            if (g && g != 2 && g != 4 && g != 8 && g != 16 && g != 32)
+                return set_error(SPMV_ERR_INVALID_ARG, "subwarp must be 2, 4, 8, 16 or 32");
+            h->params.subwarp = g;
+            SPMV_TRY(build_csr_vector(c, g));
+            break;
+        }
+        case SPMV_FMT_ELL_R:
+            h->params.C = 32;
+            h->params.sigma = 1;
+            SPMV_TRY(build_sell_like(c, format, 32, 1));
+            break;
+        case SPMV_FMT_SELL:
+            SPMV_TRY(build_sell_like(c, format, C, sigma));
+            break;
+        case SPMV_FMT_HYB: {
+            const int32_t cap = default_threshold(SPMV_FMT_SELL, h->dtype);
+            int32_t K = prm.K >= 0 ? prm.K : hyb_auto_width(c, h->dtype, n, cap);
+            const int spill_csr = prm.spill_csr >= 0 ? (prm.spill_csr ? 1 : 0) : 1;
+            h->params.K = K;
+            h->params.spill_csr = spill_csr;
+            h->params.long_row_threshold = -1;
+            SPMV_TRY(build_hyb(c, K, spill_csr));
+            break;
+        }
+        default:
+            return set_error(SPMV_ERR_INVALID_ARG, "unknown format");
+    }
+    if (h->seg.kind == 1) h->kernels.push_back("merge_path");
+    if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
+    if (h->seg.kind != 0 && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
+    return sync(c.s);
+}
+
+void free_handle(spmv_handle_t h) {
+    if (!h) return;
+    for (void *p : h->allocations) cudaFree(p);
+    delete h;
+}
+
+// ---------------------------------------------------------------------------
+// apply
+// ---------------------------------------------------------------------------
+struct Recorder {
+    std::vector<cudaEvent_t> ev;
+    int mark(cudaStream_t s) {
+        cudaEvent_t e;
+        SPMV_TRY_CUDA(cudaEventCreate(&e));
+        ev.push_back(e);
+        SPMV_TRY_CUDA(cudaEventRecord(e, s));
+        return SPMV_OK;
+    }
+    ~Recorder() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    }
+};
+
+int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *rec) {
+    if (rec) SPMV_TRY(rec->mark(s));
+    if (h->format == SPMV_FMT_CSR_VECTOR) {
+        for (const Bin &b : h->bins) {
+            SPMV_TRY_CUDA(launch_csr_vector(h->dtype, b.g, b.count, h->bin_rows ? h->bin_rows + b.offset : nullptr,
+                                            h->row_ptr, h->csr_col, h->csr_val, x, y, s));
+            if (rec) SPMV_TRY(rec->mark(s));
+        }
+    } else if (h->sliced.present) {
+        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, x, y, s));
+        if (rec) SPMV_TRY(rec->mark(s));
+    }
+    if (h->seg.kind != 0) {
+        SPMV_TRY_CUDA(launch_segmented(h->dtype, h->seg, x, y, s));
+        if (rec) SPMV_TRY(rec->mark(s));
+        if (h->seg.n_cta > 1) {
+            SPMV_TRY_CUDA(launch_carry_fixup(h->dtype, h->seg, y, s));
+            if (rec) SPMV_TRY(rec->mark(s));
+        }
+    }
+    return SPMV_OK;
+}
+
+int check_current_device(spmv_handle_t h) {
+    int dev = -1;
+    SPMV_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev != h->device)
+        return set_error(SPMV_ERR_INVALID_ARG, "the handle belongs to CUDA device " + std::to_string(h->device) +
+                                                   " but device " + std::to_string(dev) + " is current");
+    return SPMV_OK;
+}
+
+spmv_handle_t build_impl(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx, const void *vals,
+                         int dtype, int format, const spmv_format_params *params, cudaStream_t s) {
+    clear_error();
+    if (n < 0 || nnz < 0 || n >= (int64_t(1) << 31) || nnz >= (int64_t(1) << 31)) {
+        set_error(SPMV_ERR_INVALID_ARG, "n and nnz must lie in [0, 2^31)");
+        return nullptr;
+    }
+    if (dtype != SPMV_F64 && dtype != SPMV_F32) {
+        set_error(SPMV_ERR_INVALID_ARG, "dtype must be SPMV_F64 or SPMV_F32");
+        return nullptr;
+    }
+    if (format < SPMV_FMT_AUTO || format > SPMV_FMT_HYB) {
+        set_error(SPMV_ERR_INVALID_ARG, "unknown format");
+        return nullptr;
+    }
+    if (!row_ptr || (nnz > 0 && (!col_idx || !vals))) {
+        set_error(SPMV_ERR_INVALID_ARG, "NULL matrix array");
+        return nullptr;
+    }
+    if (check_device_pointer(row_ptr, "row_ptr") != SPMV_OK) return nullptr;
+    if (nnz > 0 && (check_device_pointer(col_idx, "col_idx") != SPMV_OK ||
+                    check_device_pointer(vals, "vals") != SPMV_OK))
+        return nullptr;
+    spmv_format_params prm;
+    spmv_default_params(&prm);
+    if (params) prm = *params;
+
+    spmv_handle_t h = new (std::nothrow) spmv_handle_s();
+    if (!h) {
+        set_error(SPMV_ERR_OOM, "host allocation of the handle failed");
+        return nullptr;
+    }
+    h->n = n;
+    h->nnz = nnz;
+    h->dtype = dtype;
+    h->requested_format = format;
+    if (cudaGetDevice(&h->device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        set_error(SPMV_ERR_CUDA, "no CUDA device");
+        delete h;
+        return nullptr;
+    }
+    int st;
+    {
+        BuildCtx c{h, s, row_ptr, col_idx, vals};
+        st = build_all(c, format, prm);
+        if (st == SPMV_OK) st = sync(s);
+    }
+    if (st != SPMV_OK) {
+        const int keep = g_last_error;
+        const std::string msg = g_last_msg;
+        cudaStreamSynchronize(s);
+        free_handle(h);
+        set_error(keep != SPMV_OK ? keep : st, msg);
+        return nullptr;
+    }
+    return h;
+}
+
+void append(std::string &out, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+void append(std::string &out, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    out += buf;
+}
+
+}  // namespace
+}  // namespace spmv
+
+using namespace spmv;
+
+extern "C" {
+
+int spmv_default_params(spmv_format_params *p) {
+    if (!p) return set_error(SPMV_ERR_INVALID_ARG, "NULL params");
+    p->C = -1;
+    p->sigma = -1;
+    p->K = -1;
+    p->spill_csr = -1;
+    p->long_row_threshold = -1;
+    p->subwarp = -1;
+    return SPMV_OK;
+}
+
+spmv_handle_t spmv_build_from_csr(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
+                                  const void *vals, int dtype, int format) {
+    return build_impl(n, nnz, row_ptr, col_idx, vals, dtype, format, nullptr, nullptr);
+}
+
+spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
+                                     const void *vals, int dtype, int format, const spmv_format_params *params,
+                                     void *stream) {
+    return build_impl(n, nnz, row_ptr, col_idx, vals, dtype, format, params, static_cast<cudaStream_t>(stream));
+}
+
+int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (h->n == 0) return SPMV_OK;
+    if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    SPMV_TRY(check_current_device(h));
+    return enqueue(h, x, y, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (h->n == 0) return SPMV_OK;
+    if (!x_host || !y_host) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    SPMV_TRY(check_current_device(h));
+    const size_t bytes = static_cast<size_t>(h->n) * value_bytes(h->dtype);
+    if (!h->x_stage) SPMV_TRY(dev_alloc(h, &h->x_stage, bytes));
+    if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    SPMV_TRY_CUDA(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
+    SPMV_TRY(enqueue(h, h->x_stage, h->y_stage, s, nullptr));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
+int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, float *kernel_ms, int cap) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (h->n == 0) return 0;
+    if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    SPMV_TRY(check_current_device(h));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Recorder rec;
+    SPMV_TRY(enqueue(h, x, y, s, &rec));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    const int k = static_cast<int>(rec.ev.size()) - 1;
+    for (int i = 0; i < k && i < cap; ++i) {
+        float ms = 0.f;
+        SPMV_TRY_CUDA(cudaEventElapsedTime(&ms, rec.ev[i], rec.ev[i + 1]));
+        if (kernel_ms) kernel_ms[i] = ms;
+    }
+    return k;
+}
+
+void spmv_destroy(spmv_handle_t h) { free_handle(h); }
+
+int spmv_last_error(void) { return g_last_error; }
+const char *spmv_last_error_message(void) { return g_last_msg; }
+
+const char *spmv_error_string(int status) {
+    switch (status) {
+        case SPMV_OK: return "success";
+        case SPMV_ERR_INVALID_ARG: return "invalid argument";
+        case SPMV_ERR_BAD_CSR: return "malformed CSR matrix";
+        case SPMV_ERR_CUDA: return "CUDA runtime error";
+        case SPMV_ERR_OOM: return "out of device memory";
+        case SPMV_ERR_TOO_LARGE: return "layout too large";
+        case SPMV_ERR_UNSUPPORTED: return "unsupported parameter combination";
+        case SPMV_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int spmv_to_csr(spmv_handle_t h, int32_t *row_ptr, int32_t *col_idx, void *vals, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (!row_ptr || (h->nnz > 0 && (!col_idx || !vals))) return set_error(SPMV_ERR_INVALID_ARG, "NULL output array");
+    SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_device_pointer(row_ptr, "row_ptr"));
+    if (h->nnz > 0) {
+        SPMV_TRY(check_device_pointer(col_idx, "col_idx"));
+        SPMV_TRY(check_device_pointer(vals, "vals"));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t vb = value_bytes(h->dtype);
+    SPMV_TRY_CUDA(cudaMemcpyAsync(row_ptr, h->row_ptr, sizeof(int32_t) * (h->n + 1), cudaMemcpyDeviceToDevice, s));
+    if (h->format == SPMV_FMT_CSR_VECTOR) {
+        if (h->nnz > 0) {
+            SPMV_TRY_CUDA(cudaMemcpyAsync(col_idx, h->csr_col, sizeof(int32_t) * h->nnz, cudaMemcpyDeviceToDevice, s));
+            SPMV_TRY_CUDA(cudaMemcpyAsync(vals, h->csr_val, vb * h->nnz, cudaMemcpyDeviceToDevice, s));
+        }
+    } else {
+        SPMV_TRY_CUDA(launch_sliced_to_csr(h->dtype, h->n, h->sliced, h->row_ptr, col_idx, vals, s));
+        SPMV_TRY_CUDA(launch_segment_to_csr(h->dtype, h->seg, h->row_ptr, col_idx, vals, s));
+    }
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
+int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (!h->sliced.present) return set_error(SPMV_ERR_UNSUPPORTED, "the handle has no sliced part");
+    SPMV_TRY(check_current_device(h));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (perm && h->n > 0) {
+        SPMV_TRY(check_device_pointer(perm, "perm"));
+        if (h->sliced.perm) {
+            SPMV_TRY_CUDA(cudaMemcpyAsync(perm, h->sliced.perm, sizeof(int32_t) * h->n, cudaMemcpyDeviceToDevice, s));
+        } else {
+            std::vector<int32_t> iota(static_cast<size_t>(h->n));
+            for (int64_t i = 0; i < h->n; ++i) iota[i] = static_cast<int32_t>(i);
+            SPMV_TRY_CUDA(cudaMemcpyAsync(perm, iota.data(), sizeof(int32_t) * h->n, cudaMemcpyHostToDevice, s));
+            SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+        }
+    }
+    if (slice_ptr) {
+        SPMV_TRY(check_device_pointer(slice_ptr, "slice_ptr"));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(slice_ptr, h->sliced.slice_ptr, sizeof(int64_t) * (h->sliced.n_slices + 1),
+                                      cudaMemcpyDeviceToDevice, s));
+    }
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
+int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
+    if (!h || !json || cap == 0) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle or buffer");
+    const int64_t vb = static_cast<int64_t>(value_bytes(h->dtype));
+    const Sliced &sl = h->sliced;
+    const Segmented &sg = h->seg;
+    std::string o = "{";
+    append(o, "\"format\":\"%s\",\"requested_format\":\"%s\",\"dtype\":\"%s\",", format_name(h->format),
+           format_name(h->requested_format), h->dtype == SPMV_F64 ? "f64" : "f32");
+    append(o, "\"n\":%lld,\"nnz\":%lld,\"max_len\":%d,\"mean_len\":%.6f,", (long long)h->n, (long long)h->nnz,
+           h->max_len, h->mean_len);
+    append(o, "\"C\":%d,\"sigma\":%lld,\"K\":%d,\"spill_csr\":%d,\"long_row_threshold\":%d,\"subwarp\":%d,",
+           h->params.C, (long long)h->params.sigma, h->params.K, h->params.spill_csr, h->params.long_row_threshold,
+           h->params.subwarp);
+    append(o, "\"sliced\":%s,\"n_slices\":%lld,\"slots\":%lld,\"padded_entries\":%lld,\"stored_entries\":%lld,"
+              "\"ld\":%lld,\"max_width\":%d,\"permuted\":%s,",
+           sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,
+           (long long)sl.stored_entries, (long long)sl.ld, sl.max_width, sl.perm ? "true" : "false");
+    append(o, "\"n_long_rows\":%lld,\"long_nnz\":%lld,", (long long)h->n_long_rows, (long long)h->long_nnz);
+    append(o, "\"segment\":\"%s\",\"segment_rows\":%lld,\"segment_nnz\":%lld,\"segment_ctas\":%lld,",
+           sg.kind == 0 ? "none" : sg.kind == 1 ? "csr_merge_path" : "coo", (long long)sg.n_rows, (long long)sg.nnz,
+           (long long)sg.n_cta);
+    o += "\"bins\":[";
+    for (size_t i = 0; i < h->bins.size(); ++i)
+        append(o, "%s[%d,%lld]", i ? "," : "", h->bins[i].g, (long long)h->bins[i].count);
+    o += "],\"kernels\":[";
+    for (size_t i = 0; i < h->kernels.size(); ++i) append(o, "%s\"%s\"", i ? "," : "", h->kernels[i].c_str());
+    o += "],";
+    // bytes one apply streams from the format (x counted once, y written once)
+    int64_t matrix_bytes = 0;
+    if (h->format == SPMV_FMT_CSR_VECTOR) {
+        int64_t rows_binned = 0;
+        for (const Bin &b : h->bins) rows_binned += b.count;
+        matrix_bytes += (h->nnz - h->long_nnz) * (vb + 4) + rows_binned * 8 + (h->bin_rows ? rows_binned * 4 : 0);
+    } else if (sl.present) {
+        matrix_bytes += sl.stored_entries * (vb + 4) + sl.n_pos * 4 + (sl.perm ? sl.n_pos * 4 : 0) + sl.n_slices * 8;
+    }
+    if (sg.kind == 1) matrix_bytes += sg.nnz * (vb + 4) + sg.n_rows * 8 + sg.n_cta * 12;
+    if (sg.kind == 2) matrix_bytes += sg.nnz * (vb + 8) + sg.n_cta * 12;
+    append(o, "\"format_bytes\":%lld,\"vector_bytes\":%lld}", (long long)matrix_bytes, (long long)(2 * h->n * vb));
+    std::snprintf(json, cap, "%s", o.c_str());
+    if (o.size() + 1 > cap) return set_error(SPMV_ERR_INVALID_ARG, "describe buffer too small");
+    return SPMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+// Internal declarations of the sm_103a SpMV library: handle layout, launch
+// constants and the host-side launchers of the build and apply kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "spmv.h"
+
+namespace spmv {
+
+// ----------------------------------------------------------------------------
+// launch constants
+// ----------------------------------------------------------------------------
+constexpr int kBlock = 256;                 // generic 1-D kernels
+constexpr int kSellBlock = 256;             // sliced apply
+constexpr int kMergeThreads = 256;          // merge-path / COO segmented pass
+constexpr int kMergeIpt = 8;                // path items per thread
+constexpr int kMergeItems = kMergeThreads * kMergeIpt;
+constexpr int kHistCap = 4096;              // row-length histogram: buckets 0..kHistCap-1, last = ">= kHistCap"
+constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows are sorted in one CTA
+
+// ----------------------------------------------------------------------------
+// format parts
+// ----------------------------------------------------------------------------
+
+// Sliced column-major storage: SELL-C-sigma, ELLPACK-R, or the ELL part of HYB.
+// Sorted position p lives in slice s = p >> log2C at row r = p & cmask of the
+// slice; its j-th stored entry sits at slot slice_ptr[s] + j * stride + r.
+// SELL: stride = C.  ELL (one slice): log2C = 31, cmask = 0x7fffffff, stride = ld.
+struct Sliced {
+    bool present = false;
+    int64_t n_pos = 0;        // positions: n rounded up to C (SELL) or to ld (ELL)
+    int log2C = 0;
+    uint32_t cmask = 0;
+    int64_t stride = 0;
+    int32_t C = 0;
+    int64_t sigma = 1;
+    int64_t ld = 0;
+    int64_t n_slices = 0;
+    int64_t slots = 0;           // allocated slot count (sum of C * width)
+    int64_t padded_entries = 0;  // sum over real rows of their slice width
+    int64_t stored_entries = 0;  // entries actually held (sum of len)
+    int32_t max_width = 0;
+    int64_t *slice_ptr = nullptr;  // [n_slices + 1]
+    int32_t *width = nullptr;      // [n_slices]
+    int32_t *len = nullptr;        // [n_pos] entries stored at each position
+    int32_t *perm = nullptr;       // [n_pos] original row (-1 = padding); nullptr = identity
+    int32_t *col = nullptr;        // [slots]
+    void *val = nullptr;           // [slots]
+};
+
+// Rows handled by the segmented pass: the long rows taken out of a format, or
+// the HYB spill.  kind 1 = compact CSR walked by merge-path, kind 2 = COO.
+struct Segmented {
+    int kind = 0;
+    int64_t n_rows = 0;
+    int64_t nnz = 0;
+    int32_t *rows = nullptr;     // [n_rows] original row of each compact row (increasing)
+    int32_t *ptr = nullptr;      // [n_rows + 1] compact row pointer
+    int32_t *coo_row = nullptr;  // [nnz] original row of every entry (kind 2)
+    int32_t *col = nullptr;      // [nnz]
+    void *val = nullptr;         // [nnz]
+    int64_t n_cta = 0;
+    int32_t *carry_row = nullptr;  // [n_cta] row left open at the end of each CTA (-1 = none)
+    double *carry_val = nullptr;   // [n_cta] its partial sum
+    int accumulate = 1;            // 1: add into y (y written before), 0: write y
+    int32_t dst_offset = 0;        // in-row position of the first held entry (K for the spill)
+};
+
+// One CSR-vector launch: g lanes per row over rows bin_rows[offset, offset + count),
+// or rows [0, count) when the handle has no bin list.
+struct Bin {
+    int g = 0;
+    int64_t count = 0;
+    int64_t offset = 0;
+};
+
+}  // namespace spmv
+
+struct spmv_handle_s {
+    int64_t n = 0;
+    int64_t nnz = 0;
+    int dtype = SPMV_F64;
+    int format = SPMV_FMT_AUTO;
+    int requested_format = SPMV_FMT_AUTO;
+    spmv_format_params params{};
+    int device = 0;
+    int32_t max_len = 0;
+    double mean_len = 0.0;
+
+    // the input CSR (row pointer always kept; columns/values for CSR-vector)
+    int32_t *row_ptr = nullptr;
+    int32_t *csr_col = nullptr;
+    void *csr_val = nullptr;
+
+    spmv::Sliced sliced;
+    spmv::Segmented seg;
+    std::vector<spmv::Bin> bins;
+    int32_t *bin_rows = nullptr;
+
+    int64_t n_long_rows = 0;
+    int64_t long_nnz = 0;
+    int32_t K = 0;
+
+    // spmv_apply_host staging
+    void *x_stage = nullptr;
+    void *y_stage = nullptr;
+
+    std::vector<std::string> kernels;  // launch sequence of one apply
+    std::vector<void *> allocations;
+};
+
+namespace spmv {
+
+// ----------------------------------------------------------------------------
+// error state (thread-local) -- api.cu
+// ----------------------------------------------------------------------------
+int set_error(int status, const std::string &msg);
+int set_cuda_error(cudaError_t err, const char *what);
+
+#define SPMV_TRY_CUDA(expr)                                              \
+    do {                                                                 \
+        cudaError_t spmv_err__ = (expr);                                 \
+        if (spmv_err__ != cudaSuccess) return ::spmv::set_cuda_error(spmv_err__, #expr); \
+    } while (0)
+
+#define SPMV_TRY(expr)                      \
+    do {                                    \
+        int spmv_st__ = (expr);             \
+        if (spmv_st__ != SPMV_OK) return spmv_st__; \
+    } while (0)
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t value_bytes(int dtype) { return dtype == SPMV_F64 ? 8 : 4; }
+
+// ----------------------------------------------------------------------------
+// build launchers -- build.cu.  All enqueue on `s`; none synchronises.
+// ----------------------------------------------------------------------------
+
+// status[0]: bad row_ptr flag, status[1]: bad column flag, status[2]: max row length.
+cudaError_t launch_validate(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
+                            int32_t *len, int32_t *status, cudaStream_t s);
+// hist[kHistCap + 1] of min(len, kHistCap); stats[0] = rows with len > threshold,
+// stats[1] = their entries, stats[2] = longest row with len <= threshold.
+cudaError_t launch_histogram(int64_t n, const int32_t *len, int32_t threshold, int64_t *hist,
+                             int64_t *stats, cudaStream_t s);
+// out[i] = 0 for rows longer than threshold (threshold < 0: no cut), else len[i].
+cudaError_t launch_clip_long(int64_t n, const int32_t *len, int32_t threshold, int32_t *out,
+                             cudaStream_t s);
+cudaError_t launch_min_len(int64_t n, const int32_t *len, int32_t K, int32_t *out, cudaStream_t s);
+
+// Exclusive scan of int64 values: out[i] = sum in[0..i), out has n+1 entries.
+// Needs scan_temp_elems(n) int64 of temporary storage.
+int64_t scan_temp_elems(int64_t n);
+cudaError_t launch_exclusive_scan(const int64_t *in, int64_t n, int64_t *out, int64_t *temp,
+                                  cudaStream_t s);
+
+// Stable partition / radix sort machinery (8-bit digits).
+int64_t radix_blocks(int64_t n);
+// One stable counting pass on digit (key >> shift) & 255.  counts/offsets need
+// 256 * radix_blocks(n) + 1 int64; scan_temp needs scan_temp_elems(256*blocks).
+cudaError_t launch_radix_pass(const uint32_t *keys_in, const int32_t *vals_in, int64_t n, int shift,
+                              uint32_t *keys_out, int32_t *vals_out, int64_t *counts,
+                              int64_t *offsets, int64_t *scan_temp, cudaStream_t s);
+
+// SELL ordering.  Window sort for sigma <= kWindowSortMax.
+cudaError_t launch_window_sort(const int32_t *len, int64_t n, int64_t sigma, int32_t *perm,
+                               cudaStream_t s);
+// key[i] = (i / sigma) << len_bits | (max_len - len[i]); val[i] = i.
+cudaError_t launch_sort_keys(const int32_t *len, int64_t n, int64_t sigma, int len_bits,
+                             int32_t max_len, uint32_t *keys, int32_t *vals, cudaStream_t s);
+// len_sorted[p] = len[perm[p]] for p < n, 0 beyond; perm_out[p] = perm[p] or -1.
+cudaError_t launch_gather_sorted(const int32_t *len, const int32_t *perm, int64_t n, int64_t n_pos,
+                                 int32_t *len_sorted, int32_t *perm_out, cudaStream_t s);
+// width[s] = max len_sorted over the slice; size[s] = C * width[s].
+cudaError_t launch_slice_widths(const int32_t *len_sorted, int64_t n_slices, int32_t C,
+                                int32_t *width, int64_t *size, cudaStream_t s);
+// Slot fill from CSR (values of `dtype`), padding slots get column 0 / value 0.
+cudaError_t launch_fill_sliced(int dtype, const Sliced &sl, const int32_t *row_ptr,
+                               const int32_t *col_in, const void *val_in, cudaStream_t s);
+
+// bucket[i] = pred(len[i]) for partitions.
+// mode 0: long rows (len > a); mode 1: HYB spill rows (len > a);
+// mode 2: CSR-vector bin id (6 = long row, beyond a) for len.
+cudaError_t launch_bucket_keys(int64_t n, const int32_t *len, int mode, int32_t a, int32_t forced_g,
+                               uint32_t *keys, int32_t *vals, cudaStream_t s);
+// size[i] = len[rows[i]] - offset
+cudaError_t launch_compact_sizes(int64_t m, const int32_t *rows, const int32_t *len, int32_t offset,
+                                 int64_t *size, cudaStream_t s);
+cudaError_t launch_int64_to_int32(const int64_t *in, int64_t n, int32_t *out, cudaStream_t s);
+// Copy entries [row_ptr[r] + offset, row_ptr[r+1]) of each listed row into compact arrays.
+cudaError_t launch_compact_copy(int dtype, int64_t m, const int32_t *rows, const int32_t *row_ptr,
+                                int32_t offset, const int32_t *col_in, const void *val_in,
+                                const int64_t *cptr, int32_t *col_out, void *val_out,
+                                int32_t *coo_row, cudaStream_t s);
+
+// to_csr
+cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const int32_t *out_ptr,
+                                 int32_t *out_col, void *out_val, cudaStream_t s);
+cudaError_t launch_segment_to_csr(int dtype, const Segmented &sg, const int32_t *out_ptr,
+                                  int32_t *out_col, void *out_val, cudaStream_t s);
+
+// ----------------------------------------------------------------------------
+// apply launchers -- apply.cu
+// ----------------------------------------------------------------------------
+cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y,
+                              cudaStream_t s);
+cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *rows,
+                              const int32_t *row_ptr, const int32_t *col, const void *val,
+                              const void *x, void *y, cudaStream_t s);
+cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
+cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
+int64_t merge_ctas(int64_t n_rows, int64_t nnz);
+int64_t coo_ctas(int64_t nnz);
+
+}  // namespace spmv

@@ -1,0 +1,103 @@
+"""The C library builds, loads without a GPU, and exports every symbol include/spmv.h declares.
+
+No compute call is made here: these run on machines without a GPU.
+"""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spmv.h")
+PKG = os.path.join(ROOT, "sparse_matrix_vector_csr_gb300")
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from sparse_matrix_vector_csr_gb300 import _build
+
+    return _build.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SPMV_API\s+[\w\s\*]*?\b(spmv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("spmv_build_from_csr", "spmv_apply", "spmv_destroy"):
+        assert required in names
+    assert len(names) >= 13
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_binding_covers_every_declared_symbol(libpath):
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    assert sorted(spmv._abi.EXPORTS) == declared_functions()
+    for name in declared_functions():
+        assert callable(getattr(spmv, name))
+
+
+def test_exports_are_only_the_c_abi(libpath):
+    out = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True).stdout
+    text_syms = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(declared_functions()) <= text_syms
+    assert all(s.startswith("spmv_") for s in text_syms), sorted(s for s in text_syms if not s.startswith("spmv_"))
+
+
+def test_host_only_calls_without_gpu(libpath):
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    assert spmv.spmv_error_string(0) == "success"
+    assert spmv.spmv_error_string(-2) == "malformed CSR matrix"
+    p = spmv.spmv_default_params()
+    assert (p.C, p.sigma, p.K, p.spill_csr, p.long_row_threshold, p.subwarp) == (-1, -1, -1, -1, -1, -1)
+    # a NULL handle is rejected before any CUDA call
+    with pytest.raises(spmv.SpmvError):
+        spmv.spmv_apply(None, None, None, 0)
+    assert spmv.spmv_last_error() == -1
+    spmv.spmv_destroy(None)
+
+
+def test_missing_library_fails_loudly(libpath):
+    with tempfile.TemporaryDirectory() as d:
+        dst = os.path.join(d, "sparse_matrix_vector_csr_gb300")
+        shutil.copytree(PKG, dst, ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__"))
+        code = "import sparse_matrix_vector_csr_gb300"
+        res = subprocess.run([sys.executable, "-c", code], cwd=d, capture_output=True, text=True)
+        assert res.returncode != 0 and "ImportError" in res.stderr
+
+
+def _imports(path):
+    mods = set()
+    for dirpath, _, files in os.walk(path):
+        for f in files:
+            if f.endswith(".py"):
+                src = open(os.path.join(dirpath, f)).read()
+                mods |= set(re.findall(r"^\s*(?:from|import)\s+([\w\.]+)", src, re.M))
+    return mods
+
+
+def test_product_and_oracle_share_nothing():
+    prod = _imports(PKG)
+    assert not any(m.split(".")[0] in ("oracle", "workloads") for m in prod), prod
+    orc = _imports(os.path.join(ROOT, "oracle"))
+    assert not any(m.split(".")[0] == "sparse_matrix_vector_csr_gb300" for m in orc), orc
+    gen = _imports(os.path.join(ROOT, "workloads"))
+    assert not any(m.split(".")[0] in ("oracle", "sparse_matrix_vector_csr_gb300") for m in gen), gen
+    # no C/CUDA source is shared either
+    csrc = os.path.join(PKG, "csrc")
+    for f in os.listdir(csrc):
+        assert "oracle" not in open(os.path.join(csrc, f)).read().lower()

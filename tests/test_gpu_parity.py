@@ -1,0 +1,315 @@
+"""GPU parity: the CUDA path against the oracle, element by element, through the C ABI.
+
+Acceptance rule (per row i):  |y_gpu - y_ref| <= tau * sum_j |a_ij x_j| with
+tau = 1e-12 for float64 and 1e-5 for float32, y_ref the long double oracle value;
+bit-exact equality on integer-valued matrices and vectors, where every partial
+sum is an exactly representable integer whatever the summation order.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import layout
+from tests.gpu_util import (FORMAT_CASES, assert_parity, assert_roundtrip, build, case_id, run,
+                            torch_cuda)
+from workloads import CSR, laplacian_2d, make_workload, random_csr, integer_x, uniform_x
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["lap2d_small", "lap3d_small", "hmep_small", "powerlaw_small", "uniform16_small"]
+
+_cache = {}
+
+
+def small(name, dtype=None):
+    key = (name, dtype)
+    if key not in _cache:
+        csr, x = make_workload(name, dtype=dtype)
+        _cache[key] = (csr, x, oracle.spmv(csr, x))
+    return _cache[key]
+
+
+@pytest.mark.parametrize("case", FORMAT_CASES, ids=case_id)
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workloads_all_formats(name, case):
+    fmt, params = case
+    csr, x, ref = small(name)
+    with build(csr, fmt, **params) as A:
+        y = run(A, x)
+        assert_parity(y, ref, csr.dtype, label=f"{name}/{case_id(case)}")
+        assert_roundtrip(A, csr, label=f"{name}/{case_id(case)}")
+
+
+@pytest.mark.parametrize("case", [c for c in FORMAT_CASES if c[0] in ("auto", "csr_vector", "sell", "hyb")],
+                         ids=case_id)
+@pytest.mark.parametrize("name", ["lap3d_small", "powerlaw_small", "hmep_small"])
+def test_small_workloads_float32(name, case):
+    fmt, params = case
+    csr, x, ref = small(name, np.float32)
+    with build(csr, fmt, **params) as A:
+        y = run(A, x)
+        assert_parity(y, ref, np.float32, label=f"{name}/f32/{case_id(case)}")
+        assert_roundtrip(A, csr)
+
+
+@pytest.mark.parametrize("case", FORMAT_CASES, ids=case_id)
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_integer_inputs_bit_exact(case, dtype):
+    fmt, params = case
+    A_csr = laplacian_2d(256, 256, dtype=dtype)
+    x = integer_x(A_csr.n, dtype=dtype)
+    ref = oracle.spmv(A_csr, x)
+    with build(A_csr, fmt, **params) as A:
+        assert_parity(run(A, x), ref, dtype, exact=True, label=f"lap2d_256 integer x/{case_id(case)}")
+    R = random_csr(3000, 0.004, seed=7, dtype=dtype, integer_values=True, duplicates=True, unsorted=True,
+                   empty_row_fraction=0.2, full_rows=2)
+    xr = integer_x(R.n, seed=3, dtype=dtype)
+    ref = oracle.spmv(R, xr)
+    with build(R, fmt, **params) as A:
+        assert_parity(run(A, xr), ref, dtype, exact=True, label=f"random integer/{case_id(case)}")
+        assert_roundtrip(A, R)
+
+
+@pytest.mark.parametrize("case", FORMAT_CASES, ids=case_id)
+def test_duplicates_unsorted_empty_rows(case):
+    fmt, params = case
+    for seed in (1, 2):
+        csr = random_csr(2500, 0.01, seed=seed, duplicates=True, unsorted=True, empty_row_fraction=0.3, full_rows=1)
+        x = uniform_x(csr.n, seed=seed)
+        with build(csr, fmt, **params) as A:
+            assert_parity(run(A, x), oracle.spmv(csr, x), np.float64, label=case_id(case))
+            assert_roundtrip(A, csr)
+
+
+# --------------------------------------------------------------------------- #
+# degenerate and extreme shapes
+# --------------------------------------------------------------------------- #
+
+
+def _csr_from_rows(n, rows, dtype=np.float64, seed=0, integer=False):
+    rng = np.random.default_rng(seed)
+    lens = np.array([len(r) for r in rows], dtype=np.int64)
+    rp = np.zeros(n + 1, np.int64)
+    np.cumsum(lens, out=rp[1:])
+    col = np.concatenate([np.asarray(r, np.int64) for r in rows]).astype(np.int32) if lens.sum() else np.zeros(0, np.int32)
+    vals = (rng.integers(-8, 9, col.size) if integer else rng.standard_normal(col.size)).astype(dtype)
+    return CSR(n, rp.astype(np.int32), col, vals)
+
+
+@pytest.mark.parametrize("case", FORMAT_CASES, ids=case_id)
+def test_all_rows_empty(case):
+    fmt, params = case
+    n = 1000
+    csr = CSR(n, np.zeros(n + 1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float64))
+    with build(csr, fmt, **params) as A:
+        y = run(A, uniform_x(n))
+        assert np.all(y == 0) and not np.any(np.signbit(y))
+
+
+def test_zero_order_matrix():
+    torch = torch_cuda()
+    csr = CSR(0, np.zeros(1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float64))
+    with build(csr, "auto") as A:
+        x = torch.zeros(0, dtype=torch.float64, device="cuda")
+        A.apply(x, torch.zeros(0, dtype=torch.float64, device="cuda"))
+        assert A.describe()["n"] == 0
+
+
+@pytest.mark.parametrize("fmt", ["auto", "csr_vector", "sell", "hyb"])
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_single_row_of_a_million(fmt, dtype):
+    """One row with 10^6 entries spread over several hundred merge-path CTAs."""
+    n = 1_000_000
+    row_ptr = np.full(n + 1, n, dtype=np.int32)
+    row_ptr[0] = 0
+    rng = np.random.default_rng(5)
+    for integer in (True, False):
+        vals = (rng.integers(-8, 9, n) if integer else rng.standard_normal(n)).astype(dtype)
+        csr = CSR(n, row_ptr, np.arange(n, dtype=np.int32), vals)
+        x = integer_x(n, dtype=dtype) if integer else uniform_x(n, dtype=dtype)
+        ref = oracle.spmv(csr, x, rows=np.arange(0, n, 997))
+        with build(csr, fmt) as A:
+            y = run(A, x)
+            d = A.describe()
+            assert d["segment"] != "none" and d["segment_ctas"] > 400
+            assert_parity(y[::997], ref, dtype, exact=integer, label=f"{fmt} integer={integer}")
+
+
+@pytest.mark.parametrize("case", FORMAT_CASES, ids=case_id)
+def test_alternating_empty_and_long_rows(case):
+    fmt, params = case
+    n = 20000
+    rng = np.random.default_rng(3)
+    rows = [np.sort(rng.choice(n, 5000, replace=False)) if i % 2 == 0 and i < 40 else
+            (np.sort(rng.choice(n, 3, replace=False)) if i % 3 == 0 else []) for i in range(n)]
+    for integer in (True, False):
+        csr = _csr_from_rows(n, rows, seed=4, integer=integer)
+        x = integer_x(n) if integer else uniform_x(n)
+        with build(csr, fmt, **params) as A:
+            assert_parity(run(A, x), oracle.spmv(csr, x), np.float64, exact=integer, label=case_id(case))
+            assert_roundtrip(A, csr)
+
+
+@pytest.mark.parametrize("case", FORMAT_CASES, ids=case_id)
+def test_padding_never_touches_x(case):
+    """x is +Inf and NaN at columns no stored entry uses; padding must not pick them up."""
+    fmt, params = case
+    n = 4096
+    rng = np.random.default_rng(9)
+    rows = [np.sort(rng.choice(np.arange(2, n), rng.integers(0, 40), replace=False)) for _ in range(n)]
+    csr = _csr_from_rows(n, rows, seed=2)
+    x = uniform_x(n)
+    x[0], x[1] = np.inf, np.nan
+    with build(csr, fmt, **params) as A:
+        y = run(A, x)
+        assert np.all(np.isfinite(y))
+        assert_parity(y, oracle.spmv(csr, x), np.float64, label=case_id(case))
+
+
+# --------------------------------------------------------------------------- #
+# layouts against the oracle's layout definitions (bit-exact integer work)
+# --------------------------------------------------------------------------- #
+
+
+@pytest.mark.parametrize("C,sigma", [(32, 1), (32, 256), (64, 1), (64, 2048), (32, 4096), (32, 1 << 30)])
+@pytest.mark.parametrize("name", ["powerlaw_small", "hmep_small", "lap3d_small"])
+def test_sell_layout_matches_definition(name, C, sigma):
+    csr, _, _ = small(name)
+    lens = layout.row_lengths(csr.row_ptr)
+    with build(csr, "sell", C=C, sigma=sigma) as A:
+        d = A.describe()
+        thr = d["long_row_threshold"]
+        exp = layout.sell_layout(lens, C, min(sigma, csr.n), exclude=layout.long_rows(lens, thr))
+        perm, sp = A.layout()
+        assert np.array_equal(perm.cpu().numpy(), exp["perm"])
+        assert np.array_equal(sp.cpu().numpy(), exp["slice_ptr"])
+        assert d["padded_entries"] == exp["padded_entries"]
+        assert d["slots"] == exp["allocated_slots"]
+        assert d["n_long_rows"] == layout.long_rows(lens, thr).size
+
+
+@pytest.mark.parametrize("N,b_r", [(1024, 32), (4096, 32), (4096, 64), (777, 64)])
+def test_pjds_storage_of_one_full_row(N, b_r):
+    """One full row + one entry per other row: pJDS stores (b_r + 1) N - b_r, ELLPACK N^2."""
+    rows = [[i % N] for i in range(N)]
+    rows[N // 3] = list(range(N))
+    csr = _csr_from_rows(N, rows)
+    with build(csr, "sell", C=b_r, sigma=1 << 30, long_row_threshold=0) as A:
+        assert A.describe()["padded_entries"] == (b_r + 1) * N - b_r
+    with build(csr, "ell_r", long_row_threshold=0) as A:
+        d = A.describe()
+        assert d["padded_entries"] == N * N
+        assert d["ld"] % 32 == 0 and d["ld"] >= N
+
+
+@pytest.mark.parametrize("name", ["powerlaw_small", "hmep_small", "uniform16_small"])
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_hyb_split_matches_rule(name, dtype):
+    csr, x, _ = small(name)
+    csr = csr.astype(dtype)
+    x = x.astype(dtype)
+    lens = layout.row_lengths(csr.row_ptr)
+    vb = np.dtype(dtype).itemsize
+    ld = layout.ell_leading_dim(csr.n)
+    cap = 4096 if dtype == np.float64 else 128
+    K = layout.hyb_width(lens, vb, ld, k_cap=cap)
+    split = layout.hyb_split(lens, K)
+    with build(csr, "hyb") as A:
+        d = A.describe()
+        assert d["K"] == K and d["ld"] == ld and d["ld"] % 256 == 0
+        assert d["segment_nnz"] == split["spill_nnz"]
+        assert d["segment_rows"] == split["spill_rows"].size
+        assert_parity(run(A, x), oracle.spmv(csr, x), dtype)
+
+
+def test_csr_vector_bins():
+    csr, _, _ = small("powerlaw_small")
+    lens = layout.row_lengths(csr.row_ptr)
+    with build(csr, "csr_vector") as A:
+        d = A.describe()
+        thr = d["long_row_threshold"]
+        short = lens[lens <= thr]
+        expect = {2: (short <= 2).sum(), 4: ((short > 2) & (short <= 4)).sum(), 8: ((short > 4) & (short <= 8)).sum(),
+                  16: ((short > 8) & (short <= 16)).sum(), 32: (short > 16).sum()}
+        got = {g: c for g, c in d["bins"]}
+        assert got == {g: int(c) for g, c in expect.items() if c}
+        assert d["n_long_rows"] == int((lens > thr).sum())
+
+
+# --------------------------------------------------------------------------- #
+# API behaviour
+# --------------------------------------------------------------------------- #
+
+
+def test_bad_csr_is_rejected():
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    good = random_csr(100, 0.05, seed=1)
+    bad_cases = []
+    c = good.col_idx.copy()
+    c[3] = 100
+    bad_cases.append(CSR(100, good.row_ptr, c, good.vals))
+    r = good.row_ptr.copy()
+    r[50], r[51] = r[51], r[50]
+    if r[50] != r[51]:
+        bad_cases.append(CSR(100, r, good.col_idx, good.vals))
+    r2 = good.row_ptr.copy()
+    r2[0] = 1
+    bad_cases.append(CSR(100, r2, good.col_idx, good.vals))
+    for bad in bad_cases:
+        with pytest.raises(spmv.SpmvError) as ei:
+            build(bad, "sell")
+        assert ei.value.status == -2
+    # the library still works afterwards
+    x = uniform_x(100)
+    with build(good, "sell") as A:
+        assert_parity(run(A, x), oracle.spmv(good, x), np.float64)
+
+
+def test_host_pointers_are_rejected():
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    csr = random_csr(50, 0.1, seed=1)
+    with pytest.raises(spmv.SpmvError) as ei:
+        spmv.spmv_build_from_csr(csr.n, csr.nnz, csr.row_ptr, csr.col_idx, csr.vals, 0, "sell")
+    assert ei.value.status == -1
+
+
+def test_too_large_layout_is_refused():
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    n = 3_000_000
+    rows_ptr = np.zeros(n + 1, np.int64)
+    rows_ptr[1:] = n  # row 0 is full, the rest empty
+    csr = CSR(n, rows_ptr.astype(np.int32), np.arange(n, dtype=np.int32), np.ones(n))
+    with pytest.raises(spmv.SpmvError) as ei:
+        build(csr, "ell_r", long_row_threshold=0)  # 3e6 x 3e6 rectangle
+    assert ei.value.status == -5
+
+
+def test_apply_on_a_side_stream_and_host_path():
+    torch = torch_cuda()
+    csr, x, ref = small("hmep_small")
+    with build(csr, "auto") as A:
+        s = torch.cuda.Stream()
+        xd = torch.from_numpy(x).cuda()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            y = torch.empty_like(xd)
+            A.apply(xd, y)
+        s.synchronize()
+        assert_parity(y.cpu().numpy(), ref, np.float64)
+        xh = torch.from_numpy(x).pin_memory().numpy()
+        yh = torch.empty(csr.n, dtype=torch.float64).pin_memory().numpy()
+        A.apply_host(xh, yh)
+        assert np.array_equal(yh, y.cpu().numpy())
+        times = A.apply_profiled(xd, y)
+        assert len(times) == len(A.describe()["kernels"]) and all(t > 0 for t in times)
+
+
+def test_repeated_applies_are_deterministic():
+    csr, x, _ = small("powerlaw_small")
+    with build(csr, "sell", sigma=256) as A:
+        y1 = run(A, x)
+        y2 = run(A, x)
+        assert np.array_equal(y1.view(np.uint64), y2.view(np.uint64))
