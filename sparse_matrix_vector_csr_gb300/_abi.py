@@ -50,7 +50,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build the CUDA library first "
-            "(python -m sparse_matrix_vector_csr_gb300._build)")
+            "(python sparse_matrix_vector_csr_gb300/_build.py)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i64, i32, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
     lib.spmv_default_params.argtypes = [ctypes.POINTER(FormatParams)]

@@ -1,9 +1,10 @@
 """Compile the CUDA library ``libspmv_gb300.so`` in-tree for sm_103a.
 
 Three translation units are compiled in parallel with nvcc and linked into a
-shared library inside this package directory.  Usage::
+shared library inside this package directory.  Run it as a script (importing
+the package itself needs the built library)::
 
-    python -m sparse_matrix_vector_csr_gb300._build
+    python sparse_matrix_vector_csr_gb300/_build.py
 """
 from __future__ import annotations
 

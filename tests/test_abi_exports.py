@@ -19,9 +19,9 @@ PKG = os.path.join(ROOT, "sparse_matrix_vector_csr_gb300")
 
 @pytest.fixture(scope="module")
 def libpath():
-    from sparse_matrix_vector_csr_gb300 import _build
+    import __graft_entry__
 
-    return _build.build()
+    return __graft_entry__._build_module().build()
 
 
 def declared_functions():
