@@ -1,0 +1,102 @@
+"""Host-side logic of bench.py, on the CPU: byte model, rank aggregation (gloo, world size 2),
+clock parsing, the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_effective_bytes_formula():
+    # 3D Laplacian 128^3 in fp64: nnz*(8+4) + (n+1)*4 + 2*n*8
+    n, nnz = 2_097_152, 14_581_760
+    assert bench.effective_bytes(n, nnz, 8) == nnz * 12 + (n + 1) * 4 + n * 16 == 216_924_164
+    assert bench.effective_bytes(0, 0, 4) == 4
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist = bench.init_dist(world, "gloo")
+    local_seconds = 1.0 + rank  # rank 1 is the slow one
+    bench.barrier(world)
+    mx = bench.reduce_max(local_seconds, world)
+    rate = bench.aggregate_rate(100.0, world, mx)
+    out.put((rank, mx, rate))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_gloo():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [2.0, 2.0]          # every rank sees the slowest time
+    assert [r[2] for r in res] == [100.0, 100.0]      # 2 ranks x 100 units / 2 s
+
+
+def test_clock_summary_parsing():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples = [(10.0, "1965, 2070, 800.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"),
+                 (10.1, "1980, 2070, 810.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active"),
+                 (99.0, "300, 2070, 80.0, 0x0, Not Active, Not Active, Not Active, Not Active")]
+    out = s.summary(9.9, 10.2)
+    assert out["sm_mhz"] == pytest.approx(1972.5) and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 2
+
+
+def test_traffic_is_null_when_kernel_changed(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    (tmp_path / "traffic.json").write_text(json.dumps([
+        {"workload": "w", "dtype": "f64", "kernel": "sell", "apply_cu_sha": "0" * 16, "dram_bytes_per_launch": 5}]))
+    assert bench.committed_traffic("w", "f64", "sell") is None
+    (tmp_path / "traffic.json").write_text(json.dumps([
+        {"workload": "w", "dtype": "f64", "kernel": "sell", "apply_cu_sha": bench.apply_source_sha(),
+         "dram_bytes_per_launch": 5}]))
+    assert bench.committed_traffic("w", "f64", "sell") == 5
+
+
+def _run_bench(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, capture_output=True, text=True,
+                          env=env, cwd=ROOT, timeout=300)
+
+
+def test_reference_arm_prints_one_json_line():
+    res = _run_bench(["--impl", "reference", "--workload", "lap2d_small", "--steps", "4", "--warmup", "3"])
+    assert res.returncode == 0, res.stderr
+    lines = [ln for ln in res.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["unit"] == "GFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 4 and line["warmup"] == 3
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    res = _run_bench(["--impl", "reference", "--workload", "lap2d_small", "--steps", "2", "--warmup", "3"],
+                     {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert res.returncode == 0 and res.stdout.strip() == ""
