@@ -25,7 +25,8 @@
  *  - Errors: functions returning int return an spmv_status (0 = success); functions
  *    returning a handle return NULL on failure.  In both cases spmv_last_error()
  *    and spmv_last_error_message() describe the failure for the calling thread.
- *    No entry point traps or aborts on bad input.
+ *    No entry point traps or aborts on bad input; every entry point except
+ *    spmv_csr_apply_noalloc validates its matrix.
  */
 #ifndef SPMV_GB300_H
 #define SPMV_GB300_H
@@ -201,6 +202,35 @@ SPMV_API int spmv_describe(spmv_handle_t h, char *json, size_t cap);
  * SPMV_ERR_UNSUPPORTED for a handle without a sliced part.  Synchronises `stream`.
  */
 SPMV_API int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr, void *stream);
+
+/*
+ * y = A x computed directly from a CSR matrix in the caller's device memory, with
+ * no device allocation at all (no handle, no cudaMalloc / cudaFree, no allocating
+ * library call).  None of the pages has a counterpart to this entry point: it is
+ * there for callers that cannot allocate device memory -- for example a program
+ * that hands all device memory to its own pool at start-up and forbids other
+ * allocations, or a time-critical loop that cannot afford the implicit device
+ * synchronisation of cudaMalloc / cudaFree -- and therefore cannot build a handle.
+ *
+ * The computation is the load-balanced merge-path pass used for long rows,
+ * applied to every row; y is overwritten.  Its only scratch (one partial sum per
+ * 2048-item share of the work) sits in a fixed 768 KiB array inside this
+ * library's device image, which every GPU that loads the library keeps until the
+ * process exits.  Hence:
+ *   - n + nnz must not exceed 134,217,728; larger matrices return SPMV_ERR_TOO_LARGE
+ *     before anything runs;
+ *   - all calls share that array: calls that overlap on the GPU (different streams,
+ *     or different host threads) race on it and give wrong results; serialise them;
+ *   - the first call on a device looks up the array's device address (and, with
+ *     lazy module loading, makes the driver load the library's device code); make
+ *     that first call before any stream capture;
+ *   - the CSR is NOT validated (validation would need a device-to-host round trip):
+ *     pass a matrix that spmv_build_from_csr would accept.
+ * Arguments are as in spmv_build_from_csr plus x, y (device arrays of n values of
+ * `dtype`) and `stream`.  Asynchronous; returns an spmv_status.
+ */
+SPMV_API int spmv_csr_apply_noalloc(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
+                                    const void *vals, int dtype, const void *x, void *y, void *stream);
 
 #ifdef __cplusplus
 }

@@ -19,6 +19,7 @@ from ._abi import (  # noqa: F401
     spmv_apply_profiled,
     spmv_build_from_csr,
     spmv_build_from_csr_ex,
+    spmv_csr_apply_noalloc,
     spmv_default_params,
     spmv_describe,
     spmv_destroy,

@@ -26,6 +26,7 @@ EXPORTS = (
     "spmv_default_params", "spmv_build_from_csr", "spmv_build_from_csr_ex", "spmv_apply",
     "spmv_apply_host", "spmv_apply_profiled", "spmv_destroy", "spmv_last_error",
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
+    "spmv_csr_apply_noalloc",
 )
 
 
@@ -79,6 +80,8 @@ def _load():
     lib.spmv_describe.restype = c_int
     lib.spmv_get_layout.argtypes = [vp, vp, vp, vp]
     lib.spmv_get_layout.restype = c_int
+    lib.spmv_csr_apply_noalloc.argtypes = [i64, i64, vp, vp, vp, c_int, vp, vp, vp]
+    lib.spmv_csr_apply_noalloc.restype = c_int
     del i32
     return lib
 
@@ -212,3 +215,9 @@ def spmv_describe(h) -> dict:
 
 def spmv_get_layout(h, perm=None, slice_ptr=None, stream=None) -> None:
     _check(lib.spmv_get_layout(h, _ptr(perm), _ptr(slice_ptr), _stream(stream)))
+
+
+def spmv_csr_apply_noalloc(n, nnz, row_ptr, col_idx, vals, dtype, x, y, stream=None) -> None:
+    """y = A x from a device CSR without any device allocation (see spmv.h)."""
+    _check(lib.spmv_csr_apply_noalloc(int(n), int(nnz), _ptr(row_ptr), _ptr(col_idx), _ptr(vals), int(dtype),
+                                      _ptr(x), _ptr(y), _stream(stream)))

@@ -1,6 +1,6 @@
 """Compile the CUDA library ``libspmv_gb300.so`` in-tree for sm_103a.
 
-Three translation units are compiled in parallel with nvcc and linked into a
+Four translation units are compiled in parallel with nvcc and linked into a
 shared library inside this package directory.  Run it as a script (importing
 the package itself needs the built library)::
 
@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspmv_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["api.cu", "build.cu", "apply.cu"]
+SOURCES = ["api.cu", "build.cu", "apply.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -176,7 +176,8 @@ __device__ __forceinline__ T seg_scan_exclusive(int f, T v, SegScan<T, THREADS> 
 // ---------------------------------------------------------------------------
 // merge-path over a compact CSR (long rows, or the HEC spill)
 // ---------------------------------------------------------------------------
-template <typename T>
+// kIdentityRows: compact row i is matrix row i (rows may be NULL).
+template <typename T, bool kIdentityRows = false>
 __global__ void __launch_bounds__(kMergeThreads) k_merge_path(
     int64_t n_rows, int64_t nnz, const int32_t *__restrict__ ptr, const int32_t *__restrict__ rows,
     const int32_t *__restrict__ col, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y,
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_path(
     T acc = carry_in;
     for (int it = dl; it < dl_end; ++it) {
         if (il < ni && s_end[il] <= kl) {
-            const int32_t r = __ldg(rows + i0 + il);
+            const int32_t r = kIdentityRows ? static_cast<int32_t>(i0 + il) : __ldg(rows + i0 + il);
             y[r] = accumulate ? y[r] + acc : acc;
             acc = T(0);
             ++il;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_path(
         const T inclusive = flag ? run : carry_in + run;
         const int64_t i = i0 + open_row;
         if (i < n_rows) {
-            carry_row[blockIdx.x] = __ldg(rows + i);
+            carry_row[blockIdx.x] = kIdentityRows ? static_cast<int32_t>(i) : __ldg(rows + i);
             carry_val[blockIdx.x] = static_cast<double>(inclusive);
         } else {
             carry_row[blockIdx.x] = -1;
@@ -411,6 +412,24 @@ cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void
                                                         static_cast<const float *>(x), static_cast<float *>(y),
                                                         sg.carry_row, sg.carry_val, sg.accumulate);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_path_identity(int dtype, int64_t n_rows, int64_t nnz, const int32_t *ptr,
+                                       const int32_t *col, const void *val, const void *x, void *y,
+                                       int32_t *carry_row, double *carry_val, int64_t n_cta, cudaStream_t s) {
+    if (n_cta <= 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>(n_cta);
+    if (dtype == SPMV_F64)
+        k_merge_path<double, true><<<grid, kMergeThreads, 0, s>>>(n_rows, nnz, ptr, nullptr, col,
+                                                                  static_cast<const double *>(val),
+                                                                  static_cast<const double *>(x),
+                                                                  static_cast<double *>(y), carry_row, carry_val, 0);
+    else
+        k_merge_path<float, true><<<grid, kMergeThreads, 0, s>>>(n_rows, nnz, ptr, nullptr, col,
+                                                                 static_cast<const float *>(val),
+                                                                 static_cast<const float *>(x),
+                                                                 static_cast<float *>(y), carry_row, carry_val, 0);
     return cudaGetLastError();
 }
 

@@ -214,6 +214,10 @@ cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *ro
                               const void *x, void *y, cudaStream_t s);
 cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
+// merge-path over a whole CSR (row i of the path is matrix row i), writing y
+cudaError_t launch_merge_path_identity(int dtype, int64_t n_rows, int64_t nnz, const int32_t *ptr,
+                                       const int32_t *col, const void *val, const void *x, void *y,
+                                       int32_t *carry_row, double *carry_val, int64_t n_cta, cudaStream_t s);
 int64_t merge_ctas(int64_t n_rows, int64_t nnz);
 int64_t coo_ctas(int64_t nnz);
 
