@@ -211,8 +211,12 @@ def measure_device(torch, spmv, csr, x_np, steps, warmup, sampler=None, fmt="aut
     build_ms = (time.perf_counter() - t_b) * 1e3
     desc = A.describe()
     stream = torch.cuda.current_stream()
+    # the C entry point itself, with its arguments marshalled once
+    apply_c = spmv._abi.lib.spmv_apply
+    args = (A._h, x.data_ptr(), y.data_ptr(), stream.cuda_stream or None)
+    rc = 0
     for _ in range(warmup):
-        A.apply(x, y)
+        rc |= apply_c(*args)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -221,10 +225,12 @@ def measure_device(torch, spmv, csr, x_np, steps, warmup, sampler=None, fmt="aut
     t0 = time.time()
     e0.record(stream)
     for _ in range(steps):
-        A.apply(x, y)
+        rc |= apply_c(*args)
     e1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
+    if rc:
+        raise RuntimeError(f"spmv_apply failed: {spmv.spmv_last_error_message()}")
     region_ms = e0.elapsed_time(e1)
     # per-kernel split of one apply (separate, event-bracketed launches)
     splits = [A.apply_profiled(x, y) for _ in range(20)]

@@ -70,6 +70,11 @@ typedef enum { SPMV_F64 = 0, SPMV_F32 = 1 } spmv_dtype;
  *      row, as COO (HYB) or CSR (HEC); the ELL part is computed first and writes y,
  *      the spill adds into y.  Krylov/AMG paper, matrix formats, Figs. 1-3 and the
  *      HEC SpMV algorithm.
+ *  SPMV_FMT_MERGE       CSR kept as given, every row processed by the load-balanced
+ *      merge-path pass: each CTA takes an equal share of the sequence that merges
+ *      row ends with entries, whatever the row lengths (the merge-path split the
+ *      Trilinos issue attributes to the vendor library; the load-balanced CSR/COO
+ *      kernels of the scite report's abstract).  Suited to irregular matrices.
  *  SPMV_FMT_AUTO        the builder picks one of the above from the row lengths.
  * In every format, rows longer than the long-row threshold are taken out and
  * handled by a load-balanced merge-path pass (the "very long rows" class of the
@@ -81,7 +86,8 @@ typedef enum {
     SPMV_FMT_CSR_VECTOR = 1,
     SPMV_FMT_ELL_R = 2,
     SPMV_FMT_SELL = 3,
-    SPMV_FMT_HYB = 4
+    SPMV_FMT_HYB = 4,
+    SPMV_FMT_MERGE = 5
 } spmv_format;
 
 /*

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspmv_gb300.so")
 
 SPMV_F64, SPMV_F32 = 0, 1
-FORMATS = {"auto": 0, "csr_vector": 1, "ell_r": 2, "sell": 3, "hyb": 4}
+FORMATS = {"auto": 0, "csr_vector": 1, "ell_r": 2, "sell": 3, "hyb": 4, "merge": 5}
 STATUS = {
     0: "SPMV_OK", -1: "SPMV_ERR_INVALID_ARG", -2: "SPMV_ERR_BAD_CSR", -3: "SPMV_ERR_CUDA",
     -4: "SPMV_ERR_OOM", -5: "SPMV_ERR_TOO_LARGE", -6: "SPMV_ERR_UNSUPPORTED", -7: "SPMV_ERR_TIMEOUT",

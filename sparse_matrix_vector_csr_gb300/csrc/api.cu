@@ -129,6 +129,7 @@ const char *format_name(int f) {
         case SPMV_FMT_ELL_R: return "ell_r";
         case SPMV_FMT_SELL: return "sell";
         case SPMV_FMT_HYB: return "hyb";
+        case SPMV_FMT_MERGE: return "merge";
         default: return "?";
     }
 }
@@ -192,6 +193,20 @@ int partition_rows(BuildCtx &c, int mode, int32_t a, int32_t forced_g, int32_t *
     return SPMV_OK;
 }
 
+// Carry slots of the segmented pass and, for merge-path, the precomputed split of
+// every CTA boundary (so the apply kernel does no search).
+int alloc_carries(BuildCtx &c, Segmented &sg) {
+    spmv_handle_t h = c.h;
+    if (sg.n_cta <= 0) return SPMV_OK;
+    SPMV_TRY(dev_alloc_n(h, &sg.carry_row, sg.n_cta));
+    SPMV_TRY(dev_alloc_n(h, &sg.carry_val, sg.n_cta));
+    if (sg.kind == 1) {
+        SPMV_TRY(dev_alloc_n(h, &sg.part, sg.n_cta + 1));
+        SPMV_TRY_CUDA(launch_merge_partition(sg.n_rows, sg.nnz, sg.ptr, sg.n_cta, sg.part, c.s));
+    }
+    return SPMV_OK;
+}
+
 // Compact CSR of the listed rows, entries from in-row position `offset` on.
 int build_segment(BuildCtx &c, const int32_t *rows_dev, int64_t m, int32_t offset, int kind, int accumulate) {
     spmv_handle_t h = c.h;
@@ -224,10 +239,7 @@ int build_segment(BuildCtx &c, const int32_t *rows_dev, int64_t m, int32_t offse
     SPMV_TRY_CUDA(launch_compact_copy(h->dtype, m, sg.rows, c.row_ptr, offset, c.col, c.val, cptr, sg.col, sg.val,
                                       sg.coo_row, c.s));
     sg.n_cta = (kind == 1) ? merge_ctas(m, total) : coo_ctas(total);
-    if (sg.n_cta > 0) {
-        SPMV_TRY(dev_alloc_n(h, &sg.carry_row, sg.n_cta));
-        SPMV_TRY(dev_alloc_n(h, &sg.carry_val, sg.n_cta));
-    }
+    SPMV_TRY(alloc_carries(c, sg));
     return SPMV_OK;
 }
 
@@ -474,6 +486,33 @@ int build_csr_vector(BuildCtx &c, int32_t forced_g) {
     return SPMV_OK;
 }
 
+// Every row through merge-path over a copy of the CSR (identity row map, writes y).
+int build_merge(BuildCtx &c) {
+    spmv_handle_t h = c.h;
+    const size_t vb = value_bytes(h->dtype);
+    SPMV_TRY(dev_alloc_n(h, &h->csr_col, h->nnz));
+    SPMV_TRY(dev_alloc(h, &h->csr_val, static_cast<size_t>(h->nnz) * vb));
+    if (h->nnz > 0) {
+        SPMV_TRY_CUDA(cudaMemcpyAsync(h->csr_col, c.col, sizeof(int32_t) * h->nnz, cudaMemcpyDeviceToDevice, c.s));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(h->csr_val, c.val, vb * h->nnz, cudaMemcpyDeviceToDevice, c.s));
+    }
+    Segmented &sg = h->seg;
+    sg = Segmented();
+    sg.kind = 1;
+    sg.n_rows = h->n;
+    sg.nnz = h->nnz;
+    sg.rows = nullptr;
+    sg.ptr = h->row_ptr;
+    sg.col = h->csr_col;
+    sg.val = h->csr_val;
+    sg.accumulate = 0;
+    sg.n_cta = merge_ctas(h->n, h->nnz);
+    SPMV_TRY(alloc_carries(c, sg));
+    h->n_long_rows = 0;
+    h->long_nnz = 0;
+    return SPMV_OK;
+}
+
 // Padded slot count of SELL-32 in natural order (sigma = 1), for the AUTO choice.
 int probe_sigma1_slots(BuildCtx &c, int64_t *slots) {
     const int64_t n = c.h->n;
@@ -535,7 +574,7 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     const int fmt_for_thr = (format == SPMV_FMT_AUTO) ? SPMV_FMT_SELL : format;
     if (thr < 0) thr = default_threshold(fmt_for_thr, h->dtype);
     if (prm.long_row_threshold == 0) thr = -1;  // 0 = never cut
-    if (format == SPMV_FMT_HYB) thr = -1;         // the spill takes every long tail
+    if (format == SPMV_FMT_HYB || format == SPMV_FMT_MERGE) thr = -1;  // no separate long-row pass
     c.threshold = thr;
 
     int64_t *hist_d = nullptr, *stats_d = nullptr;
@@ -579,19 +618,9 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
             const bool good = static_cast<double>(h->sliced.slots) <= 1.10 * static_cast<double>(stored) + 32.0 * 64;
             release_sliced(h);
             if (!good) {
-                format = SPMV_FMT_CSR_VECTOR;
-                thr = prm.long_row_threshold < 0 ? default_threshold(format, h->dtype) : thr;
-                if (thr != c.threshold) {
-                    c.threshold = thr;
-                    SPMV_TRY_CUDA(launch_histogram(n, c.len, thr, hist_d, stats_d, c.s));
-                    SPMV_TRY_CUDA(cudaMemcpyAsync(stats, stats_d, sizeof(stats), cudaMemcpyDeviceToHost, c.s));
-                    SPMV_TRY(sync(c.s));
-                    c.n_long = stats[0];
-                    c.long_nnz = stats[1];
-                    c.max_short = static_cast<int32_t>(stats[2]);
-                    h->n_long_rows = c.n_long;
-                    h->long_nnz = c.long_nnz;
-                }
+                // irregular row lengths: equal work shares per CTA regardless of rows
+                format = SPMV_FMT_MERGE;
+                c.threshold = -1;
             }
         }
     }
@@ -617,6 +646,10 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
             break;
         case SPMV_FMT_SELL:
             SPMV_TRY(build_sell_like(c, format, C, sigma));
+            break;
+        case SPMV_FMT_MERGE:
+            h->params.long_row_threshold = -1;
+            SPMV_TRY(build_merge(c));
             break;
         case SPMV_FMT_HYB: {
             const int32_t cap = default_threshold(SPMV_FMT_SELL, h->dtype);
@@ -703,7 +736,7 @@ spmv_handle_t build_impl(int64_t n, int64_t nnz, const int32_t *row_ptr, const i
         set_error(SPMV_ERR_INVALID_ARG, "dtype must be SPMV_F64 or SPMV_F32");
         return nullptr;
     }
-    if (format < SPMV_FMT_AUTO || format > SPMV_FMT_HYB) {
+    if (format < SPMV_FMT_AUTO || format > SPMV_FMT_MERGE) {
         set_error(SPMV_ERR_INVALID_ARG, "unknown format");
         return nullptr;
     }
@@ -863,7 +896,7 @@ int spmv_to_csr(spmv_handle_t h, int32_t *row_ptr, int32_t *col_idx, void *vals,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t vb = value_bytes(h->dtype);
     SPMV_TRY_CUDA(cudaMemcpyAsync(row_ptr, h->row_ptr, sizeof(int32_t) * (h->n + 1), cudaMemcpyDeviceToDevice, s));
-    if (h->format == SPMV_FMT_CSR_VECTOR) {
+    if (h->format == SPMV_FMT_CSR_VECTOR || h->format == SPMV_FMT_MERGE) {
         if (h->nnz > 0) {
             SPMV_TRY_CUDA(cudaMemcpyAsync(col_idx, h->csr_col, sizeof(int32_t) * h->nnz, cudaMemcpyDeviceToDevice, s));
             SPMV_TRY_CUDA(cudaMemcpyAsync(vals, h->csr_val, vb * h->nnz, cudaMemcpyDeviceToDevice, s));
@@ -937,7 +970,7 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     } else if (sl.present) {
         matrix_bytes += sl.stored_entries * (vb + 4) + sl.n_pos * 4 + (sl.perm ? sl.n_pos * 4 : 0) + sl.n_slices * 8;
     }
-    if (sg.kind == 1) matrix_bytes += sg.nnz * (vb + 4) + sg.n_rows * 8 + sg.n_cta * 12;
+    if (sg.kind == 1) matrix_bytes += sg.nnz * (vb + 4) + sg.n_rows * (sg.rows ? 8 : 4) + sg.n_cta * 16;
     if (sg.kind == 2) matrix_bytes += sg.nnz * (vb + 8) + sg.n_cta * 12;
     append(o, "\"format_bytes\":%lld,\"vector_bytes\":%lld}", (long long)matrix_bytes, (long long)(2 * h->n * vb));
     std::snprintf(json, cap, "%s", o.c_str());

@@ -41,38 +41,73 @@ __device__ __forceinline__ T ld_x(const T *p) { return __ldg(p); }
 // ---------------------------------------------------------------------------
 // sliced layout
 // ---------------------------------------------------------------------------
+// Entries of a row are processed U at a time: the U column indices and values
+// (predicated on the row length, so padding is never touched) are loaded first,
+// then the U gathers of x, then U fused multiply-adds.  This keeps 2U independent
+// streaming loads in flight per thread before the dependent gathers.  U = 4 for
+// fp64 and 8 for fp32 fills the load queue without raising register use above
+// 32, which keeps all 64 warps of an SM resident.
 template <typename T>
-__global__ void __launch_bounds__(kSellBlock) k_sell(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
-                                                     const int64_t *__restrict__ slice_ptr,
-                                                     const int32_t *__restrict__ len,
-                                                     const int32_t *__restrict__ perm,
-                                                     const int32_t *__restrict__ col, const T *__restrict__ val,
-                                                     const T *__restrict__ x, T *__restrict__ y, int64_t n) {
+struct SellChunk {
+    static constexpr int U = sizeof(T) == 8 ? 4 : 8;
+};
+
+// CS > 0: SELL with a compile-time slice height CS (stride = CS).
+// CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
+//          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
+template <typename T, int CS>
+__global__ void __launch_bounds__(kSellBlock, 8) k_sell(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
+                                                        const int64_t *__restrict__ slice_ptr,
+                                                        const int32_t *__restrict__ len,
+                                                        const int32_t *__restrict__ perm,
+                                                        const int32_t *__restrict__ col, const T *__restrict__ val,
+                                                        const T *__restrict__ x, T *__restrict__ y, int64_t n) {
+    constexpr int U = SellChunk<T>::U;
     const int64_t p = gtid();
     if (p >= n_pos) return;
     const int w = __ldg(len + p);
-    const int64_t slot = __ldg(slice_ptr + (p >> log2C)) + static_cast<int64_t>(p & cmask);
+    const uint64_t up = static_cast<uint64_t>(p);
+    const int64_t slot = CS > 0 ? __ldg(slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
+                                : __ldg(slice_ptr + (p >> log2C)) + static_cast<int64_t>(p & cmask);
     const int32_t *cp = col + slot;
     const T *vp = val + slot;
     T acc = T(0);
-    int j = 0;
-    for (; j + 4 <= w; j += 4) {
-        const int32_t c0 = ld_stream(cp), c1 = ld_stream(cp + stride), c2 = ld_stream(cp + 2 * stride),
-                      c3 = ld_stream(cp + 3 * stride);
-        const T v0 = ld_stream(vp), v1 = ld_stream(vp + stride), v2 = ld_stream(vp + 2 * stride),
-                v3 = ld_stream(vp + 3 * stride);
-        const T x0 = ld_x(x + c0), x1 = ld_x(x + c1), x2 = ld_x(x + c2), x3 = ld_x(x + c3);
-        acc = fma(v0, x0, acc);
-        acc = fma(v1, x1, acc);
-        acc = fma(v2, x2, acc);
-        acc = fma(v3, x3, acc);
-        cp += 4 * stride;
-        vp += 4 * stride;
-    }
-    for (; j < w; ++j) {
-        acc = fma(ld_stream(vp), ld_x(x + ld_stream(cp)), acc);
-        cp += stride;
-        vp += stride;
+    if constexpr (CS > 0) {
+        for (int j = 0; j < w; j += U) {
+            int32_t c[U];
+            T a[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool on = j + u < w;
+                c[u] = on ? ld_stream(cp + u * CS) : 0;
+                a[u] = on ? ld_stream(vp + u * CS) : T(0);
+            }
+            T xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc = fma(a[u], xv[u], acc);  // inactive slots add +0 * +0
+            cp += U * CS;
+            vp += U * CS;
+        }
+    } else {
+        for (int j = 0; j < w; j += U) {
+            int32_t c[U];
+            T a[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool on = j + u < w;
+                c[u] = on ? ld_stream(cp) : 0;
+                a[u] = on ? ld_stream(vp) : T(0);
+                cp += stride;
+                vp += stride;
+            }
+            T xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc = fma(a[u], xv[u], acc);
+        }
     }
     const int64_t r = perm ? static_cast<int64_t>(__ldg(perm + p)) : p;
     if (r >= 0 && r < n) y[r] = acc;
@@ -176,43 +211,78 @@ __device__ __forceinline__ T seg_scan_exclusive(int f, T v, SegScan<T, THREADS> 
 // ---------------------------------------------------------------------------
 // merge-path over a compact CSR (long rows, or the HEC spill)
 // ---------------------------------------------------------------------------
+// Stage the CTA's entries as products a_k * x[col_k] in shared memory: every
+// thread issues its (at most kMergeIpt) column/value loads first, then the gathers.
+template <typename T>
+__device__ __forceinline__ void stage_products(const int32_t *__restrict__ col, const T *__restrict__ val,
+                                               const T *__restrict__ x, int64_t k0, int nk, T *s_prod) {
+    int32_t c[kMergeIpt];
+    T a[kMergeIpt];
+#pragma unroll
+    for (int q = 0; q < kMergeIpt; ++q) {
+        const int t = threadIdx.x + q * kMergeThreads;
+        const bool on = t < nk;
+        c[q] = on ? ld_stream(col + k0 + t) : 0;
+        a[q] = on ? ld_stream(val + k0 + t) : T(0);
+    }
+#pragma unroll
+    for (int q = 0; q < kMergeIpt; ++q) {
+        const int t = threadIdx.x + q * kMergeThreads;
+        if (t < nk) s_prod[t] = a[q] * ld_x(x + c[q]);
+    }
+}
+
+// merge-path split: number of row ends among the first d items of the path that
+// merges the row ends ptr[1..n_rows] with the entry indices 0..nnz-1
+__device__ __forceinline__ int64_t merge_split(int64_t d, int64_t n_rows, int64_t nnz, const int32_t *ptr) {
+    int64_t lo = max64(0, d - nnz), hi = min64(d, n_rows);
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(ptr[mid + 1]) <= d - 1 - mid)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
 // kIdentityRows: compact row i is matrix row i (rows may be NULL).
+// part: the split of every CTA boundary, precomputed when the matrix was built
+// (part[c] = row ends among the first c * kMergeItems path items), or NULL to
+// search it here.
 template <typename T, bool kIdentityRows = false>
 __global__ void __launch_bounds__(kMergeThreads) k_merge_path(
     int64_t n_rows, int64_t nnz, const int32_t *__restrict__ ptr, const int32_t *__restrict__ rows,
     const int32_t *__restrict__ col, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y,
-    int32_t *__restrict__ carry_row, double *__restrict__ carry_val, int accumulate) {
+    int32_t *__restrict__ carry_row, double *__restrict__ carry_val, int accumulate,
+    const int32_t *__restrict__ part) {
     __shared__ T s_prod[kMergeItems];
     __shared__ int32_t s_end[kMergeItems];
-    __shared__ int64_t s_coord[4];
+    __shared__ int64_t s_coord[2];
     __shared__ SegScan<T, kMergeThreads> s_scan;
 
     const int64_t total = n_rows + nnz;
     const int64_t d0 = static_cast<int64_t>(blockIdx.x) * kMergeItems;
     const int64_t d1 = min(d0 + kMergeItems, total);
-    if (threadIdx.x < 2) {
-        // merge-path split: number of row ends among the first d path items
-        const int64_t d = threadIdx.x ? d1 : d0;
-        int64_t lo = max64(0, d - nnz), hi = min64(d, n_rows);
-        while (lo < hi) {
-            const int64_t mid = (lo + hi) >> 1;
-            if (static_cast<int64_t>(ptr[mid + 1]) <= d - 1 - mid)
-                lo = mid + 1;
-            else
-                hi = mid;
-        }
-        s_coord[2 * threadIdx.x] = lo;
-        s_coord[2 * threadIdx.x + 1] = d - lo;
+    int64_t i0, i1;
+    if (part) {
+        i0 = __ldg(part + blockIdx.x);
+        i1 = __ldg(part + blockIdx.x + 1);
+    } else {
+        if (threadIdx.x < 2) s_coord[threadIdx.x] = merge_split(threadIdx.x ? d1 : d0, n_rows, nnz, ptr);
+        __syncthreads();
+        i0 = s_coord[0];
+        i1 = s_coord[1];
     }
-    __syncthreads();
-    const int64_t i0 = s_coord[0], k0 = s_coord[1];
-    const int ni = static_cast<int>(s_coord[2] - i0);
-    const int nk = static_cast<int>(s_coord[3] - k0);
-    for (int t = threadIdx.x; t < nk; t += kMergeThreads) {
-        const int64_t k = k0 + t;
-        s_prod[t] = ld_stream(val + k) * ld_x(x + ld_stream(col + k));
+    const int64_t k0 = d0 - i0;
+    const int ni = static_cast<int>(i1 - i0);
+    const int nk = static_cast<int>((d1 - i1) - k0);
+    stage_products(col, val, x, k0, nk, s_prod);
+#pragma unroll
+    for (int q = 0; q < kMergeIpt; ++q) {
+        const int t = threadIdx.x + q * kMergeThreads;
+        if (t < ni) s_end[t] = static_cast<int32_t>(__ldg(ptr + i0 + t + 1) - k0);
     }
-    for (int t = threadIdx.x; t < ni; t += kMergeThreads) s_end[t] = static_cast<int32_t>(ptr[i0 + t + 1] - k0);
     __syncthreads();
 
     const int npath = ni + nk;
@@ -284,10 +354,11 @@ __global__ void __launch_bounds__(kMergeThreads) k_coo(int64_t nnz, const int32_
     __shared__ SegScan<T, kMergeThreads> s_scan;
     const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kMergeItems;
     const int nk = static_cast<int>(min64(kMergeItems, nnz - k0));
-    for (int t = threadIdx.x; t < nk; t += kMergeThreads) {
-        const int64_t k = k0 + t;
-        s_prod[t] = ld_stream(val + k) * ld_x(x + ld_stream(col + k));
-        s_row[t] = ld_stream(crow + k);
+    stage_products(col, val, x, k0, nk, s_prod);
+#pragma unroll
+    for (int q = 0; q < kMergeIpt; ++q) {
+        const int t = threadIdx.x + q * kMergeThreads;
+        if (t < nk) s_row[t] = ld_stream(crow + k0 + t);
     }
     if (threadIdx.x == 0) s_row[nk] = (k0 + nk < nnz) ? crow[k0 + nk] : -1;
     __syncthreads();
@@ -324,19 +395,26 @@ __global__ void __launch_bounds__(kMergeThreads) k_coo(int64_t nnz, const int32_
     }
 }
 
-// Rows crossing CTA boundaries: the first CTA of each run of equal carry rows sums
-// the run in double and adds it to y once.
+// Rows crossing CTA boundaries: carries of one row are contiguous (rows only grow
+// along the path).  One warp per carry slot; the warp whose slot starts a run sums
+// the run (lanes stride through it, then a shuffle tree, all in double) and adds
+// it to y once.  No atomics.
 template <typename T>
 __global__ void k_carry_fixup(int64_t n_cta, const int32_t *__restrict__ carry_row,
                               const double *__restrict__ carry_val, T *__restrict__ y) {
-    const int64_t c = gtid();
-    if (c >= n_cta) return;
+    const int64_t c = gtid() >> 5;
+    const int lane = threadIdx.x & 31;
+    if (c >= n_cta) return;  // whole warp
     const int32_t r = carry_row[c];
-    if (r < 0) return;
-    if (c > 0 && carry_row[c - 1] == r) return;
+    if (r < 0 || (c > 0 && carry_row[c - 1] == r)) return;
     double s = 0.0;
-    for (int64_t c2 = c; c2 < n_cta && carry_row[c2] == r; ++c2) s += carry_val[c2];
-    y[r] = static_cast<T>(static_cast<double>(y[r]) + s);
+    for (int64_t c2 = c + lane; c2 < n_cta; c2 += 32) {
+        if (carry_row[c2] != r) break;
+        s += carry_val[c2];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) y[r] = static_cast<T>(static_cast<double>(y[r]) + s);
 }
 
 template <typename T>
@@ -361,18 +439,28 @@ cudaError_t csr_vector_dispatch(int g, int64_t count, const int32_t *rows, const
 int64_t merge_ctas(int64_t n_rows, int64_t nnz) { return ceil_div(n_rows + nnz, kMergeItems); }
 int64_t coo_ctas(int64_t nnz) { return ceil_div(nnz, kMergeItems); }
 
+template <typename T>
+cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const T *x, T *y, cudaStream_t s) {
+    const unsigned grid = static_cast<unsigned>(ceil_div(sl.n_pos, kSellBlock));
+    const T *val = static_cast<const T *>(sl.val);
+    const bool sliced = sl.log2C < 31;
+    if (sliced && sl.C == 32)
+        k_sell<T, 32><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
+                                                  sl.perm, sl.col, val, x, y, n);
+    else if (sliced && sl.C == 64)
+        k_sell<T, 64><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
+                                                  sl.perm, sl.col, val, x, y, n);
+    else
+        k_sell<T, 0><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
+                                                 sl.perm, sl.col, val, x, y, n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s) {
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>(ceil_div(sl.n_pos, kSellBlock));
     if (dtype == SPMV_F64)
-        k_sell<double><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                   sl.perm, sl.col, static_cast<const double *>(sl.val),
-                                                   static_cast<const double *>(x), static_cast<double *>(y), n);
-    else
-        k_sell<float><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                  sl.perm, sl.col, static_cast<const float *>(sl.val),
-                                                  static_cast<const float *>(x), static_cast<float *>(y), n);
-    return cudaGetLastError();
+        return sell_dispatch<double>(sl, n, static_cast<const double *>(x), static_cast<double *>(y), s);
+    return sell_dispatch<float>(sl, n, static_cast<const float *>(x), static_cast<float *>(y), s);
 }
 
 cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *rows, const int32_t *row_ptr,
@@ -387,19 +475,22 @@ cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *ro
 cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s) {
     if (sg.kind == 0 || sg.n_cta <= 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>(sg.n_cta);
+    if (sg.kind == 1 && sg.rows == nullptr)
+        return launch_merge_path_identity(dtype, sg.n_rows, sg.nnz, sg.ptr, sg.col, sg.val, x, y, sg.carry_row,
+                                          sg.carry_val, sg.n_cta, s, sg.part);
     if (sg.kind == 1) {
         if (dtype == SPMV_F64)
             k_merge_path<double><<<grid, kMergeThreads, 0, s>>>(sg.n_rows, sg.nnz, sg.ptr, sg.rows, sg.col,
                                                                 static_cast<const double *>(sg.val),
                                                                 static_cast<const double *>(x),
                                                                 static_cast<double *>(y), sg.carry_row,
-                                                                sg.carry_val, sg.accumulate);
+                                                                sg.carry_val, sg.accumulate, sg.part);
         else
             k_merge_path<float><<<grid, kMergeThreads, 0, s>>>(sg.n_rows, sg.nnz, sg.ptr, sg.rows, sg.col,
                                                                static_cast<const float *>(sg.val),
                                                                static_cast<const float *>(x),
                                                                static_cast<float *>(y), sg.carry_row,
-                                                               sg.carry_val, sg.accumulate);
+                                                               sg.carry_val, sg.accumulate, sg.part);
     } else {
         if (dtype == SPMV_F64)
             k_coo<double><<<grid, kMergeThreads, 0, s>>>(sg.nnz, sg.coo_row, sg.col,
@@ -417,25 +508,28 @@ cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void
 
 cudaError_t launch_merge_path_identity(int dtype, int64_t n_rows, int64_t nnz, const int32_t *ptr,
                                        const int32_t *col, const void *val, const void *x, void *y,
-                                       int32_t *carry_row, double *carry_val, int64_t n_cta, cudaStream_t s) {
+                                       int32_t *carry_row, double *carry_val, int64_t n_cta, cudaStream_t s,
+                                       const int32_t *part) {
     if (n_cta <= 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>(n_cta);
     if (dtype == SPMV_F64)
         k_merge_path<double, true><<<grid, kMergeThreads, 0, s>>>(n_rows, nnz, ptr, nullptr, col,
                                                                   static_cast<const double *>(val),
                                                                   static_cast<const double *>(x),
-                                                                  static_cast<double *>(y), carry_row, carry_val, 0);
+                                                                  static_cast<double *>(y), carry_row, carry_val, 0,
+                                                                  part);
     else
         k_merge_path<float, true><<<grid, kMergeThreads, 0, s>>>(n_rows, nnz, ptr, nullptr, col,
                                                                  static_cast<const float *>(val),
                                                                  static_cast<const float *>(x),
-                                                                 static_cast<float *>(y), carry_row, carry_val, 0);
+                                                                 static_cast<float *>(y), carry_row, carry_val, 0,
+                                                                 part);
     return cudaGetLastError();
 }
 
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s) {
     if (sg.kind == 0 || sg.n_cta <= 1) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>(ceil_div(sg.n_cta, 256));
+    const unsigned grid = static_cast<unsigned>(ceil_div(sg.n_cta * 32, 256));
     if (dtype == SPMV_F64)
         k_carry_fixup<double><<<grid, 256, 0, s>>>(sg.n_cta, sg.carry_row, sg.carry_val, static_cast<double *>(y));
     else

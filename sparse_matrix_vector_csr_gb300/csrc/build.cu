@@ -452,6 +452,23 @@ __global__ void k_compact_copy(int64_t m, const int32_t *__restrict__ rows, cons
     }
 }
 
+// merge-path split of every CTA boundary (the same search the apply kernel would do)
+__global__ void k_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *__restrict__ ptr, int64_t n_cta,
+                                  int32_t *__restrict__ part) {
+    for (int64_t c = gtid(); c <= n_cta; c += gstride()) {
+        const int64_t d = min64(c * kMergeItems, n_rows + nnz);
+        int64_t lo = d - nnz > 0 ? d - nnz : 0, hi = min64(d, n_rows);
+        while (lo < hi) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (static_cast<int64_t>(ptr[mid + 1]) <= d - 1 - mid)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        part[c] = static_cast<int32_t>(lo);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // to_csr
 // ---------------------------------------------------------------------------
@@ -627,6 +644,12 @@ cudaError_t launch_compact_copy(int dtype, int64_t m, const int32_t *rows, const
         k_compact_copy<float><<<g, kBlock, 0, s>>>(m, rows, row_ptr, offset, col_in,
                                                    static_cast<const float *>(val_in), cptr, col_out,
                                                    static_cast<float *>(val_out), coo_row);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *ptr, int64_t n_cta, int32_t *part,
+                                   cudaStream_t s) {
+    k_merge_partition<<<grid_for(n_cta + 1, kBlock, 65536), kBlock, 0, s>>>(n_rows, nnz, ptr, n_cta, part);
     return cudaGetLastError();
 }
 

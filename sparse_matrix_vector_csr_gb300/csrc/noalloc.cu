@@ -90,7 +90,7 @@ extern "C" SPMV_API int spmv_csr_apply_noalloc(int64_t n, int64_t nnz, const int
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Every CTA writes its own carry slot, so nothing in the scratch needs clearing.
     SPMV_TRY_CUDA(launch_merge_path_identity(dtype, n, nnz, row_ptr, col_idx, vals, x, y, sg.carry_row, sg.carry_val,
-                                             n_cta, s));
+                                             n_cta, s, nullptr));
     SPMV_TRY_CUDA(launch_carry_fixup(dtype, sg, y, s));
     return SPMV_OK;
 }

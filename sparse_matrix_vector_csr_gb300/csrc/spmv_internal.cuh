@@ -67,6 +67,7 @@ struct Segmented {
     int64_t n_cta = 0;
     int32_t *carry_row = nullptr;  // [n_cta] row left open at the end of each CTA (-1 = none)
     double *carry_val = nullptr;   // [n_cta] its partial sum
+    int32_t *part = nullptr;       // [n_cta + 1] merge-path split of every CTA boundary (kind 1)
     int accumulate = 1;            // 1: add into y (y written before), 0: write y
     int32_t dst_offset = 0;        // in-row position of the first held entry (K for the spill)
 };
@@ -217,7 +218,11 @@ cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStre
 // merge-path over a whole CSR (row i of the path is matrix row i), writing y
 cudaError_t launch_merge_path_identity(int dtype, int64_t n_rows, int64_t nnz, const int32_t *ptr,
                                        const int32_t *col, const void *val, const void *x, void *y,
-                                       int32_t *carry_row, double *carry_val, int64_t n_cta, cudaStream_t s);
+                                       int32_t *carry_row, double *carry_val, int64_t n_cta, cudaStream_t s,
+                                       const int32_t *part);
+// part[c] = merge-path split at diagonal c * kMergeItems, c = 0..n_cta (build time)
+cudaError_t launch_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *ptr, int64_t n_cta, int32_t *part,
+                                   cudaStream_t s);
 int64_t merge_ctas(int64_t n_rows, int64_t nnz);
 int64_t coo_ctas(int64_t nnz);
 

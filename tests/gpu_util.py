@@ -71,6 +71,7 @@ FORMAT_CASES = [
     ("hyb", {"K": 20}),
     ("hyb", {"K": 3, "spill_csr": 0}),
     ("hyb", {"K": 0}),
+    ("merge", {}),
 ]
 
 

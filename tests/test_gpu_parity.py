@@ -40,7 +40,7 @@ def test_small_workloads_all_formats(name, case):
         assert_roundtrip(A, csr, label=f"{name}/{case_id(case)}")
 
 
-@pytest.mark.parametrize("case", [c for c in FORMAT_CASES if c[0] in ("auto", "csr_vector", "sell", "hyb")],
+@pytest.mark.parametrize("case", [c for c in FORMAT_CASES if c[0] in ("auto", "csr_vector", "sell", "hyb", "merge")],
                          ids=case_id)
 @pytest.mark.parametrize("name", ["lap3d_small", "powerlaw_small", "hmep_small"])
 def test_small_workloads_float32(name, case):
@@ -115,7 +115,7 @@ def test_zero_order_matrix():
         assert A.describe()["n"] == 0
 
 
-@pytest.mark.parametrize("fmt", ["auto", "csr_vector", "sell", "hyb"])
+@pytest.mark.parametrize("fmt", ["auto", "csr_vector", "sell", "hyb", "merge"])
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 def test_single_row_of_a_million(fmt, dtype):
     """One row with 10^6 entries spread over several hundred merge-path CTAs."""
