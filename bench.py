@@ -98,10 +98,23 @@ def load_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def apply_source_sha() -> str:
-    src = os.path.join(ROOT, "sparse_matrix_vector_csr_gb300", "csrc", "apply.cu")
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+KERNEL_SOURCES = {"sell": "sell.cu", "ell_r": "sell.cu", "hyb_ell": "sell.cu", "merge_path": "merge.cu",
+                  "coo_segmented": "merge.cu", "carry_fixup": "merge.cu"}
+
+
+def kernel_source(kernel: str) -> str:
+    name = "vector.cu" if kernel.startswith("csr_vector") else KERNEL_SOURCES.get(kernel, "")
+    return os.path.join(ROOT, "sparse_matrix_vector_csr_gb300", "csrc", name)
+
+
+def source_sha(kernel: str) -> str | None:
+    """Hash of the source file that holds a kernel (a committed ncu figure is only
+    valid for the kernel it was taken on)."""
+    try:
+        with open(kernel_source(kernel), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
 
 
 def committed_traffic(workload: str, dtype: str, kernel: str):
@@ -114,7 +127,7 @@ def committed_traffic(workload: str, dtype: str, kernel: str):
         return None
     for r in rows:
         if r.get("workload") == workload and r.get("dtype") == dtype and r.get("kernel") == kernel:
-            if r.get("apply_cu_sha") == apply_source_sha():
+            if r.get("source_sha") == source_sha(kernel):
                 return r.get("dram_bytes_per_launch")
     return None
 

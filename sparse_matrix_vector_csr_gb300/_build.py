@@ -1,6 +1,6 @@
 """Compile the CUDA library ``libspmv_gb300.so`` in-tree for sm_103a.
 
-Four translation units are compiled in parallel with nvcc and linked into a
+The translation units are compiled in parallel with nvcc and linked into a
 shared library inside this package directory.  Run it as a script (importing
 the package itself needs the built library)::
 
@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspmv_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["api.cu", "build.cu", "apply.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "build.cu", "sell.cu", "vector.cu", "merge.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -47,7 +47,8 @@ def _newer(target: str, deps: list[str]) -> bool:
 
 def _compile(src: str, extra: list[str]) -> str:
     obj = os.path.join(OBJ_DIR, os.path.splitext(src)[0] + ".o")
-    deps = [os.path.join(CSRC, src), os.path.join(CSRC, "spmv_internal.cuh"), os.path.join(INCLUDE, "spmv.h")]
+    deps = [os.path.join(CSRC, src), os.path.join(CSRC, "spmv_internal.cuh"), os.path.join(CSRC, "device_util.cuh"),
+            os.path.join(INCLUDE, "spmv.h")]
     if _newer(obj, deps):
         return obj
     cmd = [nvcc_path()] + common_flags() + extra + ["-c", os.path.join(CSRC, src), "-o", obj]

@@ -1,146 +1,19 @@
-// Apply kernels of the sm_103a SpMV library.
-//
-//  k_sell        one thread per sorted row position of a column-major sliced layout
-//                (SELL-C-sigma, ELLPACK-R, HYB's ELL part); each thread stops at its
-//                own row's length, so padding is never loaded or multiplied
-//                (ELLPACK-R, GPGPU spMVM paper arXiv 1112.5588, ELLPACK-R section;
-//                the scite report's "early stopping").
-//  k_csr_vector  g lanes per CSR row, partial sums combined with __shfl_xor_sync
-//                ("subwarp" per row, scite report quoting "Sparse Linear Algebra on
-//                AMD and NVIDIA GPUs").
-//  k_merge_path  equal shares of the merged (row ends, entries) sequence per CTA for
-//                the few very long rows (Trilinos issue on unpackAndCombine: very
-//                long rows, merge-path load balancing).
-//  k_coo         equal shares of COO entries per CTA with a segmented sum by row
-//                (load-balanced COO kernel of the scite report's abstract).
-//  k_carry_fixup adds the partial sums of rows that cross CTA boundaries; no atomics.
+// Load-balanced passes: merge-path over a compact CSR (long rows, HEC spill, or
+// every row), load-balanced COO (HYB spill), and the carry fix-up for rows that
+// cross CTA boundaries.  Equal work shares per CTA regardless of row lengths
+// (merge-path split named in the Trilinos issue on unpackAndCombine; load-balanced
+// COO of the scite report's abstract).  No atomics.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "device_util.cuh"
 #include "spmv_internal.cuh"
 
 namespace spmv {
 namespace {
 
-__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
-__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
-
-__device__ __forceinline__ int64_t gtid() {
-    return static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-}
-
-// Streaming loads for the matrix (read once per apply): evict-first in L1/L2.
-__device__ __forceinline__ int32_t ld_stream(const int32_t *p) { return __ldcs(p); }
-__device__ __forceinline__ double ld_stream(const double *p) { return __ldcs(p); }
-__device__ __forceinline__ float ld_stream(const float *p) { return __ldcs(p); }
-// x is gathered through the read-only path and kept in cache.
-template <typename T>
-__device__ __forceinline__ T ld_x(const T *p) { return __ldg(p); }
-
-// ---------------------------------------------------------------------------
-// sliced layout
-// ---------------------------------------------------------------------------
-// Entries of a row are processed U at a time: the U column indices and values
-// (predicated on the row length, so padding is never touched) are loaded first,
-// then the U gathers of x, then U fused multiply-adds.  This keeps 2U independent
-// streaming loads in flight per thread before the dependent gathers.  U = 4 for
-// fp64 and 8 for fp32 fills the load queue without raising register use above
-// 32, which keeps all 64 warps of an SM resident.
-template <typename T>
-struct SellChunk {
-    static constexpr int U = sizeof(T) == 8 ? 4 : 8;
-};
-
-// CS > 0: SELL with a compile-time slice height CS (stride = CS).
-// CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
-//          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
-template <typename T, int CS>
-__global__ void __launch_bounds__(kSellBlock, 8) k_sell(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
-                                                        const int64_t *__restrict__ slice_ptr,
-                                                        const int32_t *__restrict__ len,
-                                                        const int32_t *__restrict__ perm,
-                                                        const int32_t *__restrict__ col, const T *__restrict__ val,
-                                                        const T *__restrict__ x, T *__restrict__ y, int64_t n) {
-    constexpr int U = SellChunk<T>::U;
-    const int64_t p = gtid();
-    if (p >= n_pos) return;
-    const int w = __ldg(len + p);
-    const uint64_t up = static_cast<uint64_t>(p);
-    const int64_t slot = CS > 0 ? __ldg(slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
-                                : __ldg(slice_ptr + (p >> log2C)) + static_cast<int64_t>(p & cmask);
-    const int32_t *cp = col + slot;
-    const T *vp = val + slot;
-    T acc = T(0);
-    if constexpr (CS > 0) {
-        for (int j = 0; j < w; j += U) {
-            int32_t c[U];
-            T a[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const bool on = j + u < w;
-                c[u] = on ? ld_stream(cp + u * CS) : 0;
-                a[u] = on ? ld_stream(vp + u * CS) : T(0);
-            }
-            T xv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
-#pragma unroll
-            for (int u = 0; u < U; ++u) acc = fma(a[u], xv[u], acc);  // inactive slots add +0 * +0
-            cp += U * CS;
-            vp += U * CS;
-        }
-    } else {
-        for (int j = 0; j < w; j += U) {
-            int32_t c[U];
-            T a[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const bool on = j + u < w;
-                c[u] = on ? ld_stream(cp) : 0;
-                a[u] = on ? ld_stream(vp) : T(0);
-                cp += stride;
-                vp += stride;
-            }
-            T xv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
-#pragma unroll
-            for (int u = 0; u < U; ++u) acc = fma(a[u], xv[u], acc);
-        }
-    }
-    const int64_t r = perm ? static_cast<int64_t>(__ldg(perm + p)) : p;
-    if (r >= 0 && r < n) y[r] = acc;
-}
-
-// ---------------------------------------------------------------------------
-// CSR, G lanes per row
-// ---------------------------------------------------------------------------
-template <typename T, int G>
-__global__ void __launch_bounds__(256) k_csr_vector(int64_t count, const int32_t *__restrict__ rows,
-                                                   const int32_t *__restrict__ row_ptr,
-                                                   const int32_t *__restrict__ col, const T *__restrict__ val,
-                                                   const T *__restrict__ x, T *__restrict__ y) {
-    const int64_t sub = gtid() / G;
-    const int lane = threadIdx.x & (G - 1);
-    if (sub >= count) return;  // the G lanes of a group leave together
-    const int32_t r = rows ? __ldg(rows + sub) : static_cast<int32_t>(sub);
-    const int32_t b = __ldg(row_ptr + r), e = __ldg(row_ptr + r + 1);
-    T acc = T(0);
-    int32_t k = b + lane;
-    for (; k + G < e; k += 2 * G) {
-        const int32_t c0 = ld_stream(col + k), c1 = ld_stream(col + k + G);
-        const T v0 = ld_stream(val + k), v1 = ld_stream(val + k + G);
-        acc = fma(v0, ld_x(x + c0), acc);
-        acc = fma(v1, ld_x(x + c1), acc);
-    }
-    if (k < e) acc = fma(ld_stream(val + k), ld_x(x + ld_stream(col + k)), acc);
-    const unsigned mask =
-        (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << ((threadIdx.x & 31) & ~(G - 1)));
-#pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off, G);
-    if (lane == 0) y[r] = acc;
-}
+using namespace dev;
 
 // ---------------------------------------------------------------------------
 // CTA-wide segmented scan of (flag, value) pairs, one per thread, in thread order.
@@ -211,6 +84,19 @@ __device__ __forceinline__ T seg_scan_exclusive(int f, T v, SegScan<T, THREADS> 
 // ---------------------------------------------------------------------------
 // merge-path over a compact CSR (long rows, or the HEC spill)
 // ---------------------------------------------------------------------------
+// Shared-memory slot of path item i.  Thread t walks items t*kMergeIpt .. +kMergeIpt-1,
+// so a plain layout puts the 32 lanes of a warp kMergeIpt words apart (an 8- or
+// 16-way bank conflict).  One pad slot after every 32 (4-byte) / 16 (8-byte) items
+// spreads the lanes over all banks; the staging writes stay conflict-free.
+template <typename T>
+__device__ __forceinline__ int skew(int i) {
+    return i + (i >> (sizeof(T) == 8 ? 4 : 5));
+}
+template <typename T>
+__host__ __device__ constexpr int skewed_size(int n) {
+    return n + (n >> (sizeof(T) == 8 ? 4 : 5)) + 1;
+}
+
 // Stage the CTA's entries as products a_k * x[col_k] in shared memory: every
 // thread issues its (at most kMergeIpt) column/value loads first, then the gathers.
 template <typename T>
@@ -228,7 +114,7 @@ __device__ __forceinline__ void stage_products(const int32_t *__restrict__ col, 
 #pragma unroll
     for (int q = 0; q < kMergeIpt; ++q) {
         const int t = threadIdx.x + q * kMergeThreads;
-        if (t < nk) s_prod[t] = a[q] * ld_x(x + c[q]);
+        if (t < nk) s_prod[skew<T>(t)] = a[q] * ld_x(x + c[q]);
     }
 }
 
@@ -256,7 +142,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_path(
     const int32_t *__restrict__ col, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y,
     int32_t *__restrict__ carry_row, double *__restrict__ carry_val, int accumulate,
     const int32_t *__restrict__ part) {
-    __shared__ T s_prod[kMergeItems];
+    __shared__ T s_prod[skewed_size<T>(kMergeItems)];
     __shared__ int32_t s_end[kMergeItems];
     __shared__ int64_t s_coord[2];
     __shared__ SegScan<T, kMergeThreads> s_scan;
@@ -296,40 +182,38 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_path(
         else
             hi = mid;
     }
-    const int il0 = lo, kl0 = dl - lo;
-
-    int il = il0, kl = kl0, flag = 0;
-    T run = T(0);
+    // One walk over the thread's path items.  A row that starts and ends inside
+    // the thread is written at once; the first row the thread ends may have begun
+    // in earlier threads, so its value waits for the CTA scan.
+    int il = lo, kl = dl - lo;
+    int first = -1;
+    T first_val = T(0), run = T(0);
     for (int it = dl; it < dl_end; ++it) {
         if (il < ni && s_end[il] <= kl) {
-            flag = 1;
+            if (first < 0) {
+                first = il;
+                first_val = run;
+            } else {
+                const int32_t r = kIdentityRows ? static_cast<int32_t>(i0 + il) : __ldg(rows + i0 + il);
+                y[r] = accumulate ? y[r] + run : run;
+            }
             run = T(0);
             ++il;
         } else {
-            run += s_prod[kl];
+            run += s_prod[skew<T>(kl)];
             ++kl;
         }
     }
-    const int open_row = il;
+    const int flag = first >= 0;
     const T carry_in = seg_scan_exclusive<T, kMergeThreads>(flag, run, s_scan);
-
-    il = il0;
-    kl = kl0;
-    T acc = carry_in;
-    for (int it = dl; it < dl_end; ++it) {
-        if (il < ni && s_end[il] <= kl) {
-            const int32_t r = kIdentityRows ? static_cast<int32_t>(i0 + il) : __ldg(rows + i0 + il);
-            y[r] = accumulate ? y[r] + acc : acc;
-            acc = T(0);
-            ++il;
-        } else {
-            acc += s_prod[kl];
-            ++kl;
-        }
+    if (flag) {
+        const int32_t r = kIdentityRows ? static_cast<int32_t>(i0 + first) : __ldg(rows + i0 + first);
+        const T v = carry_in + first_val;
+        y[r] = accumulate ? y[r] + v : v;
     }
     if (threadIdx.x == kMergeThreads - 1) {
         const T inclusive = flag ? run : carry_in + run;
-        const int64_t i = i0 + open_row;
+        const int64_t i = i0 + il;
         if (i < n_rows) {
             carry_row[blockIdx.x] = kIdentityRows ? static_cast<int32_t>(i) : __ldg(rows + i);
             carry_val[blockIdx.x] = static_cast<double>(inclusive);
@@ -349,7 +233,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_coo(int64_t nnz, const int32_
                                                        const T *__restrict__ x, T *__restrict__ y,
                                                        int32_t *__restrict__ carry_row,
                                                        double *__restrict__ carry_val, int accumulate) {
-    __shared__ T s_prod[kMergeItems];
+    __shared__ T s_prod[skewed_size<T>(kMergeItems)];
     __shared__ int32_t s_row[kMergeItems + 1];
     __shared__ SegScan<T, kMergeThreads> s_scan;
     const int64_t k0 = static_cast<int64_t>(blockIdx.x) * kMergeItems;
@@ -364,24 +248,27 @@ __global__ void __launch_bounds__(kMergeThreads) k_coo(int64_t nnz, const int32_
     __syncthreads();
     const int b = min(static_cast<int>(threadIdx.x) * kMergeIpt, nk);
     const int e = min(b + kMergeIpt, nk);
-    int flag = 0;
-    T run = T(0);
+    int first = -1;
+    T first_val = T(0), run = T(0);
     for (int k = b; k < e; ++k) {
-        run += s_prod[k];
+        run += s_prod[skew<T>(k)];
         if (s_row[k] != s_row[k + 1]) {
-            flag = 1;
+            if (first < 0) {
+                first = k;
+                first_val = run;
+            } else {
+                const int32_t r = s_row[k];
+                y[r] = accumulate ? y[r] + run : run;
+            }
             run = T(0);
         }
     }
+    const int flag = first >= 0;
     const T carry_in = seg_scan_exclusive<T, kMergeThreads>(flag, run, s_scan);
-    T acc = carry_in;
-    for (int k = b; k < e; ++k) {
-        acc += s_prod[k];
-        if (s_row[k] != s_row[k + 1]) {
-            const int32_t r = s_row[k];
-            y[r] = accumulate ? y[r] + acc : acc;
-            acc = T(0);
-        }
+    if (flag) {
+        const int32_t r = s_row[first];
+        const T v = carry_in + first_val;
+        y[r] = accumulate ? y[r] + v : v;
     }
     if (threadIdx.x == kMergeThreads - 1) {
         const T inclusive = flag ? run : carry_in + run;
@@ -417,60 +304,10 @@ __global__ void k_carry_fixup(int64_t n_cta, const int32_t *__restrict__ carry_r
     if (lane == 0) y[r] = static_cast<T>(static_cast<double>(y[r]) + s);
 }
 
-template <typename T>
-cudaError_t csr_vector_dispatch(int g, int64_t count, const int32_t *rows, const int32_t *row_ptr,
-                                const int32_t *col, const T *val, const T *x, T *y, cudaStream_t s) {
-    if (count <= 0) return cudaSuccess;
-    const int64_t threads = count * g;
-    const unsigned grid = static_cast<unsigned>(ceil_div(threads, 256));
-    switch (g) {
-        case 2: k_csr_vector<T, 2><<<grid, 256, 0, s>>>(count, rows, row_ptr, col, val, x, y); break;
-        case 4: k_csr_vector<T, 4><<<grid, 256, 0, s>>>(count, rows, row_ptr, col, val, x, y); break;
-        case 8: k_csr_vector<T, 8><<<grid, 256, 0, s>>>(count, rows, row_ptr, col, val, x, y); break;
-        case 16: k_csr_vector<T, 16><<<grid, 256, 0, s>>>(count, rows, row_ptr, col, val, x, y); break;
-        case 32: k_csr_vector<T, 32><<<grid, 256, 0, s>>>(count, rows, row_ptr, col, val, x, y); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 int64_t merge_ctas(int64_t n_rows, int64_t nnz) { return ceil_div(n_rows + nnz, kMergeItems); }
 int64_t coo_ctas(int64_t nnz) { return ceil_div(nnz, kMergeItems); }
-
-template <typename T>
-cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const T *x, T *y, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>(ceil_div(sl.n_pos, kSellBlock));
-    const T *val = static_cast<const T *>(sl.val);
-    const bool sliced = sl.log2C < 31;
-    if (sliced && sl.C == 32)
-        k_sell<T, 32><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                  sl.perm, sl.col, val, x, y, n);
-    else if (sliced && sl.C == 64)
-        k_sell<T, 64><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                  sl.perm, sl.col, val, x, y, n);
-    else
-        k_sell<T, 0><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                 sl.perm, sl.col, val, x, y, n);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s) {
-    if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
-    if (dtype == SPMV_F64)
-        return sell_dispatch<double>(sl, n, static_cast<const double *>(x), static_cast<double *>(y), s);
-    return sell_dispatch<float>(sl, n, static_cast<const float *>(x), static_cast<float *>(y), s);
-}
-
-cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *rows, const int32_t *row_ptr,
-                              const int32_t *col, const void *val, const void *x, void *y, cudaStream_t s) {
-    if (dtype == SPMV_F64)
-        return csr_vector_dispatch<double>(g, count, rows, row_ptr, col, static_cast<const double *>(val),
-                                           static_cast<const double *>(x), static_cast<double *>(y), s);
-    return csr_vector_dispatch<float>(g, count, rows, row_ptr, col, static_cast<const float *>(val),
-                                      static_cast<const float *>(x), static_cast<float *>(y), s);
-}
 
 cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s) {
     if (sg.kind == 0 || sg.n_cta <= 0) return cudaSuccess;

@@ -206,7 +206,7 @@ cudaError_t launch_segment_to_csr(int dtype, const Segmented &sg, const int32_t 
                                   int32_t *out_col, void *out_val, cudaStream_t s);
 
 // ----------------------------------------------------------------------------
-// apply launchers -- apply.cu
+// apply launchers -- sell.cu, vector.cu, merge.cu
 // ----------------------------------------------------------------------------
 cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y,
                               cudaStream_t s);

@@ -70,10 +70,10 @@ def test_clock_summary_parsing():
 def test_traffic_is_null_when_kernel_changed(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
     (tmp_path / "traffic.json").write_text(json.dumps([
-        {"workload": "w", "dtype": "f64", "kernel": "sell", "apply_cu_sha": "0" * 16, "dram_bytes_per_launch": 5}]))
+        {"workload": "w", "dtype": "f64", "kernel": "sell", "source_sha": "0" * 16, "dram_bytes_per_launch": 5}]))
     assert bench.committed_traffic("w", "f64", "sell") is None
     (tmp_path / "traffic.json").write_text(json.dumps([
-        {"workload": "w", "dtype": "f64", "kernel": "sell", "apply_cu_sha": bench.apply_source_sha(),
+        {"workload": "w", "dtype": "f64", "kernel": "sell", "source_sha": bench.source_sha("sell"),
          "dram_bytes_per_launch": 5}]))
     assert bench.committed_traffic("w", "f64", "sell") == 5
 
