@@ -98,8 +98,9 @@ def load_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = {"sell": "sell.cu", "ell_r": "sell.cu", "hyb_ell": "sell.cu", "merge_path": "merge.cu",
-                  "coo_segmented": "merge.cu", "carry_fixup": "merge.cu"}
+KERNEL_SOURCES = {"sell": "sell.cu", "ell_r": "sell.cu", "hyb_ell": "sell.cu", "sell+rowsplit": "sell.cu",
+                  "ell_r+rowsplit": "sell.cu", "rowsplit_chunks": "sell.cu", "rowsplit_reduce": "sell.cu",
+                  "merge_path": "merge.cu", "coo_segmented": "merge.cu", "carry_fixup": "merge.cu"}
 
 
 def kernel_source(kernel: str) -> str:

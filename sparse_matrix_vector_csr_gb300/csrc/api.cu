@@ -62,12 +62,6 @@ int dev_alloc_n(spmv_handle_t h, T **p, int64_t count) {
     return st;
 }
 
-void dev_free(spmv_handle_t h, void *p) {
-    if (!p) return;
-    auto it = std::find(h->allocations.begin(), h->allocations.end(), p);
-    if (it != h->allocations.end()) h->allocations.erase(it);
-    cudaFree(p);
-}
 
 // Temporary device buffers of one build call, released when it returns.
 struct Temp {
@@ -138,8 +132,14 @@ const char *format_name(int f) {
 // the per-row error bound (about 4096 fp64 / 128 fp32 terms per thread)
 int32_t default_threshold(int format, int dtype) {
     if (format == SPMV_FMT_CSR_VECTOR) return dtype == SPMV_F64 ? 8192 : 4096;
-    return dtype == SPMV_F64 ? 4096 : 128;
+    // thread-per-row layouts: longer rows would stall their warp; they go to the
+    // row-split pass, which handles them with whole warps
+    (void)dtype;
+    return 128;
 }
+
+// HYB ELL width cap: one thread walks at most this many entries of a row
+int32_t hyb_width_cap(int dtype) { return dtype == SPMV_F64 ? 4096 : 128; }
 
 // ---------------------------------------------------------------------------
 // build context
@@ -207,6 +207,45 @@ int alloc_carries(BuildCtx &c, Segmented &sg) {
     return SPMV_OK;
 }
 
+// Row chunks of the row-split pass (kind 3) over the compact CSR in sg, plus the
+// partial-sum scratch it writes.
+int build_row_chunks(BuildCtx &c, Segmented &sg) {
+    spmv_handle_t h = c.h;
+    const int64_t m = sg.n_rows;
+    int64_t *count = nullptr, *cptr = nullptr, *scan_tmp = nullptr;
+    SPMV_TRY(c.temp.get(&count, m));
+    SPMV_TRY(c.temp.get(&cptr, m + 1));
+    SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(m)));
+    SPMV_TRY_CUDA(launch_chunk_counts(m, sg.ptr, count, c.s));
+    SPMV_TRY_CUDA(launch_exclusive_scan(count, m, cptr, scan_tmp, c.s));
+    int64_t total = 0;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&total, cptr + m, sizeof(int64_t), cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY(sync(c.s));
+    sg.n_chunks = total;
+    SPMV_TRY(dev_alloc_n(h, &sg.row_chunk_ptr, m + 1));
+    SPMV_TRY(dev_alloc_n(h, &sg.chunk_begin, total));
+    SPMV_TRY(dev_alloc_n(h, &sg.chunk_end, total));
+    SPMV_TRY(dev_alloc_n(h, &sg.chunk_row, total));
+    SPMV_TRY(dev_alloc_n(h, &sg.partial, total));
+    SPMV_TRY_CUDA(launch_chunk_fill(m, sg.ptr, cptr, sg.row_chunk_ptr, sg.chunk_begin, sg.chunk_end, sg.chunk_row,
+                                    c.s));
+    // rows cut into several chunks need the second (summing) launch
+    int64_t *flag = nullptr, *pos = nullptr;
+    SPMV_TRY(c.temp.get(&flag, m));
+    SPMV_TRY(c.temp.get(&pos, m + 1));
+    SPMV_TRY_CUDA(launch_multi_flags(m, count, flag, c.s));
+    SPMV_TRY_CUDA(launch_exclusive_scan(flag, m, pos, scan_tmp, c.s));
+    int64_t n_multi = 0;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&n_multi, pos + m, sizeof(int64_t), cudaMemcpyDeviceToHost, c.s));
+    SPMV_TRY(sync(c.s));
+    sg.n_multi = n_multi;
+    if (n_multi > 0) {
+        SPMV_TRY(dev_alloc_n(h, &sg.multi_rows, n_multi));
+        SPMV_TRY_CUDA(launch_multi_scatter(m, flag, pos, sg.multi_rows, c.s));
+    }
+    return SPMV_OK;
+}
+
 // Compact CSR of the listed rows, entries from in-row position `offset` on.
 int build_segment(BuildCtx &c, const int32_t *rows_dev, int64_t m, int32_t offset, int kind, int accumulate) {
     spmv_handle_t h = c.h;
@@ -238,6 +277,7 @@ int build_segment(BuildCtx &c, const int32_t *rows_dev, int64_t m, int32_t offse
     if (kind == 2) SPMV_TRY(dev_alloc_n(h, &sg.coo_row, total));
     SPMV_TRY_CUDA(launch_compact_copy(h->dtype, m, sg.rows, c.row_ptr, offset, c.col, c.val, cptr, sg.col, sg.val,
                                       sg.coo_row, c.s));
+    if (kind == 3) return build_row_chunks(c, sg);
     sg.n_cta = (kind == 1) ? merge_ctas(m, total) : coo_ctas(total);
     SPMV_TRY(alloc_carries(c, sg));
     return SPMV_OK;
@@ -252,7 +292,7 @@ int build_long_rows(BuildCtx &c, int accumulate) {
     SPMV_TRY(partition_rows(c, 0, c.threshold, 0, rows, start));
     const int64_t m = start[2] - start[1];
     if (m != c.n_long) return set_error(SPMV_ERR_CUDA, "long-row partition count mismatch");
-    return build_segment(c, rows + start[1], m, 0, 1, accumulate);
+    return build_segment(c, rows + start[1], m, 0, 3, accumulate);
 }
 
 // ---------------------------------------------------------------------------
@@ -372,16 +412,6 @@ int fill_sliced(BuildCtx &c) {
     return SPMV_OK;
 }
 
-void release_sliced(spmv_handle_t h) {
-    Sliced &sl = h->sliced;
-    dev_free(h, sl.perm);
-    dev_free(h, sl.len);
-    dev_free(h, sl.width);
-    dev_free(h, sl.slice_ptr);
-    dev_free(h, sl.col);
-    dev_free(h, sl.val);
-    sl = Sliced();
-}
 
 // ---------------------------------------------------------------------------
 // per-format builds
@@ -400,9 +430,15 @@ int build_sell_like(BuildCtx &c, int format, int32_t C, int64_t sigma) {
         SPMV_TRY(plan_sliced(c, clip, C, sigma, 0, c.max_short));
     }
     h->sliced.stored_entries = h->nnz - c.long_nnz;
+    if (c.n_long > 0) {
+        // long rows: the sliced pass leaves their y entries to the row-split pass
+        SPMV_TRY_CUDA(launch_mark_long(h->sliced.n_pos, h->sliced.perm, c.len, h->n, c.threshold, h->sliced.len,
+                                       c.s));
+    }
     SPMV_TRY(fill_sliced(c));
-    SPMV_TRY(build_long_rows(c, 1));
-    h->kernels.push_back(format == SPMV_FMT_ELL_R ? "ell_r" : "sell");
+    SPMV_TRY(build_long_rows(c, 0));
+    const std::string name = format == SPMV_FMT_ELL_R ? "ell_r" : "sell";
+    h->kernels.push_back(h->seg.kind == 3 ? name + "+rowsplit" : name);
     return SPMV_OK;
 }
 
@@ -479,7 +515,7 @@ int build_csr_vector(BuildCtx &c, int32_t forced_g) {
         }
         if (c.n_long > 0) {
             if (start[7] - start[6] != c.n_long) return set_error(SPMV_ERR_CUDA, "long-row bin count mismatch");
-            SPMV_TRY(build_segment(c, h->bin_rows + start[6], c.n_long, 0, 1, 0));
+            SPMV_TRY(build_segment(c, h->bin_rows + start[6], c.n_long, 0, 3, 0));
         }
     }
     for (const Bin &b : h->bins) h->kernels.push_back("csr_vector_g" + std::to_string(b.g));
@@ -598,31 +634,16 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     int64_t sigma = prm.sigma > 0 ? prm.sigma : 1;
 
     if (format == SPMV_FMT_AUTO) {
-        // natural-order SELL-32 when it pads little, else sorted windows of 256 rows,
-        // else one subwarp group per row
+        // SELL-32 in natural order when that pads little (it keeps x and y accesses in
+        // row order); otherwise rows sorted by length over the whole matrix (pJDS), so
+        // every slice holds rows of nearly equal length.  Long rows go to the row-split
+        // pass in both cases.
         int64_t slots1 = 0;
         SPMV_TRY(probe_sigma1_slots(c, &slots1));
         const int64_t stored = nnz - c.long_nnz;
-        if (static_cast<double>(slots1) <= 1.10 * static_cast<double>(stored) + 32.0 * 64) {
-            format = SPMV_FMT_SELL;
-            C = 32;
-            sigma = 1;
-        } else {
-            format = SPMV_FMT_SELL;
-            C = 32;
-            sigma = 256;
-            int32_t *clip = nullptr;
-            SPMV_TRY(c.temp.get(&clip, n));
-            SPMV_TRY_CUDA(launch_clip_long(n, c.len, c.threshold, clip, c.s));
-            SPMV_TRY(plan_sliced(c, clip, C, sigma, 0, c.max_short));
-            const bool good = static_cast<double>(h->sliced.slots) <= 1.10 * static_cast<double>(stored) + 32.0 * 64;
-            release_sliced(h);
-            if (!good) {
-                // irregular row lengths: equal work shares per CTA regardless of rows
-                format = SPMV_FMT_MERGE;
-                c.threshold = -1;
-            }
-        }
+        format = SPMV_FMT_SELL;
+        C = 32;
+        sigma = static_cast<double>(slots1) <= 1.10 * static_cast<double>(stored) + 32.0 * 64 ? 1 : std::max<int64_t>(n, 1);
     }
     h->format = format;
     h->params = prm;
@@ -652,7 +673,7 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
             SPMV_TRY(build_merge(c));
             break;
         case SPMV_FMT_HYB: {
-            const int32_t cap = default_threshold(SPMV_FMT_SELL, h->dtype);
+            const int32_t cap = hyb_width_cap(h->dtype);
             int32_t K = prm.K >= 0 ? prm.K : hyb_auto_width(c, h->dtype, n, cap);
             const int spill_csr = prm.spill_csr >= 0 ? (prm.spill_csr ? 1 : 0) : 1;
             h->params.K = K;
@@ -666,7 +687,11 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     }
     if (h->seg.kind == 1) h->kernels.push_back("merge_path");
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
-    if (h->seg.kind != 0 && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
+    if ((h->seg.kind == 1 || h->seg.kind == 2) && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
+    if (h->seg.kind == 3) {
+        if (!h->sliced.present) h->kernels.push_back("rowsplit_chunks");
+        if (h->seg.n_multi > 0) h->kernels.push_back("rowsplit_reduce");
+    }
     return sync(c.s);
 }
 
@@ -695,17 +720,28 @@ struct Recorder {
 
 int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *rec) {
     if (rec) SPMV_TRY(rec->mark(s));
+    const bool split = h->seg.kind == 3;
     if (h->format == SPMV_FMT_CSR_VECTOR) {
         for (const Bin &b : h->bins) {
             SPMV_TRY_CUDA(launch_csr_vector(h->dtype, b.g, b.count, h->bin_rows ? h->bin_rows + b.offset : nullptr,
                                             h->row_ptr, h->csr_col, h->csr_val, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
+        if (split) {
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s, 1));
+            if (rec) SPMV_TRY(rec->mark(s));
+        }
     } else if (h->sliced.present) {
-        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, x, y, s));
+        // sliced rows (and, in the same launch, the chunks of the long rows)
+        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &h->seg : nullptr, x, y, s));
         if (rec) SPMV_TRY(rec->mark(s));
     }
-    if (h->seg.kind != 0) {
+    if (split) {
+        if (h->seg.n_multi > 0) {
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s, 2));
+            if (rec) SPMV_TRY(rec->mark(s));
+        }
+    } else if (h->seg.kind != 0) {
         SPMV_TRY_CUDA(launch_segmented(h->dtype, h->seg, x, y, s));
         if (rec) SPMV_TRY(rec->mark(s));
         if (h->seg.n_cta > 1) {
@@ -953,8 +989,8 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
            (long long)sl.stored_entries, (long long)sl.ld, sl.max_width, sl.perm ? "true" : "false");
     append(o, "\"n_long_rows\":%lld,\"long_nnz\":%lld,", (long long)h->n_long_rows, (long long)h->long_nnz);
     append(o, "\"segment\":\"%s\",\"segment_rows\":%lld,\"segment_nnz\":%lld,\"segment_ctas\":%lld,",
-           sg.kind == 0 ? "none" : sg.kind == 1 ? "csr_merge_path" : "coo", (long long)sg.n_rows, (long long)sg.nnz,
-           (long long)sg.n_cta);
+           sg.kind == 0 ? "none" : sg.kind == 1 ? "csr_merge_path" : sg.kind == 2 ? "coo" : "row_split",
+           (long long)sg.n_rows, (long long)sg.nnz, (long long)(sg.kind == 3 ? sg.n_chunks : sg.n_cta));
     o += "\"bins\":[";
     for (size_t i = 0; i < h->bins.size(); ++i)
         append(o, "%s[%d,%lld]", i ? "," : "", h->bins[i].g, (long long)h->bins[i].count);
@@ -972,6 +1008,7 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     }
     if (sg.kind == 1) matrix_bytes += sg.nnz * (vb + 4) + sg.n_rows * (sg.rows ? 8 : 4) + sg.n_cta * 16;
     if (sg.kind == 2) matrix_bytes += sg.nnz * (vb + 8) + sg.n_cta * 12;
+    if (sg.kind == 3) matrix_bytes += sg.nnz * (vb + 4) + sg.n_rows * 8 + sg.n_chunks * 16;
     append(o, "\"format_bytes\":%lld,\"vector_bytes\":%lld}", (long long)matrix_bytes, (long long)(2 * h->n * vb));
     std::snprintf(json, cap, "%s", o.c_str());
     if (o.size() + 1 > cap) return set_error(SPMV_ERR_INVALID_ARG, "describe buffer too small");

@@ -18,6 +18,8 @@ namespace {
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
+__device__ __forceinline__ int64_t ceil_div_dev(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 __device__ __forceinline__ int64_t gtid() {
     return static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
 }
@@ -125,6 +127,14 @@ __global__ void k_clip_long(int64_t n, const int32_t *__restrict__ len, int32_t 
     for (int64_t i = gtid(); i < n; i += gstride()) {
         int32_t l = len[i];
         out[i] = (threshold >= 0 && l > threshold) ? 0 : l;
+    }
+}
+
+__global__ void k_mark_long(int64_t n_pos, const int32_t *__restrict__ perm, const int32_t *__restrict__ len,
+                            int64_t n, int32_t threshold, int32_t *__restrict__ len_sorted) {
+    for (int64_t p = gtid(); p < n_pos && p < n; p += gstride()) {
+        const int32_t r = perm ? perm[p] : static_cast<int32_t>(p);
+        if (len[r] > threshold) len_sorted[p] = -1;
     }
 }
 
@@ -469,6 +479,44 @@ __global__ void k_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *__
     }
 }
 
+__global__ void k_chunk_counts(int64_t m, const int32_t *__restrict__ ptr, int64_t *__restrict__ count) {
+    for (int64_t i = gtid(); i < m; i += gstride()) {
+        const int64_t len = static_cast<int64_t>(ptr[i + 1]) - ptr[i];
+        count[i] = len > 0 ? ceil_div_dev(len, kSplitChunk) : 1;
+    }
+}
+
+__global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, const int64_t *__restrict__ cptr,
+                             int32_t *__restrict__ row_chunk_ptr, int32_t *__restrict__ chunk_begin,
+                             int32_t *__restrict__ chunk_end, int32_t *__restrict__ chunk_row) {
+    for (int64_t i = gtid(); i < m; i += gstride()) {
+        const int32_t a = ptr[i], b = ptr[i + 1];
+        int64_t c = cptr[i];
+        const bool single = cptr[i + 1] - c == 1;
+        row_chunk_ptr[i] = static_cast<int32_t>(c);
+        if (i == m - 1) row_chunk_ptr[m] = static_cast<int32_t>(cptr[m]);
+        int32_t k = a;
+        do {
+            const int32_t e = (b - k > kSplitChunk) ? k + kSplitChunk : b;
+            chunk_begin[c] = k;
+            chunk_end[c] = e;
+            chunk_row[c] = single ? ~static_cast<int32_t>(i) : static_cast<int32_t>(i);
+            ++c;
+            k = e;
+        } while (k < b);
+    }
+}
+
+__global__ void k_multi_flags(int64_t m, const int64_t *__restrict__ count, int64_t *__restrict__ flag) {
+    for (int64_t i = gtid(); i < m; i += gstride()) flag[i] = count[i] > 1 ? 1 : 0;
+}
+
+__global__ void k_multi_scatter(int64_t m, const int64_t *__restrict__ flag, const int64_t *__restrict__ pos,
+                                int32_t *__restrict__ multi) {
+    for (int64_t i = gtid(); i < m; i += gstride())
+        if (flag[i]) multi[pos[i]] = static_cast<int32_t>(i);
+}
+
 // ---------------------------------------------------------------------------
 // to_csr
 // ---------------------------------------------------------------------------
@@ -532,6 +580,13 @@ cudaError_t launch_histogram(int64_t n, const int32_t *len, int32_t threshold, i
 
 cudaError_t launch_clip_long(int64_t n, const int32_t *len, int32_t threshold, int32_t *out, cudaStream_t s) {
     if (n > 0) k_clip_long<<<grid_for(n, kBlock, 65536), kBlock, 0, s>>>(n, len, threshold, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mark_long(int64_t n_pos, const int32_t *perm, const int32_t *len, int64_t n, int32_t threshold,
+                             int32_t *len_sorted, cudaStream_t s) {
+    if (n_pos > 0 && n > 0)
+        k_mark_long<<<grid_for(n_pos, kBlock, 65536), kBlock, 0, s>>>(n_pos, perm, len, n, threshold, len_sorted);
     return cudaGetLastError();
 }
 
@@ -653,6 +708,29 @@ cudaError_t launch_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *p
     return cudaGetLastError();
 }
 
+cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int64_t *count, cudaStream_t s) {
+    if (m > 0) k_chunk_counts<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, const int64_t *cptr, int32_t *row_chunk_ptr,
+                              int32_t *chunk_begin, int32_t *chunk_end, int32_t *chunk_row, cudaStream_t s) {
+    if (m > 0)
+        k_chunk_fill<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, cptr, row_chunk_ptr, chunk_begin, chunk_end,
+                                                                  chunk_row);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_multi_flags(int64_t m, const int64_t *count, int64_t *flag, cudaStream_t s) {
+    if (m > 0) k_multi_flags<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, count, flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_multi_scatter(int64_t m, const int64_t *flag, const int64_t *pos, int32_t *multi, cudaStream_t s) {
+    if (m > 0) k_multi_scatter<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, flag, pos, multi);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const int32_t *out_ptr, int32_t *out_col,
                                  void *out_val, cudaStream_t s) {
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
@@ -670,7 +748,7 @@ cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const i
 
 cudaError_t launch_segment_to_csr(int dtype, const Segmented &sg, const int32_t *out_ptr, int32_t *out_col,
                                   void *out_val, cudaStream_t s) {
-    if (sg.kind == 0 || sg.n_rows <= 0) return cudaSuccess;
+    if (sg.kind == 0 || sg.n_rows <= 0) return cudaSuccess;  // kinds 1-3 all hold a compact CSR
     unsigned g = grid_for(sg.n_rows * 32, kBlock, 1 << 20);
     if (dtype == SPMV_F64)
         k_segment_to_csr<double><<<g, kBlock, 0, s>>>(sg.n_rows, sg.rows, sg.ptr, sg.col,

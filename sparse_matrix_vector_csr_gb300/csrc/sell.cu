@@ -3,6 +3,15 @@
 // loaded or multiplied (ELLPACK-R of the GPGPU spMVM paper, arXiv 1112.5588,
 // ELLPACK-R section; the "early stopping" quoted in the scite report
 // "Load-balancing Sparse Matrix Vector Product Kernels on GPUs").
+//
+// Long rows leave the sliced layout for the row-split pass (the "very long rows"
+// scheme of the Trilinos issue on unpackAndCombine: over rows, then over blocks of
+// entries within a row, then over entries within a block): every long row is cut
+// into chunks of at most kSplitChunk entries and one warp reduces one chunk.  A row
+// with a single chunk is written at once; the partials of longer rows are summed in
+// double by one warp per row.  Work per warp is bounded whatever the row lengths;
+// no atomics; fixed summation order.  The sliced rows and the chunks write disjoint
+// rows of y, so both run in one launch.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,93 +39,231 @@ struct SellChunk {
     static constexpr int U = (sizeof(T) == 8 || CS == 0) ? 4 : 8;
 };
 
+struct SellArgs {
+    int64_t n_pos;
+    int log2C;
+    uint32_t cmask;
+    int64_t stride;
+    const int64_t *slice_ptr;
+    const int32_t *len;   // -1 marks a long row (handled by the row-split pass)
+    const int32_t *perm;  // nullptr = natural order
+    const int32_t *col;
+    int64_t n;
+};
+
+struct SplitArgs {
+    int64_t n_chunks;
+    const int32_t *chunk_begin;
+    const int32_t *chunk_end;
+    const int32_t *chunk_row;  // compact row, or ~row when it is the row's only chunk
+    const int32_t *rows;       // compact row -> matrix row
+    const int32_t *col;
+    double *partial;
+    int accumulate;
+};
+
 // CS > 0: SELL with a compile-time slice height CS (stride = CS).
 // CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
 //          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
 template <typename T, int CS>
-__global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6) k_sell(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
-                                                        const int64_t *__restrict__ slice_ptr,
-                                                        const int32_t *__restrict__ len,
-                                                        const int32_t *__restrict__ perm,
-                                                        const int32_t *__restrict__ col, const T *__restrict__ val,
-                                                        const T *__restrict__ x, T *__restrict__ y, int64_t n) {
+__device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
+                                         const T *__restrict__ x, T *__restrict__ y) {
     constexpr int U = SellChunk<T, CS>::U;
-    const int64_t p = gtid();
-    if (p >= n_pos) return;
-    const int w = __ldg(len + p);
+    const int w = __ldg(a.len + p);
     const uint64_t up = static_cast<uint64_t>(p);
-    const int64_t slot = CS > 0 ? __ldg(slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
-                                : __ldg(slice_ptr + (p >> log2C)) + static_cast<int64_t>(p & cmask);
-    const int32_t *cp = col + slot;
-    const T *vp = val + slot;
+    const int64_t slot = CS > 0 ? __ldg(a.slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
+                                : __ldg(a.slice_ptr + (p >> a.log2C)) + static_cast<int64_t>(p & a.cmask);
+    const int32_t *__restrict__ cp = a.col + slot;
+    const T *__restrict__ vp = val + slot;
     T acc = T(0);
     if constexpr (CS > 0) {
         for (int j = 0; j < w; j += U) {
             int32_t c[U];
-            T a[U];
+            T v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const bool on = j + u < w;
                 c[u] = on ? ld_stream(cp + u * CS) : 0;
-                a[u] = on ? ld_stream(vp + u * CS) : T(0);
+                v[u] = on ? ld_stream(vp + u * CS) : T(0);
             }
             T xv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc = fma(a[u], xv[u], acc);  // inactive slots add +0 * +0
+            for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);  // inactive slots add +0 * +0
             cp += U * CS;
             vp += U * CS;
         }
     } else {
         // the leading dimension of an ELL part is below 2^31: 32-bit offsets inside a chunk
-        const int ld = static_cast<int>(stride);
+        const int ld = static_cast<int>(a.stride);
         for (int j = 0; j < w; j += U) {
             int32_t c[U];
-            T a[U];
+            T v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const bool on = j + u < w;
                 c[u] = on ? ld_stream(cp + u * ld) : 0;
-                a[u] = on ? ld_stream(vp + u * ld) : T(0);
+                v[u] = on ? ld_stream(vp + u * ld) : T(0);
             }
             T xv[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc = fma(a[u], xv[u], acc);
+            for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);
             cp += static_cast<int64_t>(U) * ld;
             vp += static_cast<int64_t>(U) * ld;
         }
     }
-    const int64_t r = perm ? static_cast<int64_t>(__ldg(perm + p)) : p;
-    if (r >= 0 && r < n) y[r] = acc;
+    const int64_t r = a.perm ? static_cast<int64_t>(__ldg(a.perm + p)) : p;
+    if (w >= 0 && r >= 0 && r < a.n) y[r] = acc;
+}
+
+// One warp reduces chunk c of a long row.
+template <typename T>
+__device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs &a, const T *__restrict__ val,
+                                            const T *__restrict__ x, T *__restrict__ y) {
+    constexpr int U = 4;
+    const int32_t b = __ldg(a.chunk_begin + c), e = __ldg(a.chunk_end + c);
+    T acc = T(0);
+    for (int32_t k = b + lane; k < e; k += 32 * U) {
+        int32_t cc[U];
+        T v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool on = k + 32 * u < e;
+            cc[u] = on ? ld_stream(a.col + k + 32 * u) : 0;
+            v[u] = on ? ld_stream(val + k + 32 * u) : T(0);
+        }
+        T xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) xv[u] = (k + 32 * u < e) ? ld_x(x + cc[u]) : T(0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);
+    }
+    double s = static_cast<double>(acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) {
+        const int32_t cr = __ldg(a.chunk_row + c);
+        if (cr < 0) {
+            const int32_t r = __ldg(a.rows + ~cr);
+            y[r] = a.accumulate ? static_cast<T>(static_cast<double>(y[r]) + s) : static_cast<T>(s);
+        } else {
+            a.partial[c] = s;
+        }
+    }
+}
+
+template <typename T, int CS>
+__global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
+    k_sell(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y) {
+    const int64_t p = gtid();
+    if (p < a.n_pos) sell_row<T, CS>(p, a, val, x, y);
+}
+
+// Sliced rows and row-split chunks in one launch: the first split_ctas CTAs take
+// eight chunks each (one per warp), the rest take kSellBlock row positions each.
+template <typename T, int CS>
+__global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
+    k_sell_split(SellArgs a, const T *__restrict__ val, SplitArgs b, const T *__restrict__ split_val,
+                 int64_t split_ctas, const T *__restrict__ x, T *__restrict__ y) {
+    if (blockIdx.x < split_ctas) {
+        const int64_t c = (static_cast<int64_t>(blockIdx.x) * kSellBlock + threadIdx.x) >> 5;
+        if (c < b.n_chunks) split_chunk<T>(c, threadIdx.x & 31, b, split_val, x, y);
+        return;
+    }
+    const int64_t p = (static_cast<int64_t>(blockIdx.x) - split_ctas) * kSellBlock + threadIdx.x;
+    if (p < a.n_pos) sell_row<T, CS>(p, a, val, x, y);
+}
+
+// Row-split chunks alone (long rows next to the CSR-vector bins).
+template <typename T>
+__global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__restrict__ val, const T *__restrict__ x,
+                                                     T *__restrict__ y) {
+    const int64_t c = gtid() >> 5;
+    if (c < b.n_chunks) split_chunk<T>(c, threadIdx.x & 31, b, val, x, y);
+}
+
+// One warp per long row cut into several chunks: sum its partials in double.
+template <typename T>
+__global__ void __launch_bounds__(256) k_split_reduce(int64_t n_multi, const int32_t *__restrict__ multi_rows,
+                                                     const int32_t *__restrict__ rows,
+                                                     const int32_t *__restrict__ row_chunk_ptr,
+                                                     const double *__restrict__ partial, T *__restrict__ y,
+                                                     int accumulate) {
+    const int64_t w = gtid() >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= n_multi) return;
+    const int32_t i = __ldg(multi_rows + w);
+    const int32_t a = __ldg(row_chunk_ptr + i), b = __ldg(row_chunk_ptr + i + 1);
+    double s = 0.0;
+    for (int32_t c = a + lane; c < b; c += 32) s += partial[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) {
+        const int32_t r = __ldg(rows + i);
+        y[r] = accumulate ? static_cast<T>(static_cast<double>(y[r]) + s) : static_cast<T>(s);
+    }
+}
+
+SellArgs sell_args(const Sliced &sl, int64_t n) {
+    return SellArgs{sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len, sl.perm, sl.col, n};
+}
+
+SplitArgs split_args(const Segmented &sg) {
+    return SplitArgs{sg.n_chunks, sg.chunk_begin, sg.chunk_end, sg.chunk_row, sg.rows, sg.col, sg.partial,
+                     sg.accumulate};
+}
+
+template <typename T, int CS>
+cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
+    const T *val = static_cast<const T *>(sl.val);
+    const int64_t sell_ctas = ceil_div(sl.n_pos, kSellBlock);
+    if (sg && sg->kind == 3 && sg->n_chunks > 0) {
+        const int64_t split_ctas = ceil_div(sg->n_chunks * 32, kSellBlock);
+        k_sell_split<T, CS><<<static_cast<unsigned>(split_ctas + sell_ctas), kSellBlock, 0, s>>>(
+            sell_args(sl, n), val, split_args(*sg), static_cast<const T *>(sg->val), split_ctas, x, y);
+    } else {
+        k_sell<T, CS><<<static_cast<unsigned>(sell_ctas), kSellBlock, 0, s>>>(sell_args(sl, n), val, x, y);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
+    const bool sliced = sl.log2C < 31;
+    if (sliced && sl.C == 32) return sell_launch<T, 32>(sl, n, sg, x, y, s);
+    if (sliced && sl.C == 64) return sell_launch<T, 64>(sl, n, sg, x, y, s);
+    return sell_launch<T, 0>(sl, n, sg, x, y, s);
+}
+
+template <typename T>
+cudaError_t split_dispatch(const Segmented &sg, const T *x, T *y, cudaStream_t s, int which) {
+    if (sg.kind != 3 || sg.n_chunks <= 0) return cudaSuccess;
+    if (which & 1)
+        k_split_chunks<T><<<static_cast<unsigned>(ceil_div(sg.n_chunks * 32, 256)), 256, 0, s>>>(
+            split_args(sg), static_cast<const T *>(sg.val), x, y);
+    if ((which & 2) && sg.n_multi > 0)
+        k_split_reduce<T><<<static_cast<unsigned>(ceil_div(sg.n_multi * 32, 256)), 256, 0, s>>>(
+            sg.n_multi, sg.multi_rows, sg.rows, sg.row_chunk_ptr, sg.partial, y, sg.accumulate);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-template <typename T>
-cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const T *x, T *y, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>(ceil_div(sl.n_pos, kSellBlock));
-    const T *val = static_cast<const T *>(sl.val);
-    const bool sliced = sl.log2C < 31;
-    if (sliced && sl.C == 32)
-        k_sell<T, 32><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                  sl.perm, sl.col, val, x, y, n);
-    else if (sliced && sl.C == 64)
-        k_sell<T, 64><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                  sl.perm, sl.col, val, x, y, n);
-    else
-        k_sell<T, 0><<<grid, kSellBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len,
-                                                 sl.perm, sl.col, val, x, y, n);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s) {
+cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segmented *split, const void *x, void *y,
+                              cudaStream_t s) {
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
     if (dtype == SPMV_F64)
-        return sell_dispatch<double>(sl, n, static_cast<const double *>(x), static_cast<double *>(y), s);
-    return sell_dispatch<float>(sl, n, static_cast<const float *>(x), static_cast<float *>(y), s);
+        return sell_dispatch<double>(sl, n, split, static_cast<const double *>(x), static_cast<double *>(y), s);
+    return sell_dispatch<float>(sl, n, split, static_cast<const float *>(x), static_cast<float *>(y), s);
+}
+
+cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s, int which) {
+    if (dtype == SPMV_F64)
+        return split_dispatch<double>(sg, static_cast<const double *>(x), static_cast<double *>(y), s, which);
+    return split_dispatch<float>(sg, static_cast<const float *>(x), static_cast<float *>(y), s, which);
 }
 
 }  // namespace spmv

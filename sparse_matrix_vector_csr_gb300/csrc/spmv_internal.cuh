@@ -22,6 +22,7 @@ constexpr int kMergeIpt = 8;                // path items per thread
 constexpr int kMergeItems = kMergeThreads * kMergeIpt;
 constexpr int kHistCap = 4096;              // row-length histogram: buckets 0..kHistCap-1, last = ">= kHistCap"
 constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows are sorted in one CTA
+constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows
 
 // ----------------------------------------------------------------------------
 // format parts
@@ -54,7 +55,8 @@ struct Sliced {
 };
 
 // Rows handled by the segmented pass: the long rows taken out of a format, or
-// the HYB spill.  kind 1 = compact CSR walked by merge-path, kind 2 = COO.
+// the HYB spill.  kind 1 = compact CSR walked by merge-path, kind 2 = COO,
+// kind 3 = compact CSR cut into row chunks (row-split pass).
 struct Segmented {
     int kind = 0;
     int64_t n_rows = 0;
@@ -68,6 +70,14 @@ struct Segmented {
     int32_t *carry_row = nullptr;  // [n_cta] row left open at the end of each CTA (-1 = none)
     double *carry_val = nullptr;   // [n_cta] its partial sum
     int32_t *part = nullptr;       // [n_cta + 1] merge-path split of every CTA boundary (kind 1)
+    int64_t n_chunks = 0;          // kind 3: chunks of at most kSplitChunk entries, none crossing a row
+    int32_t *chunk_begin = nullptr;    // [n_chunks] first entry of each chunk (compact CSR index)
+    int32_t *chunk_end = nullptr;      // [n_chunks] one past its last entry
+    int32_t *row_chunk_ptr = nullptr;  // [n_rows + 1] chunks of compact row i
+    int32_t *chunk_row = nullptr;      // [n_chunks] compact row of the chunk; ~row if it is the row's only chunk
+    int64_t n_multi = 0;               // compact rows cut into more than one chunk
+    int32_t *multi_rows = nullptr;     // [n_multi] those rows (compact indices)
+    double *partial = nullptr;         // [n_chunks] partial sums (scratch of the pass)
     int accumulate = 1;            // 1: add into y (y written before), 0: write y
     int32_t dst_offset = 0;        // in-row position of the first held entry (K for the spill)
 };
@@ -152,6 +162,9 @@ cudaError_t launch_histogram(int64_t n, const int32_t *len, int32_t threshold, i
 // out[i] = 0 for rows longer than threshold (threshold < 0: no cut), else len[i].
 cudaError_t launch_clip_long(int64_t n, const int32_t *len, int32_t threshold, int32_t *out,
                              cudaStream_t s);
+// len_sorted[p] = -1 where the row at sorted position p is longer than threshold
+cudaError_t launch_mark_long(int64_t n_pos, const int32_t *perm, const int32_t *len, int64_t n, int32_t threshold,
+                             int32_t *len_sorted, cudaStream_t s);
 cudaError_t launch_min_len(int64_t n, const int32_t *len, int32_t K, int32_t *out, cudaStream_t s);
 
 // Exclusive scan of int64 values: out[i] = sum in[0..i), out has n+1 entries.
@@ -199,6 +212,15 @@ cudaError_t launch_compact_copy(int dtype, int64_t m, const int32_t *rows, const
                                 const int64_t *cptr, int32_t *col_out, void *val_out,
                                 int32_t *coo_row, cudaStream_t s);
 
+// row chunks of a compact CSR: count[i] = ceil(len_i / kSplitChunk) (at least 1)
+cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int64_t *count, cudaStream_t s);
+cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, const int64_t *cptr, int32_t *row_chunk_ptr,
+                              int32_t *chunk_begin, int32_t *chunk_end, int32_t *chunk_row, cudaStream_t s);
+// flag[i] = 1 when compact row i has more than one chunk; after an exclusive scan
+// of the flags into pos, multi[pos[i]] = i for the flagged rows
+cudaError_t launch_multi_flags(int64_t m, const int64_t *count, int64_t *flag, cudaStream_t s);
+cudaError_t launch_multi_scatter(int64_t m, const int64_t *flag, const int64_t *pos, int32_t *multi, cudaStream_t s);
+
 // to_csr
 cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const int32_t *out_ptr,
                                  int32_t *out_col, void *out_val, cudaStream_t s);
@@ -208,13 +230,16 @@ cudaError_t launch_segment_to_csr(int dtype, const Segmented &sg, const int32_t 
 // ----------------------------------------------------------------------------
 // apply launchers -- sell.cu, vector.cu, merge.cu
 // ----------------------------------------------------------------------------
-cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y,
+// split: the row-split pass of the long rows (kind 3) to run in the same launch, or nullptr
+cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segmented *split, const void *x, void *y,
                               cudaStream_t s);
 cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *rows,
                               const int32_t *row_ptr, const int32_t *col, const void *val,
                               const void *x, void *y, cudaStream_t s);
 cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
+// row-split pass (kind 3): which & 1 = chunks alone, which & 2 = sums of rows cut into several chunks
+cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s, int which);
 // merge-path over a whole CSR (row i of the path is matrix row i), writing y
 cudaError_t launch_merge_path_identity(int dtype, int64_t n_rows, int64_t nnz, const int32_t *ptr,
                                        const int32_t *col, const void *val, const void *x, void *y,
