@@ -99,7 +99,7 @@ def load_peaks() -> tuple[float, str]:
 
 
 KERNEL_SOURCES = {"sell": "sell.cu", "ell_r": "sell.cu", "hyb_ell": "sell.cu", "sell+rowsplit": "sell.cu",
-                  "ell_r+rowsplit": "sell.cu", "rowsplit_chunks": "sell.cu", "rowsplit_reduce": "sell.cu",
+                  "ell_r+rowsplit": "sell.cu", "rowsplit_chunks": "sell.cu",
                   "merge_path": "merge.cu", "coo_segmented": "merge.cu", "carry_fixup": "merge.cu"}
 
 
@@ -450,6 +450,64 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+SWEEP_FORMATS = [
+    ("auto", {}), ("csr_vector", {}), ("ell_r", {}),
+    ("sell", {"C": 32, "sigma": 1}), ("sell", {"C": 64, "sigma": 1}), ("sell", {"C": 32, "sigma": 256}),
+    ("sell", {"C": 64, "sigma": 256}), ("sell", {"C": 32, "sigma": 1 << 30}), ("sell", {"C": 64, "sigma": 1 << 30}),
+    ("hyb", {}), ("hyb", {"spill_csr": 0}), ("hyb", {"K": 20}), ("merge", {}),
+]
+
+
+def run_sweep(args):
+    """One JSON line per storage format on the chosen workload (format comparison)."""
+    import numpy as np
+    import torch
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+    from workloads import WORKLOADS, make_workload
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = load_peaks()
+    dtypes = [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+    for dt in dtypes:
+        csr, x_np = make_workload(args.workload, dtype=dt)
+        sv = csr.vals.dtype.itemsize
+        beff = effective_bytes(csr.n, csr.nnz, sv)
+        dev = torch.device("cuda", 0)
+        rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
+        x = torch.from_numpy(x_np).to(dev)
+        y = torch.empty_like(x)
+        for fmt, params in SWEEP_FORMATS:
+            rec = {"workload": args.workload, "dtype": "f64" if sv == 8 else "f32", "format": fmt, "params": params}
+            try:
+                A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=fmt, **params)
+            except spmv.SpmvError as e:
+                rec["error"] = str(e)
+                print(json.dumps(rec), flush=True)
+                continue
+            apply_c = spmv._abi.lib.spmv_apply
+            call = (A._h, x.data_ptr(), y.data_ptr(), None)
+            for _ in range(args.warmup):
+                apply_c(*call)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            steps = max(args.steps // 100, 20)
+            e0.record()
+            for _ in range(steps):
+                apply_c(*call)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            d = A.describe()
+            rec.update({"chosen": d["format"], "C": d["C"], "sigma": d["sigma"], "K": d["K"],
+                        "us_per_apply": ms * 1e3, "gflops": 2.0 * csr.nnz / ms / 1e6,
+                        "effective_gbs": beff / ms / 1e6, "frac": beff / ms / 1e6 / peak,
+                        "peak": f"{peak} GB/s {peak_kind}", "slots_per_nnz": d["slots"] / max(csr.nnz, 1),
+                        "n_long_rows": d["n_long_rows"], "kernels": d["kernels"],
+                        "per_kernel_ms": A.apply_profiled(x, y)})
+            A.close()
+            print(json.dumps(rec), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -459,10 +517,13 @@ def main(argv=None):
     ap.add_argument("--workload", default="lap3d_128")
     ap.add_argument("--format", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -229,20 +229,15 @@ int build_row_chunks(BuildCtx &c, Segmented &sg) {
     SPMV_TRY(dev_alloc_n(h, &sg.partial, total));
     SPMV_TRY_CUDA(launch_chunk_fill(m, sg.ptr, cptr, sg.row_chunk_ptr, sg.chunk_begin, sg.chunk_end, sg.chunk_row,
                                     c.s));
-    // rows cut into several chunks need the second (summing) launch
-    int64_t *flag = nullptr, *pos = nullptr;
-    SPMV_TRY(c.temp.get(&flag, m));
-    SPMV_TRY(c.temp.get(&pos, m + 1));
-    SPMV_TRY_CUDA(launch_multi_flags(m, count, flag, c.s));
-    SPMV_TRY_CUDA(launch_exclusive_scan(flag, m, pos, scan_tmp, c.s));
-    int64_t n_multi = 0;
-    SPMV_TRY_CUDA(cudaMemcpyAsync(&n_multi, pos + m, sizeof(int64_t), cudaMemcpyDeviceToHost, c.s));
+    // completion counters of the rows cut into several chunks (start at zero; the
+    // warp that finishes a row resets its counter)
+    SPMV_TRY(dev_alloc_n(h, &sg.done, m));
+    SPMV_TRY_CUDA(cudaMemsetAsync(sg.done, 0, sizeof(int32_t) * m, c.s));
+    std::vector<int64_t> counts_host(static_cast<size_t>(m));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(counts_host.data(), count, sizeof(int64_t) * m, cudaMemcpyDeviceToHost, c.s));
     SPMV_TRY(sync(c.s));
-    sg.n_multi = n_multi;
-    if (n_multi > 0) {
-        SPMV_TRY(dev_alloc_n(h, &sg.multi_rows, n_multi));
-        SPMV_TRY_CUDA(launch_multi_scatter(m, flag, pos, sg.multi_rows, c.s));
-    }
+    sg.n_multi = 0;
+    for (int64_t v : counts_host) sg.n_multi += v > 1;
     return SPMV_OK;
 }
 
@@ -688,10 +683,7 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     if (h->seg.kind == 1) h->kernels.push_back("merge_path");
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
     if ((h->seg.kind == 1 || h->seg.kind == 2) && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
-    if (h->seg.kind == 3) {
-        if (!h->sliced.present) h->kernels.push_back("rowsplit_chunks");
-        if (h->seg.n_multi > 0) h->kernels.push_back("rowsplit_reduce");
-    }
+    if (h->seg.kind == 3 && !h->sliced.present) h->kernels.push_back("rowsplit_chunks");
     return sync(c.s);
 }
 
@@ -728,7 +720,7 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
             if (rec) SPMV_TRY(rec->mark(s));
         }
         if (split) {
-            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s, 1));
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
     } else if (h->sliced.present) {
@@ -736,12 +728,7 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
         SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &h->seg : nullptr, x, y, s));
         if (rec) SPMV_TRY(rec->mark(s));
     }
-    if (split) {
-        if (h->seg.n_multi > 0) {
-            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s, 2));
-            if (rec) SPMV_TRY(rec->mark(s));
-        }
-    } else if (h->seg.kind != 0) {
+    if (!split && h->seg.kind != 0) {
         SPMV_TRY_CUDA(launch_segmented(h->dtype, h->seg, x, y, s));
         if (rec) SPMV_TRY(rec->mark(s));
         if (h->seg.n_cta > 1) {

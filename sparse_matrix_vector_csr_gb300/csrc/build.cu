@@ -507,16 +507,6 @@ __global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, const i
     }
 }
 
-__global__ void k_multi_flags(int64_t m, const int64_t *__restrict__ count, int64_t *__restrict__ flag) {
-    for (int64_t i = gtid(); i < m; i += gstride()) flag[i] = count[i] > 1 ? 1 : 0;
-}
-
-__global__ void k_multi_scatter(int64_t m, const int64_t *__restrict__ flag, const int64_t *__restrict__ pos,
-                                int32_t *__restrict__ multi) {
-    for (int64_t i = gtid(); i < m; i += gstride())
-        if (flag[i]) multi[pos[i]] = static_cast<int32_t>(i);
-}
-
 // ---------------------------------------------------------------------------
 // to_csr
 // ---------------------------------------------------------------------------
@@ -718,16 +708,6 @@ cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, const int64_t *cptr
     if (m > 0)
         k_chunk_fill<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, cptr, row_chunk_ptr, chunk_begin, chunk_end,
                                                                   chunk_row);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_multi_flags(int64_t m, const int64_t *count, int64_t *flag, cudaStream_t s) {
-    if (m > 0) k_multi_flags<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, count, flag);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_multi_scatter(int64_t m, const int64_t *flag, const int64_t *pos, int32_t *multi, cudaStream_t s) {
-    if (m > 0) k_multi_scatter<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, flag, pos, multi);
     return cudaGetLastError();
 }
 

@@ -8,10 +8,12 @@
 // scheme of the Trilinos issue on unpackAndCombine: over rows, then over blocks of
 // entries within a row, then over entries within a block): every long row is cut
 // into chunks of at most kSplitChunk entries and one warp reduces one chunk.  A row
-// with a single chunk is written at once; the partials of longer rows are summed in
-// double by one warp per row.  Work per warp is bounded whatever the row lengths;
-// no atomics; fixed summation order.  The sliced rows and the chunks write disjoint
-// rows of y, so both run in one launch.
+// with a single chunk is written at once; for longer rows the warp that completes
+// the last chunk sums the row's partials (in double, in chunk order) -- it learns it
+// is last from a per-row integer counter.  Work per warp is bounded whatever the
+// row lengths; values are never accumulated atomically, and the summation order is
+// fixed.  The sliced rows and the chunks write disjoint rows of y, so both run in
+// one launch.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -55,10 +57,12 @@ struct SplitArgs {
     int64_t n_chunks;
     const int32_t *chunk_begin;
     const int32_t *chunk_end;
-    const int32_t *chunk_row;  // compact row, or ~row when it is the row's only chunk
-    const int32_t *rows;       // compact row -> matrix row
+    const int32_t *chunk_row;      // compact row, or ~row when it is the row's only chunk
+    const int32_t *rows;           // compact row -> matrix row
+    const int32_t *row_chunk_ptr;  // chunks of compact row i: [row_chunk_ptr[i], row_chunk_ptr[i+1])
     const int32_t *col;
-    double *partial;
+    double *partial;               // one partial sum per chunk of a row with several chunks
+    int32_t *done;                 // per compact row: chunks finished in this apply (back to 0 after it)
     int accumulate;
 };
 
@@ -144,14 +148,35 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
     double s = static_cast<double>(acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) {
-        const int32_t cr = __ldg(a.chunk_row + c);
-        if (cr < 0) {
+    const int32_t cr = __ldg(a.chunk_row + c);
+    if (cr < 0) {  // the row's only chunk
+        if (lane == 0) {
             const int32_t r = __ldg(a.rows + ~cr);
             y[r] = a.accumulate ? static_cast<T>(static_cast<double>(y[r]) + s) : static_cast<T>(s);
-        } else {
-            a.partial[c] = s;
         }
+        return;
+    }
+    // A row with several chunks: publish this chunk's partial; the warp that finishes
+    // the row's last chunk adds all of them up in chunk order (same order every
+    // apply) and writes y, then clears the row's counter for the next apply.
+    const int32_t c0 = __ldg(a.row_chunk_ptr + cr), c1 = __ldg(a.row_chunk_ptr + cr + 1);
+    int last = 0;
+    if (lane == 0) {
+        a.partial[c] = s;
+        __threadfence();
+        last = atomicAdd(a.done + cr, 1) == (c1 - c0) - 1;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    double t = 0.0;
+    for (int32_t q = c0 + lane; q < c1; q += 32) t += __ldcg(a.partial + q);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) {
+        const int32_t r = __ldg(a.rows + cr);
+        y[r] = a.accumulate ? static_cast<T>(static_cast<double>(y[r]) + t) : static_cast<T>(t);
+        a.done[cr] = 0;
     }
 }
 
@@ -185,35 +210,13 @@ __global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__re
     if (c < b.n_chunks) split_chunk<T>(c, threadIdx.x & 31, b, val, x, y);
 }
 
-// One warp per long row cut into several chunks: sum its partials in double.
-template <typename T>
-__global__ void __launch_bounds__(256) k_split_reduce(int64_t n_multi, const int32_t *__restrict__ multi_rows,
-                                                     const int32_t *__restrict__ rows,
-                                                     const int32_t *__restrict__ row_chunk_ptr,
-                                                     const double *__restrict__ partial, T *__restrict__ y,
-                                                     int accumulate) {
-    const int64_t w = gtid() >> 5;
-    const int lane = threadIdx.x & 31;
-    if (w >= n_multi) return;
-    const int32_t i = __ldg(multi_rows + w);
-    const int32_t a = __ldg(row_chunk_ptr + i), b = __ldg(row_chunk_ptr + i + 1);
-    double s = 0.0;
-    for (int32_t c = a + lane; c < b; c += 32) s += partial[c];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) {
-        const int32_t r = __ldg(rows + i);
-        y[r] = accumulate ? static_cast<T>(static_cast<double>(y[r]) + s) : static_cast<T>(s);
-    }
-}
-
 SellArgs sell_args(const Sliced &sl, int64_t n) {
     return SellArgs{sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len, sl.perm, sl.col, n};
 }
 
 SplitArgs split_args(const Segmented &sg) {
-    return SplitArgs{sg.n_chunks, sg.chunk_begin, sg.chunk_end, sg.chunk_row, sg.rows, sg.col, sg.partial,
-                     sg.accumulate};
+    return SplitArgs{sg.n_chunks, sg.chunk_begin, sg.chunk_end, sg.chunk_row, sg.rows, sg.row_chunk_ptr,
+                     sg.col, sg.partial, sg.done, sg.accumulate};
 }
 
 template <typename T, int CS>
@@ -239,14 +242,10 @@ cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const Segmented *sg, cons
 }
 
 template <typename T>
-cudaError_t split_dispatch(const Segmented &sg, const T *x, T *y, cudaStream_t s, int which) {
+cudaError_t split_dispatch(const Segmented &sg, const T *x, T *y, cudaStream_t s) {
     if (sg.kind != 3 || sg.n_chunks <= 0) return cudaSuccess;
-    if (which & 1)
-        k_split_chunks<T><<<static_cast<unsigned>(ceil_div(sg.n_chunks * 32, 256)), 256, 0, s>>>(
-            split_args(sg), static_cast<const T *>(sg.val), x, y);
-    if ((which & 2) && sg.n_multi > 0)
-        k_split_reduce<T><<<static_cast<unsigned>(ceil_div(sg.n_multi * 32, 256)), 256, 0, s>>>(
-            sg.n_multi, sg.multi_rows, sg.rows, sg.row_chunk_ptr, sg.partial, y, sg.accumulate);
+    k_split_chunks<T><<<static_cast<unsigned>(ceil_div(sg.n_chunks * 32, 256)), 256, 0, s>>>(
+        split_args(sg), static_cast<const T *>(sg.val), x, y);
     return cudaGetLastError();
 }
 
@@ -260,10 +259,10 @@ cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segm
     return sell_dispatch<float>(sl, n, split, static_cast<const float *>(x), static_cast<float *>(y), s);
 }
 
-cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s, int which) {
+cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s) {
     if (dtype == SPMV_F64)
-        return split_dispatch<double>(sg, static_cast<const double *>(x), static_cast<double *>(y), s, which);
-    return split_dispatch<float>(sg, static_cast<const float *>(x), static_cast<float *>(y), s, which);
+        return split_dispatch<double>(sg, static_cast<const double *>(x), static_cast<double *>(y), s);
+    return split_dispatch<float>(sg, static_cast<const float *>(x), static_cast<float *>(y), s);
 }
 
 }  // namespace spmv

@@ -76,7 +76,7 @@ struct Segmented {
     int32_t *row_chunk_ptr = nullptr;  // [n_rows + 1] chunks of compact row i
     int32_t *chunk_row = nullptr;      // [n_chunks] compact row of the chunk; ~row if it is the row's only chunk
     int64_t n_multi = 0;               // compact rows cut into more than one chunk
-    int32_t *multi_rows = nullptr;     // [n_multi] those rows (compact indices)
+    int32_t *done = nullptr;           // [n_rows] chunks of the row finished in the running apply
     double *partial = nullptr;         // [n_chunks] partial sums (scratch of the pass)
     int accumulate = 1;            // 1: add into y (y written before), 0: write y
     int32_t dst_offset = 0;        // in-row position of the first held entry (K for the spill)
@@ -216,10 +216,7 @@ cudaError_t launch_compact_copy(int dtype, int64_t m, const int32_t *rows, const
 cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int64_t *count, cudaStream_t s);
 cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, const int64_t *cptr, int32_t *row_chunk_ptr,
                               int32_t *chunk_begin, int32_t *chunk_end, int32_t *chunk_row, cudaStream_t s);
-// flag[i] = 1 when compact row i has more than one chunk; after an exclusive scan
-// of the flags into pos, multi[pos[i]] = i for the flagged rows
-cudaError_t launch_multi_flags(int64_t m, const int64_t *count, int64_t *flag, cudaStream_t s);
-cudaError_t launch_multi_scatter(int64_t m, const int64_t *flag, const int64_t *pos, int32_t *multi, cudaStream_t s);
+
 
 // to_csr
 cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const int32_t *out_ptr,
@@ -238,8 +235,8 @@ cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *ro
                               const void *x, void *y, cudaStream_t s);
 cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
-// row-split pass (kind 3): which & 1 = chunks alone, which & 2 = sums of rows cut into several chunks
-cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s, int which);
+// row-split pass (kind 3) on its own (next to the CSR-vector bins)
+cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
 // merge-path over a whole CSR (row i of the path is matrix row i), writing y
 cudaError_t launch_merge_path_identity(int dtype, int64_t n_rows, int64_t nnz, const int32_t *ptr,
                                        const int32_t *col, const void *val, const void *x, void *y,
