@@ -1,0 +1,103 @@
+"""Parity at the full workload sizes, in the launch configuration the bench times (AUTO format).
+
+The oracle evaluates sampled rows one by one (random rows, both ends, every long row); the
+Laplacians are also checked on every row against their closed forms, and the 2D Laplacian
+bit-exactly on integer x.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import assert_parity, build, run
+from workloads import integer_x, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(csr, k=20000, seed=0, extra=()):
+    rng = np.random.default_rng(seed)
+    n = csr.n
+    rows = np.concatenate([np.arange(min(n, 1000)), np.arange(max(0, n - 1000), n),
+                           rng.integers(0, n, size=min(k, n)), np.asarray(extra, dtype=np.int64)])
+    return np.unique(rows)
+
+
+def stencil_expect(grid, f):
+    """y of the Dirichlet Laplacian applied to x = f(position): missing neighbours contribute f there."""
+    dims = len(grid)
+    idx = np.arange(int(np.prod(grid)), dtype=np.int64)
+    coords, rest = [], idx
+    for g in grid:
+        coords.append(rest % g)
+        rest = rest // g
+    y = np.zeros(idx.size)
+    for axis in range(dims):
+        for step in (-1, 1):
+            q = [c.copy() for c in coords]
+            q[axis] = q[axis] + step
+            missing = (q[axis] < 0) | (q[axis] >= grid[axis])
+            y[missing] += f(*q)[missing]
+    return y
+
+
+@pytest.mark.parametrize("name,dtype", [("lap3d_128", np.float64), ("lap3d_128", np.float32),
+                                        ("hmep_6p2m", np.float64), ("powerlaw_4m", np.float64),
+                                        ("uniform16_16m", np.float32), ("lap2d_256", np.float64)])
+def test_full_size_sampled_rows(name, dtype):
+    csr, x = make_workload(name, dtype=dtype)
+    extra = []
+    if name.startswith("powerlaw"):
+        lens = np.diff(csr.row_ptr.astype(np.int64))
+        extra = np.nonzero(lens > 128)[0][:2000]  # long rows: row-split chunks
+    rows = sample_rows(csr, extra=extra)
+    ref = oracle.spmv(csr, x, rows=rows)
+    with build(csr, "auto") as A:
+        y = run(A, x)
+        assert np.all(np.isfinite(y))
+        assert_parity(y[rows], ref, dtype, label=f"{name} {np.dtype(dtype).name} ({A.describe()['format']})")
+
+
+@pytest.mark.parametrize("fmt,params", [("csr_vector", {}), ("ell_r", {}), ("sell", {"C": 64, "sigma": 256}),
+                                        ("hyb", {}), ("hyb", {"spill_csr": 0}), ("merge", {})])
+def test_full_size_uniform_every_format(fmt, params):
+    """The random uniform workload is the one swept over every format."""
+    csr, x = make_workload("uniform16_16m")
+    rows = sample_rows(csr, k=5000, seed=1)
+    ref = oracle.spmv(csr, x, rows=rows)
+    with build(csr, fmt, **params) as A:
+        assert_parity(run(A, x)[rows], ref, np.float32, label=f"uniform16 {fmt} {params}")
+
+
+@pytest.mark.parametrize("fmt", ["merge", "hyb", "csr_vector"])
+def test_full_size_powerlaw_other_formats(fmt):
+    csr, x = make_workload("powerlaw_4m")
+    lens = np.diff(csr.row_ptr.astype(np.int64))
+    rows = sample_rows(csr, k=5000, seed=2, extra=np.argsort(-lens)[:64])
+    ref = oracle.spmv(csr, x, rows=rows)
+    with build(csr, fmt) as A:
+        assert_parity(run(A, x)[rows], ref, np.float64, label=f"powerlaw {fmt}")
+
+
+def test_full_size_laplacian_closed_forms():
+    """Every row of the full-size Laplacians against the closed form (exact integers)."""
+    for name, grid, (a, b, c, d) in [("lap3d_128", (128, 128, 128), (1, -2, 3, 5)),
+                                     ("lap2d_256", (256, 256), (3, -1, 0, 7))]:
+        csr, _ = make_workload(name)
+        coords, rest = [], np.arange(csr.n, dtype=np.int64)
+        for g in grid:
+            coords.append(rest % g)
+            rest = rest // g
+        coef = (a, b, c)[:len(grid)]
+        x = (sum(k * q for k, q in zip(coef, coords)) + d).astype(np.float64)
+        expect = stencil_expect(grid, lambda *q: sum(k * v for k, v in zip(coef, q)) + d)
+        with build(csr, "auto") as A:
+            y = run(A, x)
+        assert np.array_equal(y, expect), name
+
+
+def test_full_size_integer_x_bit_exact():
+    csr, _ = make_workload("lap2d_256")
+    x = integer_x(csr.n)
+    ref = oracle.spmv(csr, x)
+    with build(csr, "auto") as A:
+        assert_parity(run(A, x), ref, np.float64, exact=True, label="lap2d_256 integer x")
