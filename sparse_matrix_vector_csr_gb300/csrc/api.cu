@@ -680,6 +680,16 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
         default:
             return set_error(SPMV_ERR_INVALID_ARG, "unknown format");
     }
+    if (h->sliced.present) {
+        // Hint the x gathers to stay in L2 when x is small against it (float64 with
+        // x <= L2 / 4): the matrix stream then cannot evict x between applies.
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device) != cudaSuccess) {
+            (void)cudaGetLastError();
+            l2 = 0;
+        }
+        h->sliced.keep_x = h->dtype == SPMV_F64 && static_cast<double>(n) * 8.0 <= 0.25 * l2;
+    }
     if (h->seg.kind == 1) h->kernels.push_back("merge_path");
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
     if ((h->seg.kind == 1 || h->seg.kind == 2) && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
@@ -974,6 +984,7 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
               "\"ld\":%lld,\"max_width\":%d,\"permuted\":%s,",
            sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,
            (long long)sl.stored_entries, (long long)sl.ld, sl.max_width, sl.perm ? "true" : "false");
+    append(o, "\"x_evict_last\":%s,", sl.keep_x ? "true" : "false");
     append(o, "\"n_long_rows\":%lld,\"long_nnz\":%lld,", (long long)h->n_long_rows, (long long)h->long_nnz);
     append(o, "\"segment\":\"%s\",\"segment_rows\":%lld,\"segment_nnz\":%lld,\"segment_ctas\":%lld,",
            sg.kind == 0 ? "none" : sg.kind == 1 ? "csr_merge_path" : sg.kind == 2 ? "coo" : "row_split",

@@ -114,7 +114,7 @@ __device__ __forceinline__ void stage_products(const int32_t *__restrict__ col, 
 #pragma unroll
     for (int q = 0; q < kMergeIpt; ++q) {
         const int t = threadIdx.x + q * kMergeThreads;
-        if (t < nk) s_prod[skew<T>(t)] = a[q] * ld_x(x + c[q]);
+        if (t < nk) s_prod[skew<T>(t)] = a[q] * ld_x_keep(x + c[q]);
     }
 }
 

@@ -69,7 +69,7 @@ struct SplitArgs {
 // CS > 0: SELL with a compile-time slice height CS (stride = CS).
 // CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
 //          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
-template <typename T, int CS>
+template <typename T, int CS, bool K>
 __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
                                          const T *__restrict__ x, T *__restrict__ y) {
     constexpr int U = SellChunk<T, CS>::U;
@@ -92,7 +92,7 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
             }
             T xv[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
+            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
 #pragma unroll
             for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);  // inactive slots add +0 * +0
             cp += U * CS;
@@ -112,7 +112,7 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
             }
             T xv[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? ld_x(x + c[u]) : T(0);
+            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
 #pragma unroll
             for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);
             cp += static_cast<int64_t>(U) * ld;
@@ -124,7 +124,7 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
 }
 
 // One warp reduces chunk c of a long row.
-template <typename T>
+template <typename T, bool K>
 __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs &a, const T *__restrict__ val,
                                             const T *__restrict__ x, T *__restrict__ y) {
     constexpr int U = 4;
@@ -141,7 +141,7 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
         }
         T xv[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) xv[u] = (k + 32 * u < e) ? ld_x(x + cc[u]) : T(0);
+        for (int u = 0; u < U; ++u) xv[u] = (k + 32 * u < e) ? gather_x<K>(x + cc[u]) : T(0);
 #pragma unroll
         for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);
     }
@@ -180,26 +180,27 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
     }
 }
 
-template <typename T, int CS>
+// K: gather x with the L2 evict-last policy (chosen per handle at build time)
+template <typename T, int CS, bool K>
 __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
     k_sell(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y) {
     const int64_t p = gtid();
-    if (p < a.n_pos) sell_row<T, CS>(p, a, val, x, y);
+    if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y);
 }
 
 // Sliced rows and row-split chunks in one launch: the first split_ctas CTAs take
 // eight chunks each (one per warp), the rest take kSellBlock row positions each.
-template <typename T, int CS>
+template <typename T, int CS, bool K>
 __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
     k_sell_split(SellArgs a, const T *__restrict__ val, SplitArgs b, const T *__restrict__ split_val,
                  int64_t split_ctas, const T *__restrict__ x, T *__restrict__ y) {
     if (blockIdx.x < split_ctas) {
         const int64_t c = (static_cast<int64_t>(blockIdx.x) * kSellBlock + threadIdx.x) >> 5;
-        if (c < b.n_chunks) split_chunk<T>(c, threadIdx.x & 31, b, split_val, x, y);
+        if (c < b.n_chunks) split_chunk<T, K>(c, threadIdx.x & 31, b, split_val, x, y);
         return;
     }
     const int64_t p = (static_cast<int64_t>(blockIdx.x) - split_ctas) * kSellBlock + threadIdx.x;
-    if (p < a.n_pos) sell_row<T, CS>(p, a, val, x, y);
+    if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y);
 }
 
 // Row-split chunks alone (long rows next to the CSR-vector bins).
@@ -207,7 +208,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__restrict__ val, const T *__restrict__ x,
                                                      T *__restrict__ y) {
     const int64_t c = gtid() >> 5;
-    if (c < b.n_chunks) split_chunk<T>(c, threadIdx.x & 31, b, val, x, y);
+    if (c < b.n_chunks) split_chunk<T, true>(c, threadIdx.x & 31, b, val, x, y);
 }
 
 SellArgs sell_args(const Sliced &sl, int64_t n) {
@@ -219,26 +220,31 @@ SplitArgs split_args(const Segmented &sg) {
                      sg.col, sg.partial, sg.done, sg.accumulate};
 }
 
-template <typename T, int CS>
+template <typename T, int CS, bool K>
 cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
     const T *val = static_cast<const T *>(sl.val);
     const int64_t sell_ctas = ceil_div(sl.n_pos, kSellBlock);
     if (sg && sg->kind == 3 && sg->n_chunks > 0) {
         const int64_t split_ctas = ceil_div(sg->n_chunks * 32, kSellBlock);
-        k_sell_split<T, CS><<<static_cast<unsigned>(split_ctas + sell_ctas), kSellBlock, 0, s>>>(
+        k_sell_split<T, CS, K><<<static_cast<unsigned>(split_ctas + sell_ctas), kSellBlock, 0, s>>>(
             sell_args(sl, n), val, split_args(*sg), static_cast<const T *>(sg->val), split_ctas, x, y);
     } else {
-        k_sell<T, CS><<<static_cast<unsigned>(sell_ctas), kSellBlock, 0, s>>>(sell_args(sl, n), val, x, y);
+        k_sell<T, CS, K><<<static_cast<unsigned>(sell_ctas), kSellBlock, 0, s>>>(sell_args(sl, n), val, x, y);
     }
     return cudaGetLastError();
+}
+
+template <typename T, int CS>
+cudaError_t sell_launch_k(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
+    return sl.keep_x ? sell_launch<T, CS, true>(sl, n, sg, x, y, s) : sell_launch<T, CS, false>(sl, n, sg, x, y, s);
 }
 
 template <typename T>
 cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
     const bool sliced = sl.log2C < 31;
-    if (sliced && sl.C == 32) return sell_launch<T, 32>(sl, n, sg, x, y, s);
-    if (sliced && sl.C == 64) return sell_launch<T, 64>(sl, n, sg, x, y, s);
-    return sell_launch<T, 0>(sl, n, sg, x, y, s);
+    if (sliced && sl.C == 32) return sell_launch_k<T, 32>(sl, n, sg, x, y, s);
+    if (sliced && sl.C == 64) return sell_launch_k<T, 64>(sl, n, sg, x, y, s);
+    return sell_launch_k<T, 0>(sl, n, sg, x, y, s);
 }
 
 template <typename T>

@@ -46,6 +46,7 @@ struct Sliced {
     int64_t padded_entries = 0;  // sum over real rows of their slice width
     int64_t stored_entries = 0;  // entries actually held (sum of len)
     int32_t max_width = 0;
+    bool keep_x = false;           // gather x with an L2 evict-last policy
     int64_t *slice_ptr = nullptr;  // [n_slices + 1]
     int32_t *width = nullptr;      // [n_slices]
     int32_t *len = nullptr;        // [n_pos] entries stored at each position
