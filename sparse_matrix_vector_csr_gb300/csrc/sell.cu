@@ -69,6 +69,30 @@ struct SplitArgs {
 // CS > 0: SELL with a compile-time slice height CS (stride = CS).
 // CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
 //          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
+// Programmatic dependent launch: a sliced-apply kernel may start while the previous
+// kernel of the stream is still draining.  Everything read before grid_wait() is
+// the handle's own matrix data, immutable after the build; x (which the previous
+// kernel may produce) and y (which it may still read) are touched only after it.
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename T, int U, int CS>
+__device__ __forceinline__ void load_slots(const int32_t *__restrict__ cp, const T *__restrict__ vp, int64_t ld, int j,
+                                           int w, int32_t (&c)[U], T (&v)[U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const bool on = j + u < w;
+        const int64_t off = CS > 0 ? static_cast<int64_t>(u * CS) : u * ld;
+        c[u] = on ? ld_stream(cp + off) : 0;
+        v[u] = on ? ld_stream(vp + off) : T(0);
+    }
+}
+
+// CS > 0: SELL with a compile-time slice height CS (stride = CS).
+// CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
+//          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
+// Entries are processed U at a time: U column indices and values (predicated on the
+// row length, so padding is never touched), then the U gathers, then U FMAs.
 template <typename T, int CS, bool K>
 __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
                                          const T *__restrict__ x, T *__restrict__ y) {
@@ -77,49 +101,28 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
     const uint64_t up = static_cast<uint64_t>(p);
     const int64_t slot = CS > 0 ? __ldg(a.slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
                                 : __ldg(a.slice_ptr + (p >> a.log2C)) + static_cast<int64_t>(p & a.cmask);
+    // the ELL leading dimension is below 2^31
+    const int64_t ld = CS > 0 ? CS : static_cast<int64_t>(static_cast<int>(a.stride));
     const int32_t *__restrict__ cp = a.col + slot;
     const T *__restrict__ vp = val + slot;
-    T acc = T(0);
-    if constexpr (CS > 0) {
-        for (int j = 0; j < w; j += U) {
-            int32_t c[U];
-            T v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const bool on = j + u < w;
-                c[u] = on ? ld_stream(cp + u * CS) : 0;
-                v[u] = on ? ld_stream(vp + u * CS) : T(0);
-            }
-            T xv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
-#pragma unroll
-            for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);  // inactive slots add +0 * +0
-            cp += U * CS;
-            vp += U * CS;
-        }
-    } else {
-        // the leading dimension of an ELL part is below 2^31: 32-bit offsets inside a chunk
-        const int ld = static_cast<int>(a.stride);
-        for (int j = 0; j < w; j += U) {
-            int32_t c[U];
-            T v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const bool on = j + u < w;
-                c[u] = on ? ld_stream(cp + u * ld) : 0;
-                v[u] = on ? ld_stream(vp + u * ld) : T(0);
-            }
-            T xv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
-#pragma unroll
-            for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);
-            cp += static_cast<int64_t>(U) * ld;
-            vp += static_cast<int64_t>(U) * ld;
-        }
-    }
     const int64_t r = a.perm ? static_cast<int64_t>(__ldg(a.perm + p)) : p;
+    int32_t c[U];
+    T v[U];
+    load_slots<T, U, CS>(cp, vp, ld, 0, w, c, v);  // first entries before the dependency wait
+    grid_wait();
+    T acc = T(0);
+    for (int j = 0; j < w;) {
+        T xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);  // inactive slots add +0 * +0
+        j += U;
+        if (j >= w) break;
+        cp += U * ld;
+        vp += U * ld;
+        load_slots<T, U, CS>(cp, vp, ld, j, w, c, v);
+    }
     if (w >= 0 && r >= 0 && r < a.n) y[r] = acc;
 }
 
@@ -130,6 +133,7 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
     constexpr int U = 4;
     const int32_t b = __ldg(a.chunk_begin + c), e = __ldg(a.chunk_end + c);
     T acc = T(0);
+    bool first = true;
     for (int32_t k = b + lane; k < e; k += 32 * U) {
         int32_t cc[U];
         T v[U];
@@ -139,12 +143,17 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
             cc[u] = on ? ld_stream(a.col + k + 32 * u) : 0;
             v[u] = on ? ld_stream(val + k + 32 * u) : T(0);
         }
+        if (first) {
+            grid_wait();  // see sell_row
+            first = false;
+        }
         T xv[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) xv[u] = (k + 32 * u < e) ? gather_x<K>(x + cc[u]) : T(0);
 #pragma unroll
         for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);
     }
+    if (first) grid_wait();  // a lane with no entry of its own still writes after the wait
     double s = static_cast<double>(acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -184,6 +193,7 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
 template <typename T, int CS, bool K>
 __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
     k_sell(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y) {
+    allow_dependents();
     const int64_t p = gtid();
     if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y);
 }
@@ -194,6 +204,7 @@ template <typename T, int CS, bool K>
 __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
     k_sell_split(SellArgs a, const T *__restrict__ val, SplitArgs b, const T *__restrict__ split_val,
                  int64_t split_ctas, const T *__restrict__ x, T *__restrict__ y) {
+    allow_dependents();
     if (blockIdx.x < split_ctas) {
         const int64_t c = (static_cast<int64_t>(blockIdx.x) * kSellBlock + threadIdx.x) >> 5;
         if (c < b.n_chunks) split_chunk<T, K>(c, threadIdx.x & 31, b, split_val, x, y);
@@ -224,14 +235,23 @@ template <typename T, int CS, bool K>
 cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
     const T *val = static_cast<const T *>(sl.val);
     const int64_t sell_ctas = ceil_div(sl.n_pos, kSellBlock);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kSellBlock);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (sg && sg->kind == 3 && sg->n_chunks > 0) {
         const int64_t split_ctas = ceil_div(sg->n_chunks * 32, kSellBlock);
-        k_sell_split<T, CS, K><<<static_cast<unsigned>(split_ctas + sell_ctas), kSellBlock, 0, s>>>(
-            sell_args(sl, n), val, split_args(*sg), static_cast<const T *>(sg->val), split_ctas, x, y);
-    } else {
-        k_sell<T, CS, K><<<static_cast<unsigned>(sell_ctas), kSellBlock, 0, s>>>(sell_args(sl, n), val, x, y);
+        cfg.gridDim = dim3(static_cast<unsigned>(split_ctas + sell_ctas));
+        return cudaLaunchKernelEx(&cfg, k_sell_split<T, CS, K>, sell_args(sl, n), val, split_args(*sg),
+                                  static_cast<const T *>(sg->val), split_ctas, x, y);
     }
-    return cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
+    return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y);
 }
 
 template <typename T, int CS>

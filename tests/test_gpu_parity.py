@@ -313,3 +313,55 @@ def test_repeated_applies_are_deterministic():
         y1 = run(A, x)
         y2 = run(A, x)
         assert np.array_equal(y1.view(np.uint64), y2.view(np.uint64))
+
+
+@pytest.mark.parametrize("fmt,name", [("auto", "powerlaw_small"), ("auto", "lap3d_small"), ("merge", "powerlaw_small"),
+                                      ("hyb", "hmep_small"), ("csr_vector", "powerlaw_small")])
+def test_apply_inside_a_cuda_graph(fmt, name):
+    """Applies captured in a CUDA graph (back to back, as a solver loop would) replay correctly,
+    including with a new x copied into the captured buffer between replays."""
+    torch = torch_cuda()
+    csr, x0, ref0 = small(name)
+    x1 = uniform_x(csr.n, seed=55)
+    ref1 = oracle.spmv(csr, x1)
+    with build(csr, fmt) as A:
+        xd = torch.from_numpy(x0).cuda()
+        y = torch.empty_like(xd)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            A.apply(xd, y)  # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(3):
+                A.apply(xd, y)
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_parity(y.cpu().numpy(), ref0, np.float64, label=f"graph {fmt} {name} x0")
+        xd.copy_(torch.from_numpy(x1).cuda())
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_parity(y.cpu().numpy(), ref1, np.float64, label=f"graph {fmt} {name} x1")
+
+
+def test_apply_after_a_kernel_that_writes_x():
+    """The sliced kernel may start before the previous kernel of the stream ends; it must still
+    read the x that kernel wrote (and not overwrite y that kernel reads)."""
+    torch = torch_cuda()
+    csr, x0, _ = small("lap3d_small")
+    with build(csr, "auto") as A:
+        xd = torch.from_numpy(x0).cuda()
+        y = torch.empty_like(xd)
+        for k in range(5):
+            xd.mul_(-0.5).add_(1.0)          # a kernel producing x
+            A.apply(xd, y)                   # reads it
+            z = y * 2.0                      # a kernel reading y
+            A.apply(xd, y)                   # rewrites y with the same values
+            torch.cuda.synchronize()
+            ref = oracle.spmv(csr, xd.cpu().numpy())
+            assert_parity(y.cpu().numpy(), ref, np.float64, label=f"round {k}")
+            assert torch.equal(z, y * 2.0)
