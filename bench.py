@@ -356,7 +356,8 @@ def run_ours(args):
         dom = max(range(len(pk)), key=lambda i: pk[i]) if pk else 0
         if len(kernels) == 1:
             kernel_ms = r["region_ms"] / steps
-            note = "single-kernel plan: launch duration = timed region / steps"
+            note = ("single-kernel plan: launch duration = timed region / steps (consecutive launches overlap "
+                    "through programmatic dependent launch, so this is the launch-to-launch interval)")
         else:
             share = pk[dom] / sum(pk)
             kernel_ms = r["region_ms"] / steps * share
