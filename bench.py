@@ -459,6 +459,46 @@ SWEEP_FORMATS = [
 ]
 
 
+def run_multi(args):
+    """Multi-vector apply Y = A X with k = --nrhs right-hand sides (AUTO format): one JSON line per k."""
+    import numpy as np
+    import torch
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+    from workloads import make_workload
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = load_peaks()
+    dtypes = [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+    for dt in dtypes:
+        csr, x_np = make_workload(args.workload, dtype=dt)
+        sv = csr.vals.dtype.itemsize
+        dev = torch.device("cuda", 0)
+        rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
+        A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=args.format)
+        for k in sorted({1, args.nrhs}):
+            X = torch.rand((csr.n, k), dtype=vv.dtype, device=dev) * 2 - 1
+            Y = torch.empty_like(X)
+            f = spmv._abi.lib.spmv_apply_multi
+            call = (A._h, k, 1.0, X.data_ptr(), k, 0.0, Y.data_ptr(), k, None)
+            for _ in range(args.warmup):
+                f(*call)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            steps = max(args.steps // 100, 20)
+            e0.record()
+            for _ in range(steps):
+                f(*call)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            beff = csr.nnz * (sv + 4) + (csr.n + 1) * 4 + 2 * csr.n * sv * k
+            print(json.dumps({"workload": args.workload, "dtype": "f64" if sv == 8 else "f32", "nrhs": k,
+                              "format": A.describe()["format"], "us_per_apply": ms * 1e3,
+                              "gflops": 2.0 * csr.nnz * k / ms / 1e6, "effective_gbs": beff / ms / 1e6,
+                              "frac": beff / ms / 1e6 / peak, "peak": f"{peak} GB/s {peak_kind}"}), flush=True)
+        A.close()
+
+
 def run_sweep(args):
     """One JSON line per storage format on the chosen workload (format comparison)."""
     import numpy as np
@@ -519,10 +559,14 @@ def main(argv=None):
     ap.add_argument("--format", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
+    ap.add_argument("--nrhs", type=int, default=0,
+                    help="with --sweep: time the multi-vector apply with this many right-hand sides instead")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep and args.nrhs > 0:
+        run_multi(args)
     elif args.sweep:
         run_sweep(args)
     else:

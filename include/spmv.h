@@ -174,6 +174,30 @@ SPMV_API int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, 
 SPMV_API int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, float *kernel_ms,
                         int cap);
 
+/*
+ * y = alpha * A x + beta * y.  When beta == 0, y is not read (any content, NaN
+ * included, is overwritten); alpha = 1, beta = 0 is spmv_apply.  Solvers use this
+ * form for residuals r = b - A x (alpha = -1, beta = 1 with y holding b), as the
+ * Krylov iterations of the Krylov/AMG paper (BiCGSTAB algorithm) combine SpMV with
+ * vector updates.  SELL and ELLPACK-R handles fold alpha and beta into the kernel's
+ * single write of each row; the other formats compute A x into a scratch column of
+ * the handle first.  Asynchronous; same stream rules as spmv_apply.
+ */
+SPMV_API int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double beta, void *y, void *stream);
+
+/*
+ * Y = alpha * A X + beta * Y for k right-hand sides at once.  X and Y are row-major
+ * n x k blocks in device memory: element (row j, vector c) at X[j * ldx + c] and
+ * Y[j * ldy + c], with ldx >= k and ldy >= k.  The matrix is streamed once per group
+ * of up to 8 vectors and each gather of a row of X fetches that row's values with
+ * one or two wide loads (SELL handles, slice height 32 or 64; X aligned to
+ * min(16, 8 * value size) bytes with ldx a multiple of that); other formats and
+ * left-over columns go one column at a time through scratch columns of the handle.
+ * beta == 0: Y is not read.  k = 0 is a no-op.  Asynchronous.
+ */
+SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, int64_t ldx, double beta,
+                              void *Y, int64_t ldy, void *stream);
+
 /* Release every device buffer of the handle.  NULL is accepted and ignored. */
 SPMV_API void spmv_destroy(spmv_handle_t h);
 

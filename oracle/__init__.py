@@ -11,6 +11,8 @@ Contents
   (``spmv_oracle.c``), with the per-row tolerance scale sum |a_ij x_j|.
 * :mod:`oracle.layout` -- the storage-layout definitions the formats follow
   (sorted/padded row blocks of ELLPACK-R / pJDS / SELL-C-sigma, the HYB split).
+* :func:`spmv_scaled`, :func:`spmm` -- y = alpha A x + beta y and its multi-vector
+  form Y = alpha A X + beta Y, from the long double product above.
 * :func:`check_rows` -- the acceptance rule for a computed y.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
@@ -115,6 +117,43 @@ def spmv(csr, x, rows=None, lib=None) -> dict:
     if rc != 0:
         raise ValueError("oracle rejected the CSR input (index out of range or non-monotone row_ptr)")
     return {"y_hi": y_hi, "y_lo": y_lo, "y": y, "scale": scale}
+
+
+def spmv_scaled(csr, x, alpha, beta, y_old, rows=None, lib=None) -> dict:
+    """y = alpha * A x + beta * y_old, combined in long double from the CSR result.
+
+    beta == 0 does not read y_old (its content, NaN included, does not matter).  The
+    tolerance scale becomes |alpha| * sum |a_ij x_j| + |beta * y_old_i|.
+    """
+    r = spmv(csr, x, rows=rows, lib=lib)
+    dt = np.dtype(csr.vals.dtype)
+    ax = r["y_hi"].astype(np.longdouble) + r["y_lo"].astype(np.longdouble)
+    a = np.longdouble(alpha)
+    if beta == 0:
+        val = a * ax
+        extra = np.zeros(ax.shape)
+    else:
+        yo = np.asarray(y_old, dtype=dt)
+        if rows is not None:
+            yo = yo[np.asarray(rows, dtype=np.int64)]
+        val = a * ax + np.longdouble(beta) * yo.astype(np.longdouble)
+        extra = np.abs(float(beta) * yo.astype(np.float64))
+    hi = val.astype(np.float64)
+    return {"y_hi": hi, "y_lo": (val - hi.astype(np.longdouble)).astype(np.float64), "y": val.astype(dt),
+            "scale": abs(float(alpha)) * r["scale"] + extra}
+
+
+def spmm(csr, X, alpha=1.0, beta=0.0, Y_old=None, rows=None, lib=None) -> dict:
+    """Y = alpha * A X + beta * Y_old for the k columns of X (n x k), column by column.
+
+    Returns the same keys as :func:`spmv_scaled`, each an array of shape (rows, k).
+    """
+    X = np.asarray(X)
+    k = X.shape[1]
+    cols = [spmv_scaled(csr, np.ascontiguousarray(X[:, c]), alpha, beta,
+                        None if Y_old is None else np.ascontiguousarray(np.asarray(Y_old)[:, c]), rows=rows, lib=lib)
+            for c in range(k)]
+    return {key: np.stack([cc[key] for cc in cols], axis=1) for key in ("y_hi", "y_lo", "y", "scale")}
 
 
 #: per-row tolerance factors: |y - y_ref| <= tau * sum_j |a_ij x_j|

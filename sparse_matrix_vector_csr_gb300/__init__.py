@@ -15,7 +15,9 @@ from ._abi import (  # noqa: F401
     FORMATS,
     SpmvError,
     spmv_apply,
+    spmv_apply_ex,
     spmv_apply_host,
+    spmv_apply_multi,
     spmv_apply_profiled,
     spmv_build_from_csr,
     spmv_build_from_csr_ex,
@@ -71,16 +73,38 @@ class SpmvMatrix:
         if v.dtype != self.dtype or v.numel() != self.n:
             raise ValueError(f"{name} must hold {self.n} values of {self.dtype}")
 
-    def apply(self, x, y=None, stream=None):
-        """y = A x on the current (or given) stream; allocates y when not given."""
+    def apply(self, x, y=None, stream=None, alpha=1.0, beta=0.0):
+        """y = alpha * A x + beta * y (default y = A x) on the current (or given) stream;
+        allocates y when not given (then beta must be 0)."""
         import torch
 
         self._check_vec(x, "x")
         if y is None:
+            if beta != 0.0:
+                raise ValueError("beta != 0 needs an input y")
             y = torch.empty_like(x)
         self._check_vec(y, "y")
-        spmv_apply(self._h, x, y, stream)
+        if alpha == 1.0 and beta == 0.0:
+            spmv_apply(self._h, x, y, stream)
+        else:
+            spmv_apply_ex(self._h, alpha, x, beta, y, stream)
         return y
+
+    def apply_multi(self, X, Y=None, alpha=1.0, beta=0.0, stream=None):
+        """Y = alpha * A X + beta * Y for the k columns of a row-major n x k CUDA tensor X."""
+        import torch
+
+        if not (isinstance(X, torch.Tensor) and X.is_cuda and X.dim() == 2 and X.shape[0] == self.n
+                and X.stride(1) == 1 and X.dtype == self.dtype):
+            raise TypeError(f"X must be an n x k CUDA tensor of {self.dtype} with unit column stride")
+        if Y is None:
+            if beta != 0.0:
+                raise ValueError("beta != 0 needs an input Y")
+            Y = torch.empty_like(X, memory_format=torch.contiguous_format)
+        if not (Y.shape == X.shape and Y.stride(1) == 1 and Y.dtype == self.dtype and Y.is_cuda):
+            raise TypeError("Y must match X in shape and type, with unit column stride")
+        spmv_apply_multi(self._h, X.shape[1], alpha, X, X.stride(0), beta, Y, Y.stride(0), stream)
+        return Y
 
     __matmul__ = apply
 

@@ -26,7 +26,7 @@ EXPORTS = (
     "spmv_default_params", "spmv_build_from_csr", "spmv_build_from_csr_ex", "spmv_apply",
     "spmv_apply_host", "spmv_apply_profiled", "spmv_destroy", "spmv_last_error",
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
-    "spmv_csr_apply_noalloc",
+    "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi",
 )
 
 
@@ -82,6 +82,11 @@ def _load():
     lib.spmv_get_layout.restype = c_int
     lib.spmv_csr_apply_noalloc.argtypes = [i64, i64, vp, vp, vp, c_int, vp, vp, vp]
     lib.spmv_csr_apply_noalloc.restype = c_int
+    f64 = ctypes.c_double
+    lib.spmv_apply_ex.argtypes = [vp, f64, vp, f64, vp, vp]
+    lib.spmv_apply_ex.restype = c_int
+    lib.spmv_apply_multi.argtypes = [vp, i64, f64, vp, i64, f64, vp, i64, vp]
+    lib.spmv_apply_multi.restype = c_int
     del i32
     return lib
 
@@ -221,3 +226,14 @@ def spmv_csr_apply_noalloc(n, nnz, row_ptr, col_idx, vals, dtype, x, y, stream=N
     """y = A x from a device CSR without any device allocation (see spmv.h)."""
     _check(lib.spmv_csr_apply_noalloc(int(n), int(nnz), _ptr(row_ptr), _ptr(col_idx), _ptr(vals), int(dtype),
                                       _ptr(x), _ptr(y), _stream(stream)))
+
+
+def spmv_apply_ex(h, alpha, x, beta, y, stream=None) -> None:
+    """y = alpha * A x + beta * y (y not read when beta == 0)."""
+    _check(lib.spmv_apply_ex(h, float(alpha), _ptr(x), float(beta), _ptr(y), _stream(stream)))
+
+
+def spmv_apply_multi(h, k, alpha, X, ldx, beta, Y, ldy, stream=None) -> None:
+    """Y = alpha * A X + beta * Y for k row-major right-hand sides."""
+    _check(lib.spmv_apply_multi(h, int(k), float(alpha), _ptr(X), int(ldx), float(beta), _ptr(Y), int(ldy),
+                                _stream(stream)))

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspmv_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["api.cu", "build.cu", "sell.cu", "vector.cu", "merge.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "build.cu", "sell.cu", "sellmm.cu", "vector.cu", "merge.cu", "vecops.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -48,7 +48,7 @@ def _newer(target: str, deps: list[str]) -> bool:
 def _compile(src: str, extra: list[str]) -> str:
     obj = os.path.join(OBJ_DIR, os.path.splitext(src)[0] + ".o")
     deps = [os.path.join(CSRC, src), os.path.join(CSRC, "spmv_internal.cuh"), os.path.join(CSRC, "device_util.cuh"),
-            os.path.join(INCLUDE, "spmv.h")]
+            os.path.join(CSRC, "sell_common.cuh"), os.path.join(INCLUDE, "spmv.h")]
     if _newer(obj, deps):
         return obj
     cmd = [nvcc_path()] + common_flags() + extra + ["-c", os.path.join(CSRC, src), "-o", obj]

@@ -226,7 +226,7 @@ int build_row_chunks(BuildCtx &c, Segmented &sg) {
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_begin, total));
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_end, total));
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_row, total));
-    SPMV_TRY(dev_alloc_n(h, &sg.partial, total));
+    SPMV_TRY(dev_alloc_n(h, &sg.partial, total * 8));  // up to 8 right-hand sides per pass
     SPMV_TRY_CUDA(launch_chunk_fill(m, sg.ptr, cptr, sg.row_chunk_ptr, sg.chunk_begin, sg.chunk_end, sg.chunk_row,
                                     c.s));
     // completion counters of the rows cut into several chunks (start at zero; the
@@ -694,6 +694,10 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
     if ((h->seg.kind == 1 || h->seg.kind == 2) && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
     if (h->seg.kind == 3 && !h->sliced.present) h->kernels.push_back("rowsplit_chunks");
+    // one column of x and of y for the scaled and multi-vector applies of formats
+    // without a fused epilogue
+    SPMV_TRY(dev_alloc(h, &h->tmp_x, static_cast<size_t>(n) * value_bytes(h->dtype)));
+    SPMV_TRY(dev_alloc(h, &h->tmp_y, static_cast<size_t>(n) * value_bytes(h->dtype)));
     return sync(c.s);
 }
 
@@ -720,7 +724,19 @@ struct Recorder {
     }
 };
 
-int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *rec) {
+// Formats whose kernels write y exactly once per row (so alpha/beta fold into that write).
+bool fused_epilogue(spmv_handle_t h) {
+    return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && (h->seg.kind == 0 || h->seg.kind == 3);
+}
+
+int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *rec, const Scale *scale = nullptr) {
+    if (scale && !fused_epilogue(h)) {
+        // y = alpha * t + beta * y with t = A x computed into the handle's scratch column
+        SPMV_TRY(enqueue(h, x, h->tmp_y, s, rec, nullptr));
+        SPMV_TRY_CUDA(launch_axpby_col(h->dtype, h->n, scale->alpha, h->tmp_y, scale->beta, y, 1, s));
+        if (rec) SPMV_TRY(rec->mark(s));
+        return SPMV_OK;
+    }
     if (rec) SPMV_TRY(rec->mark(s));
     const bool split = h->seg.kind == 3;
     if (h->format == SPMV_FMT_CSR_VECTOR) {
@@ -735,7 +751,7 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
         }
     } else if (h->sliced.present) {
         // sliced rows (and, in the same launch, the chunks of the long rows)
-        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &h->seg : nullptr, x, y, s));
+        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &h->seg : nullptr, x, y, s, scale));
         if (rec) SPMV_TRY(rec->mark(s));
     }
     if (!split && h->seg.kind != 0) {
@@ -896,6 +912,58 @@ int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, f
         if (kernel_ms) kernel_ms[i] = ms;
     }
     return k;
+}
+
+int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double beta, void *y, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (h->n == 0) return SPMV_OK;
+    if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    SPMV_TRY(check_current_device(h));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (alpha == 1.0 && beta == 0.0) return enqueue(h, x, y, s, nullptr);
+    const Scale scale{alpha, beta};
+    return enqueue(h, x, y, s, nullptr, &scale);
+}
+
+int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, int64_t ldx, double beta, void *Y,
+                     int64_t ldy, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (k < 0 || ldx < k || ldy < k) return set_error(SPMV_ERR_INVALID_ARG, "need 0 <= k <= ldx and k <= ldy");
+    if (h->n == 0 || k == 0) return SPMV_OK;
+    if (!X || !Y) return set_error(SPMV_ERR_INVALID_ARG, "NULL X or Y");
+    SPMV_TRY(check_current_device(h));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (k == 1 && ldx == 1 && ldy == 1) return spmv_apply_ex(h, alpha, X, beta, Y, stream);  // contiguous vectors
+    const size_t vb = value_bytes(h->dtype);
+    const Scale scale{alpha, beta};
+    const bool fused = fused_epilogue(h) && sell_multi_supported(h->sliced);
+    const Segmented *split = h->seg.kind == 3 ? &h->seg : nullptr;
+    int64_t c = 0;
+    while (c < k) {
+        const char *xc = static_cast<const char *>(X) + c * vb;
+        char *yc = static_cast<char *>(Y) + c * vb;
+        int nv = 0;
+        if (fused) {
+            for (int cand : {8, 4, 2}) {
+                const size_t align = std::min<size_t>(16, cand * vb);
+                if (k - c >= cand && reinterpret_cast<uintptr_t>(xc) % align == 0 && (ldx * vb) % align == 0) {
+                    nv = cand;
+                    break;
+                }
+            }
+        }
+        if (nv) {
+            SPMV_TRY_CUDA(launch_sell_multi(h->dtype, nv, h->sliced, h->n, split, xc, ldx, yc, ldy, s, scale));
+            c += nv;
+        } else {
+            // one column through the single-vector path
+            SPMV_TRY_CUDA(launch_gather_col(h->dtype, h->n, xc, ldx, h->tmp_x, s));
+            SPMV_TRY(enqueue(h, h->tmp_x, h->tmp_y, s, nullptr));
+            SPMV_TRY_CUDA(launch_axpby_col(h->dtype, h->n, alpha, h->tmp_y, beta, yc, ldy, s));
+            c += 1;
+        }
+    }
+    return SPMV_OK;
 }
 
 void spmv_destroy(spmv_handle_t h) { free_handle(h); }

@@ -19,12 +19,14 @@
 #include <cstdint>
 
 #include "device_util.cuh"
+#include "sell_common.cuh"
 #include "spmv_internal.cuh"
 
 namespace spmv {
 namespace {
 
 using namespace dev;
+using namespace sellk;
 
 // ---------------------------------------------------------------------------
 // sliced layout
@@ -40,41 +42,6 @@ struct SellChunk {
     // runtime-stride addressing needs a 64-bit address per load: keep 4 in flight
     static constexpr int U = (sizeof(T) == 8 || CS == 0) ? 4 : 8;
 };
-
-struct SellArgs {
-    int64_t n_pos;
-    int log2C;
-    uint32_t cmask;
-    int64_t stride;
-    const int64_t *slice_ptr;
-    const int32_t *len;   // -1 marks a long row (handled by the row-split pass)
-    const int32_t *perm;  // nullptr = natural order
-    const int32_t *col;
-    int64_t n;
-};
-
-struct SplitArgs {
-    int64_t n_chunks;
-    const int32_t *chunk_begin;
-    const int32_t *chunk_end;
-    const int32_t *chunk_row;      // compact row, or ~row when it is the row's only chunk
-    const int32_t *rows;           // compact row -> matrix row
-    const int32_t *row_chunk_ptr;  // chunks of compact row i: [row_chunk_ptr[i], row_chunk_ptr[i+1])
-    const int32_t *col;
-    double *partial;               // one partial sum per chunk of a row with several chunks
-    int32_t *done;                 // per compact row: chunks finished in this apply (back to 0 after it)
-    int accumulate;
-};
-
-// CS > 0: SELL with a compile-time slice height CS (stride = CS).
-// CS == 0: runtime addressing (slice p >> log2C, row p & cmask, stride `stride`),
-//          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
-// Programmatic dependent launch: a sliced-apply kernel may start while the previous
-// kernel of the stream is still draining.  Everything read before grid_wait() is
-// the handle's own matrix data, immutable after the build; x (which the previous
-// kernel may produce) and y (which it may still read) are touched only after it.
-__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename T, int U, int CS>
 __device__ __forceinline__ void load_slots(const int32_t *__restrict__ cp, const T *__restrict__ vp, int64_t ld, int j,
@@ -95,7 +62,7 @@ __device__ __forceinline__ void load_slots(const int32_t *__restrict__ cp, const
 // row length, so padding is never touched), then the U gathers, then U FMAs.
 template <typename T, int CS, bool K>
 __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
-                                         const T *__restrict__ x, T *__restrict__ y) {
+                                         const T *__restrict__ x, T *__restrict__ y, const Epi &ep) {
     constexpr int U = SellChunk<T, CS>::U;
     const int w = __ldg(a.len + p);
     const uint64_t up = static_cast<uint64_t>(p);
@@ -123,13 +90,13 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
         vp += U * ld;
         load_slots<T, U, CS>(cp, vp, ld, j, w, c, v);
     }
-    if (w >= 0 && r >= 0 && r < a.n) y[r] = acc;
+    if (w >= 0 && r >= 0 && r < a.n) store_y(y, r, acc, ep);
 }
 
 // One warp reduces chunk c of a long row.
 template <typename T, bool K>
 __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs &a, const T *__restrict__ val,
-                                            const T *__restrict__ x, T *__restrict__ y) {
+                                            const T *__restrict__ x, T *__restrict__ y, const Epi &ep) {
     constexpr int U = 4;
     const int32_t b = __ldg(a.chunk_begin + c), e = __ldg(a.chunk_end + c);
     T acc = T(0);
@@ -161,7 +128,10 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
     if (cr < 0) {  // the row's only chunk
         if (lane == 0) {
             const int32_t r = __ldg(a.rows + ~cr);
-            y[r] = a.accumulate ? static_cast<T>(static_cast<double>(y[r]) + s) : static_cast<T>(s);
+            if (a.accumulate)
+                y[r] = static_cast<T>(static_cast<double>(y[r]) + s);
+            else
+                store_y(y, r, static_cast<T>(s), ep);
         }
         return;
     }
@@ -184,7 +154,10 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
     if (lane == 0) {
         const int32_t r = __ldg(a.rows + cr);
-        y[r] = a.accumulate ? static_cast<T>(static_cast<double>(y[r]) + t) : static_cast<T>(t);
+        if (a.accumulate)
+            y[r] = static_cast<T>(static_cast<double>(y[r]) + t);
+        else
+            store_y(y, r, static_cast<T>(t), ep);
         a.done[cr] = 0;
     }
 }
@@ -192,10 +165,10 @@ __device__ __forceinline__ void split_chunk(int64_t c, int lane, const SplitArgs
 // K: gather x with the L2 evict-last policy (chosen per handle at build time)
 template <typename T, int CS, bool K>
 __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
-    k_sell(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y) {
+    k_sell(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     allow_dependents();
     const int64_t p = gtid();
-    if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y);
+    if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y, ep);
 }
 
 // Sliced rows and row-split chunks in one launch: the first split_ctas CTAs take
@@ -203,15 +176,15 @@ __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
 template <typename T, int CS, bool K>
 __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
     k_sell_split(SellArgs a, const T *__restrict__ val, SplitArgs b, const T *__restrict__ split_val,
-                 int64_t split_ctas, const T *__restrict__ x, T *__restrict__ y) {
+                 int64_t split_ctas, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     allow_dependents();
     if (blockIdx.x < split_ctas) {
         const int64_t c = (static_cast<int64_t>(blockIdx.x) * kSellBlock + threadIdx.x) >> 5;
-        if (c < b.n_chunks) split_chunk<T, K>(c, threadIdx.x & 31, b, split_val, x, y);
+        if (c < b.n_chunks) split_chunk<T, K>(c, threadIdx.x & 31, b, split_val, x, y, ep);
         return;
     }
     const int64_t p = (static_cast<int64_t>(blockIdx.x) - split_ctas) * kSellBlock + threadIdx.x;
-    if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y);
+    if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y, ep);
 }
 
 // Row-split chunks alone (long rows next to the CSR-vector bins).
@@ -219,20 +192,12 @@ template <typename T>
 __global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__restrict__ val, const T *__restrict__ x,
                                                      T *__restrict__ y) {
     const int64_t c = gtid() >> 5;
-    if (c < b.n_chunks) split_chunk<T, true>(c, threadIdx.x & 31, b, val, x, y);
-}
-
-SellArgs sell_args(const Sliced &sl, int64_t n) {
-    return SellArgs{sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len, sl.perm, sl.col, n};
-}
-
-SplitArgs split_args(const Segmented &sg) {
-    return SplitArgs{sg.n_chunks, sg.chunk_begin, sg.chunk_end, sg.chunk_row, sg.rows, sg.row_chunk_ptr,
-                     sg.col, sg.partial, sg.done, sg.accumulate};
+    if (c < b.n_chunks) split_chunk<T, true>(c, threadIdx.x & 31, b, val, x, y, Epi{1.0, 0.0, 0});
 }
 
 template <typename T, int CS, bool K>
-cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
+cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s,
+                        const Epi &ep) {
     const T *val = static_cast<const T *>(sl.val);
     const int64_t sell_ctas = ceil_div(sl.n_pos, kSellBlock);
     cudaLaunchAttribute attr[1];
@@ -248,23 +213,26 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
         const int64_t split_ctas = ceil_div(sg->n_chunks * 32, kSellBlock);
         cfg.gridDim = dim3(static_cast<unsigned>(split_ctas + sell_ctas));
         return cudaLaunchKernelEx(&cfg, k_sell_split<T, CS, K>, sell_args(sl, n), val, split_args(*sg),
-                                  static_cast<const T *>(sg->val), split_ctas, x, y);
+                                  static_cast<const T *>(sg->val), split_ctas, x, y, ep);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
-    return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y);
+    return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y, ep);
 }
 
 template <typename T, int CS>
-cudaError_t sell_launch_k(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
-    return sl.keep_x ? sell_launch<T, CS, true>(sl, n, sg, x, y, s) : sell_launch<T, CS, false>(sl, n, sg, x, y, s);
+cudaError_t sell_launch_k(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s,
+                          const Epi &ep) {
+    return sl.keep_x ? sell_launch<T, CS, true>(sl, n, sg, x, y, s, ep)
+                     : sell_launch<T, CS, false>(sl, n, sg, x, y, s, ep);
 }
 
 template <typename T>
-cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s) {
+cudaError_t sell_dispatch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s,
+                          const Epi &ep) {
     const bool sliced = sl.log2C < 31;
-    if (sliced && sl.C == 32) return sell_launch_k<T, 32>(sl, n, sg, x, y, s);
-    if (sliced && sl.C == 64) return sell_launch_k<T, 64>(sl, n, sg, x, y, s);
-    return sell_launch_k<T, 0>(sl, n, sg, x, y, s);
+    if (sliced && sl.C == 32) return sell_launch_k<T, 32>(sl, n, sg, x, y, s, ep);
+    if (sliced && sl.C == 64) return sell_launch_k<T, 64>(sl, n, sg, x, y, s, ep);
+    return sell_launch_k<T, 0>(sl, n, sg, x, y, s, ep);
 }
 
 template <typename T>
@@ -278,11 +246,12 @@ cudaError_t split_dispatch(const Segmented &sg, const T *x, T *y, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segmented *split, const void *x, void *y,
-                              cudaStream_t s) {
+                              cudaStream_t s, const Scale *scale) {
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
+    const Epi ep = scale ? Epi{scale->alpha, scale->beta, 1} : Epi{1.0, 0.0, 0};
     if (dtype == SPMV_F64)
-        return sell_dispatch<double>(sl, n, split, static_cast<const double *>(x), static_cast<double *>(y), s);
-    return sell_dispatch<float>(sl, n, split, static_cast<const float *>(x), static_cast<float *>(y), s);
+        return sell_dispatch<double>(sl, n, split, static_cast<const double *>(x), static_cast<double *>(y), s, ep);
+    return sell_dispatch<float>(sl, n, split, static_cast<const float *>(x), static_cast<float *>(y), s, ep);
 }
 
 cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s) {

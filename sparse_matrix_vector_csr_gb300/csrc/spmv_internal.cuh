@@ -121,6 +121,9 @@ struct spmv_handle_s {
     // spmv_apply_host staging
     void *x_stage = nullptr;
     void *y_stage = nullptr;
+    // one column of x and of y, for scaled / multi-vector applies without a fused path
+    void *tmp_x = nullptr;
+    void *tmp_y = nullptr;
 
     std::vector<std::string> kernels;  // launch sequence of one apply
     std::vector<void *> allocations;
@@ -228,14 +231,28 @@ cudaError_t launch_segment_to_csr(int dtype, const Segmented &sg, const int32_t 
 // ----------------------------------------------------------------------------
 // apply launchers -- sell.cu, vector.cu, merge.cu
 // ----------------------------------------------------------------------------
-// split: the row-split pass of the long rows (kind 3) to run in the same launch, or nullptr
+// y = alpha * (A x) + beta * y instead of y = A x (y not read when beta == 0)
+struct Scale {
+    double alpha;
+    double beta;
+};
+// split: the row-split pass of the long rows (kind 3) to run in the same launch, or nullptr;
+// scale: nullptr for y = A x
 cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segmented *split, const void *x, void *y,
-                              cudaStream_t s);
+                              cudaStream_t s, const Scale *scale = nullptr);
 cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *rows,
                               const int32_t *row_ptr, const int32_t *col, const void *val,
                               const void *x, void *y, cudaStream_t s);
 cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
+// multi-vector apply on the sliced layout (NV = 2, 4, 8 right-hand sides, row-major X/Y) -- sellmm.cu
+bool sell_multi_supported(const Sliced &sl);
+cudaError_t launch_sell_multi(int dtype, int nv, const Sliced &sl, int64_t n, const Segmented *split, const void *X,
+                              int64_t ldx, void *Y, int64_t ldy, cudaStream_t s, const Scale &scale);
+// vecops.cu: out[i] = X[i * ldx]; Y[i * ldy] = alpha * t[i] + beta * Y[i * ldy] (Y unread when beta == 0)
+cudaError_t launch_gather_col(int dtype, int64_t n, const void *X, int64_t ldx, void *out, cudaStream_t s);
+cudaError_t launch_axpby_col(int dtype, int64_t n, double alpha, const void *t, double beta, void *Y, int64_t ldy,
+                             cudaStream_t s);
 // row-split pass (kind 3) on its own (next to the CSR-vector bins)
 cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s);
 // merge-path over a whole CSR (row i of the path is matrix row i), writing y

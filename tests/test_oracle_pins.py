@@ -240,3 +240,42 @@ def test_pins_catch_planted_mistakes(mutation):
         path = oracle.build(os.path.join(d, f"mut{mutation}.so"), mutation=mutation)
         lib = oracle.load(path)
         assert not _pins_pass(lib), f"mutation {mutation} slipped through the pins"
+
+
+# --------------------------------------------------------------------------- #
+# y = alpha A x + beta y and the multi-vector form
+# --------------------------------------------------------------------------- #
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-1.0, 1.0), (2.5, -0.5), (0.0, 3.0), (-3.0, 0.0)])
+def test_scaled_matches_dense(alpha, beta):
+    csr = random_csr(48, 0.2, seed=21, integer_values=True, duplicates=True, empty_row_fraction=0.2)
+    x = integer_x(48, seed=4)
+    y_old = integer_x(48, seed=5)
+    ref = oracle.spmv_scaled(csr, x, alpha, beta, y_old)
+    expect = alpha * (dense_of(csr) @ x) + beta * y_old  # small integers and halves: exact
+    assert np.array_equal(ref["y"], expect)
+    if alpha == 1.0 and beta == 0.0:
+        plain = oracle.spmv(csr, x)
+        for key in ("y", "y_hi", "y_lo", "scale"):
+            assert np.array_equal(ref[key], plain[key])
+
+
+def test_scaled_beta_zero_ignores_y():
+    csr = random_csr(30, 0.3, seed=2)
+    x = uniform_x(30, seed=3)
+    y_nan = np.full(30, np.nan)
+    ref = oracle.spmv_scaled(csr, x, 2.0, 0.0, y_nan)
+    assert np.all(np.isfinite(ref["y"]))
+    assert np.all(np.abs(ref["y_hi"] - 2.0 * (dense_of(csr) @ x)) <= 1e-13 * ref["scale"])
+
+
+@pytest.mark.parametrize("k", [1, 3, 8])
+def test_spmm_matches_dense(k):
+    csr = random_csr(40, 0.25, seed=7, integer_values=True, empty_row_fraction=0.1)
+    rng = np.random.default_rng(k)
+    X = rng.integers(-8, 9, size=(40, k)).astype(np.float64)
+    Y = rng.integers(-8, 9, size=(40, k)).astype(np.float64)
+    ref = oracle.spmm(csr, X, -1.0, 2.0, Y)
+    assert ref["y"].shape == (40, k)
+    assert np.array_equal(ref["y"], -1.0 * (dense_of(csr) @ X) + 2.0 * Y)
