@@ -14,10 +14,12 @@ Contents
 * :func:`spmv_scaled`, :func:`spmm` -- y = alpha A x + beta y and its multi-vector
   form Y = alpha A X + beta Y, from the long double product above.
 * :func:`check_rows` -- the acceptance rule for a computed y.
+* :mod:`oracle.cg` -- conjugate gradients (Hestenes-Stiefel) in float64 on the
+  product above, for the solver built on the library.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
-against values the pages state, closed forms, and brute force; none of them is
-"parity unpinned".
+(``tests/test_cg_oracle_pins.py`` for CG) against values the pages state, closed
+forms, and brute force; none of them is "parity unpinned".
 """
 from __future__ import annotations
 
