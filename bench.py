@@ -499,6 +499,56 @@ def run_multi(args):
         A.close()
 
 
+def run_cg(args):
+    """Conjugate gradients (spmv_cg) on a Laplacian: time per iteration from two fixed-step
+    runs, then one solve to 1e-6; one JSON line per value type."""
+    import numpy as np
+    import torch
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+    from workloads import make_workload
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = load_peaks()
+    for dt in (np.float64, np.float32):
+        csr, b_np = make_workload(args.workload, dtype=dt)
+        sv = csr.vals.dtype.itemsize
+        dev = torch.device("cuda", 0)
+        rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
+        b = torch.from_numpy(b_np).to(dev)
+        x = torch.zeros_like(b)
+        A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=args.format)
+        A.cg(b, x, rtol=0.0, max_iter=max(args.warmup, 3))
+
+        def timed(iters):
+            x.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            _, it, _ = A.cg(b, x, rtol=0.0, max_iter=iters)
+            e1.record()
+            torch.cuda.synchronize()
+            assert it == iters
+            return e0.elapsed_time(e1)
+
+        long_run, short_run = args.cg, max(args.cg // 4, 1)
+        ms_iter = statistics.median((timed(long_run) - timed(short_run)) / (long_run - short_run) for _ in range(5))
+        x.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        _, it, res = A.cg(b, x, rtol=1e-6, max_iter=100000)
+        solve_s = time.perf_counter() - t0
+        # algorithmic bytes of one iteration: the product, p.q (2 vectors read), the r
+        # update (q, r read; r written), the x and p updates (p, x, r read; x, p written)
+        bytes_iter = effective_bytes(csr.n, csr.nnz, sv) + 10 * csr.n * sv
+        print(json.dumps({"workload": args.workload, "dtype": "f64" if sv == 8 else "f32", "solver": "cg",
+                          "format": A.describe()["format"], "us_per_iteration": ms_iter * 1e3,
+                          "launches_per_iteration": 4, "bytes_per_iteration": bytes_iter,
+                          "effective_gbs": bytes_iter / ms_iter / 1e6, "frac": bytes_iter / ms_iter / 1e6 / peak,
+                          "peak": f"{peak} GB/s {peak_kind}", "solve_rtol": 1e-6, "solve_iterations": it,
+                          "solve_relative_residual": res, "solve_wall_ms": solve_s * 1e3}), flush=True)
+        A.close()
+
+
 def run_sweep(args):
     """One JSON line per storage format on the chosen workload (format comparison)."""
     import numpy as np
@@ -561,10 +611,14 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
     ap.add_argument("--nrhs", type=int, default=0,
                     help="with --sweep: time the multi-vector apply with this many right-hand sides instead")
+    ap.add_argument("--cg", type=int, default=0, metavar="ITERS",
+                    help="time conjugate gradients (ITERS fixed steps per run) instead of the bench line")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.cg > 0:
+        run_cg(args)
     elif args.sweep and args.nrhs > 0:
         run_multi(args)
     elif args.sweep:

@@ -198,6 +198,32 @@ SPMV_API int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double 
 SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, int64_t ldx, double beta,
                               void *Y, int64_t ldy, void *stream);
 
+/*
+ * Solve A x = b by conjugate gradients (Hestenes-Stiefel), the Krylov iteration the
+ * Krylov/AMG paper lists among its solvers (section on Krylov subspace algorithms),
+ * built on this handle's apply and on device vector kernels.  A must be symmetric
+ * positive definite; the handle's format does not matter.
+ *
+ *   b     device vector, length n, the handle's value type; read only.
+ *   x     device vector, length n: the initial guess on entry, the iterate on return.
+ *         Must not alias b.
+ *   rtol  stop at the first iteration k with ||r_k||_2 <= rtol * ||b||_2, where r_k is
+ *         the recurrence residual (||b|| is replaced by 1 when b = 0).  rtol = 0 runs
+ *         exactly max_iter iterations unless the residual reaches 0.
+ *   max_iter  upper bound on iterations (0: only the initial residual is computed).
+ *   iterations, relative_residual  (host pointers, may be NULL) iterations done and
+ *         ||r_k|| / ||b|| at the end.
+ *
+ * Arithmetic: vectors in the value type; every dot product and the step lengths in
+ * double, reduced in a fixed order (results are reproducible).  Workspace (3 vectors)
+ * is taken from the stream-ordered pool of `stream` and returned before the call ends.
+ * Synchronises `stream`.  Returns SPMV_ERR_UNSUPPORTED (after filling the outputs) if
+ * p.Ap <= 0 at some step, i.e. A is not positive definite; SPMV_ERR_INVALID_ARG for a
+ * NULL handle or vector, aliasing, max_iter < 0 or rtol < 0 / NaN.
+ */
+SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double rtol, int32_t max_iter, void *stream,
+                     int32_t *iterations, double *relative_residual);
+
 /* Release every device buffer of the handle.  NULL is accepted and ignored. */
 SPMV_API void spmv_destroy(spmv_handle_t h);
 

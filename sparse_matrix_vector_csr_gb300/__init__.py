@@ -21,6 +21,7 @@ from ._abi import (  # noqa: F401
     spmv_apply_profiled,
     spmv_build_from_csr,
     spmv_build_from_csr_ex,
+    spmv_cg,
     spmv_csr_apply_noalloc,
     spmv_default_params,
     spmv_describe,
@@ -105,6 +106,19 @@ class SpmvMatrix:
             raise TypeError("Y must match X in shape and type, with unit column stride")
         spmv_apply_multi(self._h, X.shape[1], alpha, X, X.stride(0), beta, Y, Y.stride(0), stream)
         return Y
+
+    def cg(self, b, x=None, rtol=1e-8, max_iter=1000, stream=None):
+        """Solve A x = b by conjugate gradients on the device (A symmetric positive definite).
+        ``x`` is the initial guess (zeros when not given) and is updated in place.
+        Returns (x, iterations, relative_residual)."""
+        import torch
+
+        self._check_vec(b, "b")
+        if x is None:
+            x = torch.zeros_like(b)
+        self._check_vec(x, "x")
+        it, res = spmv_cg(self._h, b, x, rtol, max_iter, stream)
+        return x, it, res
 
     __matmul__ = apply
 

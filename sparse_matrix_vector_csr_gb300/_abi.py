@@ -26,7 +26,7 @@ EXPORTS = (
     "spmv_default_params", "spmv_build_from_csr", "spmv_build_from_csr_ex", "spmv_apply",
     "spmv_apply_host", "spmv_apply_profiled", "spmv_destroy", "spmv_last_error",
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
-    "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi",
+    "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg",
 )
 
 
@@ -87,6 +87,8 @@ def _load():
     lib.spmv_apply_ex.restype = c_int
     lib.spmv_apply_multi.argtypes = [vp, i64, f64, vp, i64, f64, vp, i64, vp]
     lib.spmv_apply_multi.restype = c_int
+    lib.spmv_cg.argtypes = [vp, vp, vp, f64, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(f64)]
+    lib.spmv_cg.restype = c_int
     del i32
     return lib
 
@@ -237,3 +239,13 @@ def spmv_apply_multi(h, k, alpha, X, ldx, beta, Y, ldy, stream=None) -> None:
     """Y = alpha * A X + beta * Y for k row-major right-hand sides."""
     _check(lib.spmv_apply_multi(h, int(k), float(alpha), _ptr(X), int(ldx), float(beta), _ptr(Y), int(ldy),
                                 _stream(stream)))
+
+
+def spmv_cg(h, b, x, rtol, max_iter, stream=None):
+    """Conjugate gradients for A x = b (x holds the initial guess and receives the iterate).
+    Returns (iterations, relative_residual)."""
+    it = ctypes.c_int32(0)
+    res = ctypes.c_double(0.0)
+    _check(lib.spmv_cg(h, _ptr(b), _ptr(x), float(rtol), int(max_iter), _stream(stream), ctypes.byref(it),
+                       ctypes.byref(res)))
+    return int(it.value), float(res.value)

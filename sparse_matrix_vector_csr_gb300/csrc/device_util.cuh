@@ -50,5 +50,12 @@ __device__ __forceinline__ T gather_x(const T *p) {
         return __ldg(p);
 }
 
+// Programmatic dependent launch (kernels launched with programmatic stream
+// serialization): grid_wait() blocks until the previous kernel of the stream has
+// finished and its writes are visible; allow_dependents() lets the next kernel of the
+// stream be scheduled before this one ends.
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace dev
 }  // namespace spmv

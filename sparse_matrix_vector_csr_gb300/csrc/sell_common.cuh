@@ -7,6 +7,7 @@
 
 #include <cstdint>
 
+#include "device_util.cuh"
 #include "spmv_internal.cuh"
 
 namespace spmv {
@@ -62,8 +63,8 @@ struct SplitArgs {
 // kernel of the stream is still draining.  Everything read before grid_wait() is
 // the handle's own matrix data, immutable after the build; x (which the previous
 // kernel may produce) and y (which it may still read) are touched only after it.
-__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+using dev::allow_dependents;
+using dev::grid_wait;
 
 inline SellArgs sell_args(const Sliced &sl, int64_t n) {
     return SellArgs{sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.len, sl.perm, sl.col, n};
