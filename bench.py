@@ -108,14 +108,22 @@ def kernel_source(kernel: str) -> str:
     return os.path.join(ROOT, "sparse_matrix_vector_csr_gb300", "csrc", name)
 
 
+#: headers every kernel source includes; a change there changes the kernels too
+KERNEL_HEADERS = ("spmv_internal.cuh", "device_util.cuh", "sell_common.cuh")
+
+
 def source_sha(kernel: str) -> str | None:
-    """Hash of the source file that holds a kernel (a committed ncu figure is only
-    valid for the kernel it was taken on)."""
+    """Hash of the source file that holds a kernel and of the shared headers (a committed
+    ncu figure is only valid for the kernel it was taken on)."""
+    h = hashlib.sha256()
+    src = kernel_source(kernel)
     try:
-        with open(kernel_source(kernel), "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
+        for path in [src] + [os.path.join(os.path.dirname(src), hd) for hd in KERNEL_HEADERS]:
+            with open(path, "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
+    return h.hexdigest()[:16]
 
 
 def committed_traffic(workload: str, dtype: str, kernel: str):
