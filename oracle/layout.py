@@ -53,14 +53,16 @@ def sell_order(lens, sigma: int) -> np.ndarray:
     return perm
 
 
-def sell_layout(lens, C: int, sigma: int, exclude=None) -> dict:
+def sell_layout(lens, C: int, sigma: int, exclude=None, group: int = 1) -> dict:
     """SELL-C-sigma layout sizes.
 
     ``exclude``: rows that are stored elsewhere (long rows); they count as empty here.
+    ``group``: slice widths are rounded up to a multiple of it (the column-grouped
+    layout for ``group`` threads per row stores whole groups).
     Returned keys:
       perm            sorted position -> original row (length n)
       sorted_lens     lengths in sorted order (excluded rows are 0)
-      widths          per-slice width = longest row in the slice (n_slices)
+      widths          per-slice width = longest row in the slice, rounded up to whole groups (n_slices)
       slice_ptr       int64 exclusive scan of C * width (n_slices + 1)
       padded_entries  sum over real rows of their slice's width
       allocated_slots sum over slices of C * width (includes the rows that pad n to a multiple of C)
@@ -75,6 +77,7 @@ def sell_layout(lens, C: int, sigma: int, exclude=None) -> dict:
     padded = np.zeros(n_slices * C, dtype=np.int64)
     padded[:n] = sorted_lens
     widths = padded.reshape(n_slices, C).max(axis=1) if n_slices else np.zeros(0, np.int64)
+    widths = -(-widths // group) * group
     slice_ptr = np.zeros(n_slices + 1, dtype=np.int64)
     np.cumsum(widths * C, out=slice_ptr[1:])
     rows_in_slice = np.minimum(C, n - np.arange(n_slices) * C)
@@ -86,6 +89,64 @@ def sell_layout(lens, C: int, sigma: int, exclude=None) -> dict:
         "padded_entries": int((widths * rows_in_slice).sum()),
         "allocated_slots": int(slice_ptr[-1]),
     }
+
+
+def slot_offset(q, j, stride: int, group: int = 1, interleaved: bool = False):
+    """Offset, inside its slice, of entry j of the row at in-slice position q.
+
+    Column-major (the ELLPACK / SELL layout of the spMVM paper, Fig. 1): entry j of all
+    rows of the slice is contiguous, offset j * stride + q.  Column-grouped (the AMD
+    rearrangement the load-balancing SpMV paper describes, for ``group`` threads per
+    row): the slice is walked group of columns by group of columns, then row by row,
+    then column by column inside the group, i.e. entries j of row q with the same
+    j // group sit side by side: offset ((j // group) * stride + q) * group + j % group.
+    """
+    q = np.asarray(q, dtype=np.int64)
+    j = np.asarray(j, dtype=np.int64)
+    if not interleaved:
+        return j * stride + q
+    return ((j // group) * stride + q) * group + j % group
+
+
+def sell_slots(csr, C: int, sigma: int, exclude=None, group: int = 1, interleaved: bool = False,
+               ell_ld: int | None = None) -> tuple:
+    """The slot arrays (column, value) of a sliced layout built from ``csr``.
+
+    SELL (``ell_ld`` None): slices of C sorted positions with ``sell_layout`` widths.
+    ELLPACK (``ell_ld`` given): one slice, rows in natural order, leading dimension
+    ``ell_ld``, width = the longest stored row.  Widths are rounded up to whole groups
+    in the column-grouped (interleaved) layout only.  Excluded
+    rows and padding slots hold column 0 and value 0.
+    """
+    lens = row_lengths(csr.row_ptr)
+    round_to = group if interleaved else 1  # only the column-grouped layout stores whole groups
+    if ell_ld is None:
+        lay = sell_layout(lens, C, sigma, exclude=exclude, group=round_to)
+        perm, stored, starts, stride = lay["perm"], lay["sorted_lens"], lay["slice_ptr"], C
+        total = int(starts[-1])
+        pos = np.arange(perm.size, dtype=np.int64)
+        base = starts[pos // C]
+        q = pos % C
+    else:
+        stored = lens.astype(np.int64).copy()
+        if exclude is not None and len(exclude):
+            stored[np.asarray(exclude, dtype=np.int64)] = 0
+        perm = np.arange(csr.n, dtype=np.int64)
+        width = int(stored.max()) if stored.size else 0
+        width = -(-width // round_to) * round_to
+        stride, total = ell_ld, ell_ld * width
+        base = np.zeros(csr.n, dtype=np.int64)
+        q = np.arange(csr.n, dtype=np.int64)
+    col = np.zeros(total, dtype=np.int32)
+    val = np.zeros(total, dtype=csr.vals.dtype)
+    reps = stored.astype(np.int64)
+    P = np.repeat(np.arange(perm.size), reps)
+    J = np.arange(P.size) - np.repeat(np.cumsum(reps) - reps, reps)
+    src = csr.row_ptr[perm[P]].astype(np.int64) + J
+    off = base[P] + slot_offset(q[P], J, stride, group, interleaved)
+    col[off] = csr.col_idx[src]
+    val[off] = csr.vals[src]
+    return col, val
 
 
 def ellpack_entries(lens) -> int:

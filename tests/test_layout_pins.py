@@ -125,3 +125,93 @@ def test_hyb_width_cap_and_uniform_rows():
 def test_ell_leading_dimension(n):
     ld = layout.ell_leading_dim(n)
     assert ld >= n and ld % 256 == 0 and ld % 32 == 0 and ld - n < 256
+
+
+# --------------------------------------------------------------------------- #
+# slot placement: column-major and column-grouped (interleaved) layouts
+# --------------------------------------------------------------------------- #
+
+
+@pytest.mark.parametrize("stride,width,group", [(32, 12, 4), (64, 16, 8), (32, 32, 32), (40, 6, 2), (32, 7, 1)])
+def test_interleaved_offsets_enumerate_groups_rows_lanes(stride, width, group):
+    """Walking the slice group of columns by group, then row by row, then column by column
+    visits offsets 0, 1, 2, ... -- the column-grouped layout's definition."""
+    width = -(-width // group) * group
+    for interleaved in (True, False):
+        for (q, j), off in _walk_offsets(stride, width, group, interleaved).items():
+            assert layout.slot_offset(q, j, stride, group, interleaved) == off
+
+
+@pytest.mark.parametrize("group", [2, 4, 8, 16, 32])
+def test_interleaved_warp_reads_consecutive_slots(group):
+    """32 threads = 32/group rows x group lanes; at step k lane l of row q reads entry
+    k*group + l: the warp's 32 offsets are 32 consecutive slots."""
+    stride = 64
+    for q0 in range(0, stride, 32 // group):
+        for k in range(3):
+            offs = sorted(int(layout.slot_offset(q0 + r, k * group + l, stride, group, True))
+                          for r in range(32 // group) for l in range(group))
+            assert offs == list(range(offs[0], offs[0] + 32))
+
+
+def _walk_offsets(stride, width, group, interleaved):
+    """Offsets of (q, j) by walking the slice in the layout's order (no formula)."""
+    order = {}
+    if interleaved:
+        walk = ((q, jg * group + lane) for jg in range(width // group) for q in range(stride) for lane in range(group))
+    else:
+        walk = ((q, j) for j in range(width) for q in range(stride))
+    for k, key in enumerate(walk):
+        order[key] = k
+    return order
+
+
+def _brute_slots(csr, C, sigma, exclude, group, interleaved, ell_ld=None):
+    lens = layout.row_lengths(csr.row_ptr)
+    round_to = group if interleaved else 1
+    if ell_ld is None:
+        lay = layout.sell_layout(lens, C, sigma, exclude=exclude, group=round_to)
+        col = np.zeros(int(lay["slice_ptr"][-1]), np.int32)
+        val = np.zeros(col.size, csr.vals.dtype)
+        walks = [_walk_offsets(C, int(w), group, interleaved) for w in lay["widths"]]
+        for p, r in enumerate(lay["perm"]):
+            s, q = divmod(p, C)
+            for j in range(int(lay["sorted_lens"][p])):
+                off = walks[s][(q, j)]
+                col[lay["slice_ptr"][s] + off] = csr.col_idx[csr.row_ptr[r] + j]
+                val[lay["slice_ptr"][s] + off] = csr.vals[csr.row_ptr[r] + j]
+        return col, val
+    stored = lens.copy()
+    if exclude is not None:
+        stored[exclude] = 0
+    w = -(-int(stored.max()) // round_to) * round_to
+    col = np.zeros(ell_ld * w, np.int32)
+    val = np.zeros(col.size, csr.vals.dtype)
+    walk = _walk_offsets(ell_ld, w, group, interleaved)
+    for r in range(csr.n):
+        for j in range(int(stored[r])):
+            off = walk[(r, j)]
+            col[off] = csr.col_idx[csr.row_ptr[r] + j]
+            val[off] = csr.vals[csr.row_ptr[r] + j]
+    return col, val
+
+
+@pytest.mark.parametrize("C,sigma,group,interleaved", [(32, 1, 1, False), (32, 8, 4, True), (64, 1000, 8, True),
+                                                       (32, 1, 2, False), (32, 16, 32, True), (64, 1, 8, False)])
+def test_sell_slots_brute_force(C, sigma, group, interleaved):
+    from workloads import random_csr
+    csr = random_csr(150, density=0.08, seed=7)
+    lens = layout.row_lengths(csr.row_ptr)
+    exclude = layout.long_rows(lens, 20)
+    got = layout.sell_slots(csr, C, sigma, exclude=exclude, group=group, interleaved=interleaved)
+    exp = _brute_slots(csr, C, sigma, exclude, group, interleaved)
+    assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1])
+
+
+@pytest.mark.parametrize("group,interleaved", [(1, False), (4, True), (8, False)])
+def test_ell_slots_brute_force(group, interleaved):
+    from workloads import random_csr
+    csr = random_csr(90, density=0.1, seed=8)
+    got = layout.sell_slots(csr, 0, 1, group=group, interleaved=interleaved, ell_ld=96)
+    exp = _brute_slots(csr, 0, 1, None, group, interleaved, ell_ld=96)
+    assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1])
