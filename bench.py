@@ -104,7 +104,12 @@ KERNEL_SOURCES = {"sell": "sell.cu", "ell_r": "sell.cu", "hyb_ell": "sell.cu", "
 
 
 def kernel_source(kernel: str) -> str:
-    name = "vector.cu" if kernel.startswith("csr_vector") else KERNEL_SOURCES.get(kernel, "")
+    if kernel.startswith("csr_vector"):
+        name = "vector.cu"
+    elif "_g" in kernel and kernel.split("_g")[-1][:-1].isdigit():  # G threads per row: sell_g4i, ell_r_g8r, ...
+        name = "sellg.cu"
+    else:
+        name = KERNEL_SOURCES.get(kernel, "")
     return os.path.join(ROOT, "sparse_matrix_vector_csr_gb300", "csrc", name)
 
 
@@ -464,6 +469,11 @@ SWEEP_FORMATS = [
     ("sell", {"C": 32, "sigma": 1}), ("sell", {"C": 64, "sigma": 1}), ("sell", {"C": 32, "sigma": 256}),
     ("sell", {"C": 64, "sigma": 256}), ("sell", {"C": 32, "sigma": 1 << 30}), ("sell", {"C": 64, "sigma": 1 << 30}),
     ("hyb", {}), ("hyb", {"spill_csr": 0}), ("hyb", {"K": 20}), ("merge", {}),
+    ("sell", {"row_threads": 1}), ("sell", {"row_threads": 2}), ("sell", {"row_threads": 4}), ("sell", {"row_threads": 8}),
+    ("sell", {"row_threads": 16}), ("sell", {"row_threads": 32}), ("sell", {"row_threads": 4, "row_group_mode": 0}),
+    ("sell", {"row_threads": 8, "row_group_mode": 0}), ("sell", {"row_threads": 2, "row_group_mode": 2}),
+    ("sell", {"row_threads": 4, "row_group_mode": 2}), ("sell", {"row_threads": 8, "row_group_mode": 2}),
+    ("ell_r", {"row_threads": 4}),
 ]
 
 

@@ -100,6 +100,19 @@ typedef enum {
  *   long_row_threshold  rows with more entries go to the merge-path pass.  0 = never.
  *   subwarp             CSR-vector lanes per row (2, 4, 8, 16 or 32) for every row;
  *                       automatic = per row-length bin.
+ *   row_threads         threads per row in the SELL / ELLPACK-R / HYB-ELL apply (1, 2, 4,
+ *                       8, 16 or 32), the multi-thread-per-row ELL variants of the
+ *                       load-balancing SpMV paper.  Automatic: 1, unless one thread per
+ *                       row gives fewer than two waves of threads on the device; then it
+ *                       doubles while that holds and an average stored row still gives
+ *                       each thread at least 16 entries.
+ *   row_group_mode      with row_threads = G > 1: 0 = row-grouped (column-major slots,
+ *                       G adjacent threads per row striding over its entries); 1 =
+ *                       interleaved slots (a row's entries in groups of G side by side,
+ *                       same threads, so a warp reads 32 consecutive slots); 2 =
+ *                       column-grouped (column-major slots, a warp per 32 rows and
+ *                       residue class of entries mod G, G warps per row combined in
+ *                       shared memory; G <= 8).  Automatic = 1.
  */
 typedef struct {
     int32_t C;
@@ -108,6 +121,8 @@ typedef struct {
     int32_t spill_csr;
     int32_t long_row_threshold;
     int32_t subwarp;
+    int32_t row_threads;
+    int32_t row_group_mode;
 } spmv_format_params;
 
 typedef enum {
@@ -258,6 +273,19 @@ SPMV_API int spmv_describe(spmv_handle_t h, char *json, size_t cap);
  * SPMV_ERR_UNSUPPORTED for a handle without a sliced part.  Synchronises `stream`.
  */
 SPMV_API int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr, void *stream);
+
+/*
+ * Copy the slot arrays of the sliced part: col int32[slots] and val[slots] (value
+ * type of the handle), slots as in spmv_describe ("slots").  Entry j of the row at
+ * in-slice position q of a slice starting at slice_ptr[s] sits at
+ *   slice_ptr[s] + j * stride + q                                   (column-major), or
+ *   slice_ptr[s] + ((j / g) * stride + q) * g + j % g   (interleaved, g = row_threads,
+ *                                                        "row_group_mode": 1),
+ * stride = C for SELL and the leading dimension "ld" for ELLPACK-R / HYB-ELL.  Padding
+ * slots hold column 0 and value 0.  Either pointer may be NULL (device memory owned
+ * by the caller).  SPMV_ERR_UNSUPPORTED without a sliced part.  Synchronises `stream`.
+ */
+SPMV_API int spmv_get_slots(spmv_handle_t h, int32_t *col, void *val, void *stream);
 
 /*
  * y = A x computed directly from a CSR matrix in the caller's device memory, with

@@ -28,6 +28,7 @@ from ._abi import (  # noqa: F401
     spmv_destroy,
     spmv_error_string,
     spmv_get_layout,
+    spmv_get_slots,
     spmv_last_error,
     spmv_last_error_message,
     spmv_to_csr,
@@ -159,6 +160,17 @@ class SpmvMatrix:
         sp = torch.empty(d["n_slices"] + 1, dtype=torch.int64, device=dev)
         spmv_get_layout(self._h, perm, sp)
         return perm, sp
+
+    def slots(self):
+        """(col, val): the sliced part's slot arrays as CUDA tensors."""
+        import torch
+
+        d = self.describe()
+        dev = torch.device("cuda", torch.cuda.current_device())
+        col = torch.empty(d["slots"], dtype=torch.int32, device=dev)
+        val = torch.empty(d["slots"], dtype=self.dtype, device=dev)
+        spmv_get_slots(self._h, col, val)
+        return col, val
 
     def close(self):
         if self._h:

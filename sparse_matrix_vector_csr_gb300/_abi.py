@@ -26,7 +26,7 @@ EXPORTS = (
     "spmv_default_params", "spmv_build_from_csr", "spmv_build_from_csr_ex", "spmv_apply",
     "spmv_apply_host", "spmv_apply_profiled", "spmv_destroy", "spmv_last_error",
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
-    "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg",
+    "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
 )
 
 
@@ -44,6 +44,8 @@ class FormatParams(ctypes.Structure):
         ("spill_csr", ctypes.c_int32),
         ("long_row_threshold", ctypes.c_int32),
         ("subwarp", ctypes.c_int32),
+        ("row_threads", ctypes.c_int32),
+        ("row_group_mode", ctypes.c_int32),
     ]
 
 
@@ -80,6 +82,8 @@ def _load():
     lib.spmv_describe.restype = c_int
     lib.spmv_get_layout.argtypes = [vp, vp, vp, vp]
     lib.spmv_get_layout.restype = c_int
+    lib.spmv_get_slots.argtypes = [vp, vp, vp, vp]
+    lib.spmv_get_slots.restype = c_int
     lib.spmv_csr_apply_noalloc.argtypes = [i64, i64, vp, vp, vp, c_int, vp, vp, vp]
     lib.spmv_csr_apply_noalloc.restype = c_int
     f64 = ctypes.c_double
@@ -143,11 +147,13 @@ def dtype_code(dtype) -> int:
     raise TypeError(f"unsupported value type {dtype}")
 
 
-def make_params(C=-1, sigma=-1, K=-1, spill_csr=-1, long_row_threshold=-1, subwarp=-1) -> FormatParams:
+def make_params(C=-1, sigma=-1, K=-1, spill_csr=-1, long_row_threshold=-1, subwarp=-1, row_threads=-1,
+                row_group_mode=-1) -> FormatParams:
     p = FormatParams()
     lib.spmv_default_params(ctypes.byref(p))
     p.C, p.sigma, p.K = int(C), int(sigma), int(K)
     p.spill_csr, p.long_row_threshold, p.subwarp = int(spill_csr), int(long_row_threshold), int(subwarp)
+    p.row_threads, p.row_group_mode = int(row_threads), int(row_group_mode)
     return p
 
 
@@ -222,6 +228,11 @@ def spmv_describe(h) -> dict:
 
 def spmv_get_layout(h, perm=None, slice_ptr=None, stream=None) -> None:
     _check(lib.spmv_get_layout(h, _ptr(perm), _ptr(slice_ptr), _stream(stream)))
+
+
+def spmv_get_slots(h, col=None, val=None, stream=None) -> None:
+    """Copy the sliced part's slot arrays into device tensors (see spmv.h)."""
+    _check(lib.spmv_get_slots(h, _ptr(col), _ptr(val), _stream(stream)))
 
 
 def spmv_csr_apply_noalloc(n, nnz, row_ptr, col_idx, vals, dtype, x, y, stream=None) -> None:

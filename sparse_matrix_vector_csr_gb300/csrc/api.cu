@@ -155,6 +155,9 @@ struct BuildCtx {
     int64_t n_long = 0, long_nnz = 0;
     int32_t max_short = 0;
     int32_t threshold = -1;  // -1 = no long-row cut
+    int32_t group = 1;       // threads per row of the sliced apply
+    int group_mode = 0;      // 0 row-grouped, 1 interleaved slots, 2 column-grouped
+    bool interleaved = false;
     Temp temp;
 };
 
@@ -294,6 +297,25 @@ int build_long_rows(BuildCtx &c, int accumulate) {
 // sliced part (SELL-C-sigma, ELLPACK-R, HYB's ELL)
 // ---------------------------------------------------------------------------
 
+// Kernel-name suffix of the G-threads-per-row apply: _g<G> and r (row-grouped),
+// i (interleaved slots) or c (column-grouped).
+std::string group_suffix(const BuildCtx &c) {
+    return "_g" + std::to_string(c.group) + (c.group_mode == 2 ? "c" : c.group_mode == 1 ? "i" : "r");
+}
+
+// Threads per row of the sliced apply when not given: one, unless the rows are too few
+// to give about two waves of threads (2 x SMs x 2048) at one per row and long enough to
+// share; then double while that stays short of two waves and each thread keeps at least
+// 16 entries of an average stored row.
+int32_t auto_row_threads(int64_t n, int64_t stored, int sms) {
+    if (n <= 0) return 1;
+    const double target = 2.0 * sms * 2048.0;
+    const double mean = static_cast<double>(stored) / static_cast<double>(n);
+    int32_t g = 1;
+    while (g < 32 && static_cast<double>(n) * g < target && mean >= 32.0 * g) g *= 2;
+    return g;
+}
+
 // Plan: order, per-position lengths, slice widths and offsets.  `lens` are the
 // lengths to store (long rows already 0).  ell_ld > 0 selects the single-slice
 // ELL addressing with that leading dimension and width = max length.
@@ -304,6 +326,11 @@ int plan_sliced(BuildCtx &c, const int32_t *lens, int32_t C, int64_t sigma, int6
     sl = Sliced();
     sl.present = true;
     sl.sigma = sigma;
+    sl.group = c.group;
+    sl.log2g = bits_for(static_cast<uint64_t>(c.group)) - 1;
+    sl.group_mode = c.group_mode;
+    sl.interleaved = c.interleaved;
+    const int32_t round_to = c.interleaved ? c.group : 1;
     if (ell_ld > 0) {
         sl.C = static_cast<int32_t>(std::min<int64_t>(ell_ld, INT32_MAX));
         sl.ld = ell_ld;
@@ -364,19 +391,20 @@ int plan_sliced(BuildCtx &c, const int32_t *lens, int32_t C, int64_t sigma, int6
     SPMV_TRY(dev_alloc_n(h, &sl.slice_ptr, sl.n_slices + 1));
     std::vector<int32_t> widths(static_cast<size_t>(sl.n_slices));
     if (ell_ld > 0) {
-        widths[0] = max_len;
+        const int32_t w = (max_len + round_to - 1) / round_to * round_to;
+        widths[0] = w;
         SPMV_TRY_CUDA(cudaMemcpyAsync(sl.width, widths.data(), sizeof(int32_t), cudaMemcpyHostToDevice, c.s));
-        const int64_t sp[2] = {0, ell_ld * static_cast<int64_t>(max_len)};
+        const int64_t sp[2] = {0, ell_ld * static_cast<int64_t>(w)};
         SPMV_TRY_CUDA(cudaMemcpyAsync(sl.slice_ptr, sp, sizeof(sp), cudaMemcpyHostToDevice, c.s));
         SPMV_TRY(sync(c.s));
         sl.slots = sp[1];
-        sl.padded_entries = n * static_cast<int64_t>(max_len);
-        sl.max_width = max_len;
+        sl.padded_entries = n * static_cast<int64_t>(w);
+        sl.max_width = w;
     } else {
         int64_t *sizes = nullptr, *scan_tmp = nullptr;
         SPMV_TRY(c.temp.get(&sizes, sl.n_slices));
         SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(sl.n_slices)));
-        SPMV_TRY_CUDA(launch_slice_widths(sl.len, sl.n_slices, sl.C, sl.width, sizes, c.s));
+        SPMV_TRY_CUDA(launch_slice_widths(sl.len, sl.n_slices, sl.C, sl.width, sizes, c.s, round_to));
         SPMV_TRY_CUDA(launch_exclusive_scan(sizes, sl.n_slices, sl.slice_ptr, scan_tmp, c.s));
         SPMV_TRY_CUDA(cudaMemcpyAsync(widths.data(), sl.width, sizeof(int32_t) * sl.n_slices,
                                       cudaMemcpyDeviceToHost, c.s));
@@ -433,7 +461,12 @@ int build_sell_like(BuildCtx &c, int format, int32_t C, int64_t sigma) {
     SPMV_TRY(fill_sliced(c));
     SPMV_TRY(build_long_rows(c, 0));
     const std::string name = format == SPMV_FMT_ELL_R ? "ell_r" : "sell";
-    h->kernels.push_back(h->seg.kind == 3 ? name + "+rowsplit" : name);
+    if (c.group > 1) {  // grouped kernel, then the long rows' chunks in a launch of their own
+        h->kernels.push_back(name + group_suffix(c));
+        if (h->seg.kind == 3) h->kernels.push_back("rowsplit_chunks");
+    } else {
+        h->kernels.push_back(h->seg.kind == 3 ? name + "+rowsplit" : name);
+    }
     return SPMV_OK;
 }
 
@@ -458,7 +491,7 @@ int build_hyb(BuildCtx &c, int32_t K, int spill_csr) {
     const int64_t m = start[2] - start[1];
     SPMV_TRY(build_segment(c, rows + start[1], m, K, spill_csr ? 1 : 2, 1));
     h->sliced.stored_entries = h->nnz - h->seg.nnz;
-    h->kernels.push_back("hyb_ell");
+    h->kernels.push_back("hyb_ell" + (c.group > 1 ? group_suffix(c) : std::string()));
     return SPMV_OK;
 }
 
@@ -646,6 +679,31 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     h->params.sigma = sigma;
     h->params.long_row_threshold = c.threshold;
 
+    // threads per row of the sliced apply (SELL, ELLPACK-R, HYB's ELL part)
+    if (format == SPMV_FMT_SELL || format == SPMV_FMT_ELL_R || format == SPMV_FMT_HYB) {
+        int32_t g = prm.row_threads;
+        if (g > 0 && (g > 32 || (g & (g - 1))))
+            return set_error(SPMV_ERR_INVALID_ARG, "row_threads must be 1, 2, 4, 8, 16 or 32");
+        if (g <= 0) {
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+                (void)cudaGetLastError();
+                sms = 152;
+            }
+            g = auto_row_threads(n, nnz - c.long_nnz, sms);
+        }
+        int mode = prm.row_group_mode < 0 ? 1 : prm.row_group_mode;
+        if (mode > 2) return set_error(SPMV_ERR_INVALID_ARG, "row_group_mode must be 0, 1 or 2");
+        if (g == 1) mode = 0;
+        if (mode == 2 && g > 8)
+            return set_error(SPMV_ERR_UNSUPPORTED, "the column-grouped mode takes 2, 4 or 8 threads per row");
+        c.group = g;
+        c.group_mode = mode;
+        c.interleaved = mode == 1;
+    }
+    h->params.row_threads = c.group;
+    h->params.row_group_mode = c.group_mode;
+
     switch (format) {
         case SPMV_FMT_CSR_VECTOR: {
             int32_t g = prm.subwarp > 0 ? prm.subwarp : 0;
@@ -726,6 +784,7 @@ struct Recorder {
 
 // Formats whose kernels write y exactly once per row (so alpha/beta fold into that write).
 bool fused_epilogue(spmv_handle_t h) {
+    if (h->sliced.group > 1) return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
     return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && (h->seg.kind == 0 || h->seg.kind == 3);
 }
 
@@ -745,6 +804,14 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
                                             h->row_ptr, h->csr_col, h->csr_val, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
+        if (split) {
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
+            if (rec) SPMV_TRY(rec->mark(s));
+        }
+    } else if (h->sliced.present && h->sliced.group > 1) {
+        // G threads per row, then the long rows' chunks
+        SPMV_TRY_CUDA(launch_sellg_apply(h->dtype, h->sliced, h->n, x, y, s, scale));
+        if (rec) SPMV_TRY(rec->mark(s));
         if (split) {
             SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
@@ -858,6 +925,8 @@ int spmv_default_params(spmv_format_params *p) {
     p->spill_csr = -1;
     p->long_row_threshold = -1;
     p->subwarp = -1;
+    p->row_threads = -1;
+    p->row_group_mode = -1;
     return SPMV_OK;
 }
 
@@ -1035,6 +1104,24 @@ int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr, void *st
     return SPMV_OK;
 }
 
+int spmv_get_slots(spmv_handle_t h, int32_t *col, void *val, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (!h->sliced.present) return set_error(SPMV_ERR_UNSUPPORTED, "the handle has no sliced part");
+    SPMV_TRY(check_current_device(h));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t slots = h->sliced.slots;
+    if (col && slots > 0) {
+        SPMV_TRY(check_device_pointer(col, "col"));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(col, h->sliced.col, sizeof(int32_t) * slots, cudaMemcpyDeviceToDevice, s));
+    }
+    if (val && slots > 0) {
+        SPMV_TRY(check_device_pointer(val, "val"));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(val, h->sliced.val, value_bytes(h->dtype) * slots, cudaMemcpyDeviceToDevice, s));
+    }
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
 int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     if (!h || !json || cap == 0) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle or buffer");
     const int64_t vb = static_cast<int64_t>(value_bytes(h->dtype));
@@ -1048,6 +1135,7 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     append(o, "\"C\":%d,\"sigma\":%lld,\"K\":%d,\"spill_csr\":%d,\"long_row_threshold\":%d,\"subwarp\":%d,",
            h->params.C, (long long)h->params.sigma, h->params.K, h->params.spill_csr, h->params.long_row_threshold,
            h->params.subwarp);
+    append(o, "\"row_threads\":%d,\"row_group_mode\":%d,", h->params.row_threads, h->params.row_group_mode);
     append(o, "\"sliced\":%s,\"n_slices\":%lld,\"slots\":%lld,\"padded_entries\":%lld,\"stored_entries\":%lld,"
               "\"ld\":%lld,\"max_width\":%d,\"permuted\":%s,",
            sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,

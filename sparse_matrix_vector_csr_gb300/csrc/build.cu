@@ -361,7 +361,7 @@ __global__ void k_gather_sorted(const int32_t *__restrict__ len, const int32_t *
 }
 
 // one warp per slice: width = max over its C rows
-__global__ void k_slice_widths(const int32_t *__restrict__ len_sorted, int64_t n_slices, int32_t C,
+__global__ void k_slice_widths(const int32_t *__restrict__ len_sorted, int64_t n_slices, int32_t C, int32_t round_to,
                                int32_t *__restrict__ width, int64_t *__restrict__ size) {
     const int lane = threadIdx.x & 31;
     int64_t warp = gtid() >> 5;
@@ -372,6 +372,7 @@ __global__ void k_slice_widths(const int32_t *__restrict__ len_sorted, int64_t n
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (lane == 0) {
+            m = (m + round_to - 1) / round_to * round_to;  // whole groups for the interleaved layout
             width[s] = m;
             size[s] = static_cast<int64_t>(m) * C;
         }
@@ -379,7 +380,7 @@ __global__ void k_slice_widths(const int32_t *__restrict__ len_sorted, int64_t n
 }
 
 template <typename T>
-__global__ void k_fill_sliced(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
+__global__ void k_fill_sliced(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride, int log2g, bool interleaved,
                               const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ width,
                               const int32_t *__restrict__ len_sorted, const int32_t *__restrict__ perm,
                               const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_in,
@@ -388,11 +389,12 @@ __global__ void k_fill_sliced(int64_t n_pos, int log2C, uint32_t cmask, int64_t 
     for (int64_t p = gtid(); p < n_pos; p += gstride()) {
         int64_t s = p >> log2C;
         int32_t w = width[s];
-        int64_t slot = slice_ptr[s] + static_cast<int64_t>(p & cmask);
+        const int64_t base = slice_ptr[s], q = static_cast<int64_t>(p & cmask);
         int32_t L = len_sorted[p];
         int64_t src = 0;
         if (L > 0) src = row_ptr[perm ? perm[p] : p];
-        for (int32_t j = 0; j < w; ++j, slot += stride) {
+        for (int32_t j = 0; j < w; ++j) {
+            const int64_t slot = slot_of(base, q, j, stride, log2g, interleaved);
             if (j < L) {
                 col_out[slot] = col_in[src + j];
                 val_out[slot] = val_in[src + j];
@@ -511,8 +513,8 @@ __global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, const i
 // to_csr
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void k_sliced_to_csr(int64_t n, int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
-                                const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ len_sorted,
+__global__ void k_sliced_to_csr(int64_t n, int64_t n_pos, int log2C, uint32_t cmask, int64_t stride, int log2g,
+                                bool interleaved, const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ len_sorted,
                                 const int32_t *__restrict__ perm, const int32_t *__restrict__ col,
                                 const T *__restrict__ val, const int32_t *__restrict__ out_ptr,
                                 int32_t *__restrict__ out_col, T *__restrict__ out_val) {
@@ -520,9 +522,10 @@ __global__ void k_sliced_to_csr(int64_t n, int64_t n_pos, int log2C, uint32_t cm
         int64_t r = perm ? perm[p] : p;
         if (r < 0 || r >= n) continue;
         int32_t L = len_sorted[p];
-        int64_t slot = slice_ptr[p >> log2C] + static_cast<int64_t>(p & cmask);
+        const int64_t base = slice_ptr[p >> log2C], q = static_cast<int64_t>(p & cmask);
         int64_t dst = out_ptr[r];
-        for (int32_t j = 0; j < L; ++j, slot += stride) {
+        for (int32_t j = 0; j < L; ++j) {
+            const int64_t slot = slot_of(base, q, j, stride, log2g, interleaved);
             out_col[dst + j] = col[slot];
             out_val[dst + j] = val[slot];
         }
@@ -636,9 +639,10 @@ cudaError_t launch_gather_sorted(const int32_t *len, const int32_t *perm, int64_
 }
 
 cudaError_t launch_slice_widths(const int32_t *len_sorted, int64_t n_slices, int32_t C, int32_t *width,
-                                int64_t *size, cudaStream_t s) {
+                                int64_t *size, cudaStream_t s, int32_t round_to) {
     if (n_slices > 0)
-        k_slice_widths<<<grid_for(n_slices * 32, kBlock, 65536), kBlock, 0, s>>>(len_sorted, n_slices, C, width, size);
+        k_slice_widths<<<grid_for(n_slices * 32, kBlock, 65536), kBlock, 0, s>>>(len_sorted, n_slices, C, round_to,
+                                                                                width, size);
     return cudaGetLastError();
 }
 
@@ -647,12 +651,14 @@ cudaError_t launch_fill_sliced(int dtype, const Sliced &sl, const int32_t *row_p
     if (sl.n_pos <= 0 || sl.slots <= 0) return cudaSuccess;
     unsigned g = grid_for(sl.n_pos, kBlock, 1 << 20);
     if (dtype == SPMV_F64)
-        k_fill_sliced<double><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.width,
+        k_fill_sliced<double><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g, sl.interleaved,
+                                                   sl.slice_ptr, sl.width,
                                                    sl.len, sl.perm, row_ptr, col_in,
                                                    static_cast<const double *>(val_in), sl.col,
                                                    static_cast<double *>(sl.val));
     else
-        k_fill_sliced<float><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr, sl.width,
+        k_fill_sliced<float><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g, sl.interleaved,
+                                                  sl.slice_ptr, sl.width,
                                                   sl.len, sl.perm, row_ptr, col_in,
                                                   static_cast<const float *>(val_in), sl.col,
                                                   static_cast<float *>(sl.val));
@@ -716,11 +722,13 @@ cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const i
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
     unsigned g = grid_for(sl.n_pos, kBlock, 1 << 20);
     if (dtype == SPMV_F64)
-        k_sliced_to_csr<double><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr,
+        k_sliced_to_csr<double><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g,
+                                                     sl.interleaved, sl.slice_ptr,
                                                      sl.len, sl.perm, sl.col, static_cast<const double *>(sl.val),
                                                      out_ptr, out_col, static_cast<double *>(out_val));
     else
-        k_sliced_to_csr<float><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.slice_ptr,
+        k_sliced_to_csr<float><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g,
+                                                    sl.interleaved, sl.slice_ptr,
                                                     sl.len, sl.perm, sl.col, static_cast<const float *>(sl.val),
                                                     out_ptr, out_col, static_cast<float *>(out_val));
     return cudaGetLastError();

@@ -232,7 +232,9 @@ cudaError_t mm_dispatch(int nv, const Sliced &sl, int64_t n, const Segmented *sg
 
 }  // namespace
 
-bool sell_multi_supported(const Sliced &sl) { return sl.present && sl.log2C < 31 && (sl.C == 32 || sl.C == 64); }
+bool sell_multi_supported(const Sliced &sl) {
+    return sl.present && sl.group == 1 && !sl.interleaved && sl.log2C < 31 && (sl.C == 32 || sl.C == 64);
+}
 
 cudaError_t launch_sell_multi(int dtype, int nv, const Sliced &sl, int64_t n, const Segmented *split, const void *X,
                               int64_t ldx, void *Y, int64_t ldy, cudaStream_t s, const Scale &scale) {

@@ -47,6 +47,10 @@ struct Sliced {
     int64_t stored_entries = 0;  // entries actually held (sum of len)
     int32_t max_width = 0;
     bool keep_x = false;           // gather x with an L2 evict-last policy
+    int32_t group = 1;             // threads per row in the apply (1, 2, 4, ..., 32)
+    int log2g = 0;
+    int group_mode = 0;            // with group > 1: 0 row-grouped, 1 interleaved, 2 column-grouped
+    bool interleaved = false;      // slot layout, see slot_of() (group_mode 1)
     int64_t *slice_ptr = nullptr;  // [n_slices + 1]
     int32_t *width = nullptr;      // [n_slices]
     int32_t *len = nullptr;        // [n_pos] entries stored at each position
@@ -54,6 +58,20 @@ struct Sliced {
     int32_t *col = nullptr;        // [slots]
     void *val = nullptr;           // [slots]
 };
+
+// Slot of entry j of the row held at in-slice position q of a slice starting at
+// `base` (stride = C for SELL, the leading dimension for ELLPACK-R / HYB-ELL).
+// Column-major ("row-grouped"): base + j * stride + q, so entry j of the slice's
+// rows is contiguous.  Interleaved ("column-grouped", for g threads per row): the
+// entries of a row come in groups of g = 2^log2g that sit side by side,
+// base + ((j >> log2g) * stride + q) * g + (j & (g - 1)), so the g threads of a row
+// read g adjacent values and a warp reads 32 consecutive ones.  Slice widths are
+// then whole groups.
+__host__ __device__ inline int64_t slot_of(int64_t base, int64_t q, int64_t j, int64_t stride, int log2g,
+                                           bool interleaved) {
+    return interleaved ? base + ((((j >> log2g) * stride + q) << log2g) | (j & ((int64_t{1} << log2g) - 1)))
+                       : base + j * stride + q;
+}
 
 // Rows handled by the segmented pass: the long rows taken out of a format, or
 // the HYB spill.  kind 1 = compact CSR walked by merge-path, kind 2 = COO,
@@ -194,9 +212,10 @@ cudaError_t launch_sort_keys(const int32_t *len, int64_t n, int64_t sigma, int l
 // len_sorted[p] = len[perm[p]] for p < n, 0 beyond; perm_out[p] = perm[p] or -1.
 cudaError_t launch_gather_sorted(const int32_t *len, const int32_t *perm, int64_t n, int64_t n_pos,
                                  int32_t *len_sorted, int32_t *perm_out, cudaStream_t s);
-// width[s] = max len_sorted over the slice; size[s] = C * width[s].
+// width[s] = max len_sorted over the slice, rounded up to a multiple of round_to;
+// size[s] = C * width[s].
 cudaError_t launch_slice_widths(const int32_t *len_sorted, int64_t n_slices, int32_t C,
-                                int32_t *width, int64_t *size, cudaStream_t s);
+                                int32_t *width, int64_t *size, cudaStream_t s, int32_t round_to = 1);
 // Slot fill from CSR (values of `dtype`), padding slots get column 0 / value 0.
 cudaError_t launch_fill_sliced(int dtype, const Sliced &sl, const int32_t *row_ptr,
                                const int32_t *col_in, const void *val_in, cudaStream_t s);
@@ -247,6 +266,9 @@ cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
 // multi-vector apply on the sliced layout (NV = 2, 4, 8 right-hand sides, row-major X/Y) -- sellmm.cu
 bool sell_multi_supported(const Sliced &sl);
+// G = sl.group threads per row (sellg.cu); long rows (len = -1) are left to launch_rowsplit.
+cudaError_t launch_sellg_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s,
+                               const Scale *scale = nullptr);
 cudaError_t launch_sell_multi(int dtype, int nv, const Sliced &sl, int64_t n, const Segmented *split, const void *X,
                               int64_t ldx, void *Y, int64_t ldy, cudaStream_t s, const Scale &scale);
 // vecops.cu: out[i] = X[i * ldx]; Y[i * ldy] = alpha * t[i] + beta * Y[i * ldy] (Y unread when beta == 0)

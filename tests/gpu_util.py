@@ -72,6 +72,17 @@ FORMAT_CASES = [
     ("hyb", {"K": 3, "spill_csr": 0}),
     ("hyb", {"K": 0}),
     ("merge", {}),
+    # G threads per row: interleaved slots, row-grouped and column-grouped
+    ("sell", {"row_threads": 4}),
+    ("sell", {"row_threads": 8, "row_group_mode": 0}),
+    ("sell", {"row_threads": 4, "row_group_mode": 2}),
+    ("sell", {"C": 64, "sigma": 256, "row_threads": 8, "row_group_mode": 2}),
+    ("ell_r", {"row_threads": 2, "row_group_mode": 2}),
+    ("sell", {"C": 64, "sigma": 1 << 30, "row_threads": 32}),
+    ("sell", {"row_threads": 2, "long_row_threshold": 8}),
+    ("ell_r", {"row_threads": 16}),
+    ("hyb", {"row_threads": 4, "K": 3, "spill_csr": 0}),
+    ("sell", {"row_threads": 1}),
 ]
 
 

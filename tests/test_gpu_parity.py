@@ -16,7 +16,7 @@ from workloads import CSR, laplacian_2d, make_workload, random_csr, integer_x, u
 
 pytestmark = pytest.mark.gpu
 
-SMALL = ["lap2d_small", "lap3d_small", "hmep_small", "powerlaw_small", "uniform16_small"]
+SMALL = ["lap2d_small", "lap3d_small", "hmep_small", "powerlaw_small", "uniform16_small", "band_small"]
 
 _cache = {}
 
@@ -186,6 +186,35 @@ def test_sell_layout_matches_definition(name, C, sigma):
         assert d["padded_entries"] == exp["padded_entries"]
         assert d["slots"] == exp["allocated_slots"]
         assert d["n_long_rows"] == layout.long_rows(lens, thr).size
+
+
+SLOT_CASES = [("sell", 32, 1, 1, 0), ("sell", 64, 256, 1, 0), ("sell", 32, 1, 4, 1), ("sell", 32, 1 << 30, 8, 1),
+              ("sell", 64, 1, 8, 0), ("sell", 32, 4096, 32, 1), ("ell_r", 0, 1, 1, 0), ("ell_r", 0, 1, 4, 1),
+              ("ell_r", 0, 1, 2, 0), ("sell", 32, 1, 4, 2), ("ell_r", 0, 1, 8, 2)]
+
+
+@pytest.mark.parametrize("fmt,C,sigma,g,il", SLOT_CASES, ids=[f"{f}-C{c}-s{s}-g{g}-i{i}" for f, c, s, g, i in SLOT_CASES])
+@pytest.mark.parametrize("name", ["powerlaw_small", "hmep_small", "lap3d_small"])
+def test_slot_arrays_match_definition(name, fmt, C, sigma, g, il):
+    """Every slot of the sliced part (column and value, padding included) against the
+    oracle's layout definition: bit-exact index and byte work."""
+    csr, _, _ = small(name)
+    lens = layout.row_lengths(csr.row_ptr)
+    kw = {"row_threads": g, "row_group_mode": il}
+    if fmt == "sell":
+        kw.update(C=C, sigma=sigma)
+    with build(csr, fmt, **kw) as A:
+        d = A.describe()
+        assert d["row_threads"] == g and d["row_group_mode"] == il
+        exclude = layout.long_rows(lens, d["long_row_threshold"])
+        if fmt == "sell":
+            exp = layout.sell_slots(csr, C, min(sigma, csr.n), exclude=exclude, group=g, interleaved=il == 1)
+        else:
+            exp = layout.sell_slots(csr, 0, 1, exclude=exclude, group=g, interleaved=il == 1, ell_ld=d["ld"])
+        col, val = A.slots()
+        assert col.numel() == exp[0].size == d["slots"]
+        assert np.array_equal(col.cpu().numpy(), exp[0])
+        assert np.array_equal(val.cpu().numpy().view(np.uint8), exp[1].view(np.uint8))
 
 
 @pytest.mark.parametrize("N,b_r", [(1024, 32), (4096, 32), (4096, 64), (777, 64)])

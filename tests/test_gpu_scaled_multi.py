@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 SCALES = [(-1.0, 1.0), (2.5, -0.5), (0.0, 3.0), (-3.0, 0.0)]
 MULTI_FORMATS = [("auto", {}), ("sell", {"C": 64, "sigma": 256}), ("sell", {"C": 32, "sigma": 1 << 30}),
-                 ("ell_r", {}), ("hyb", {}), ("merge", {}), ("csr_vector", {})]
+                 ("ell_r", {}), ("hyb", {}), ("merge", {}), ("csr_vector", {}), ("sell", {"row_threads": 4})]
 
 _cache = {}
 

@@ -86,3 +86,15 @@ def test_random_csr_options():
     A = random_csr(50, 0.3, seed=1, duplicates=True, unsorted=True, empty_row_fraction=0.2, full_rows=2)
     lens = A.row_lengths()
     assert (lens == 50).sum() >= 2 and (lens == 0).sum() >= 1
+
+
+def test_banded_rows_shape():
+    from workloads import banded_random_rows
+    csr = banded_random_rows(5000, per_row=40, half_band=100, seed=3)
+    lens = np.diff(csr.row_ptr)
+    assert (lens == 40).all()
+    rows = np.repeat(np.arange(csr.n), lens)
+    assert (np.abs(csr.col_idx.astype(np.int64) - rows) <= 100).all()
+    c = csr.col_idx.reshape(csr.n, 40)
+    assert (np.diff(c, axis=1) > 0).all()  # distinct and sorted inside each row
+    assert (np.abs(csr.vals) <= 1).all()

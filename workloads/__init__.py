@@ -11,6 +11,7 @@ from .generators import (  # noqa: F401
     hmep_like,
     power_law,
     random_uniform_rows,
+    banded_random_rows,
     random_csr,
     identity,
     permutation_matrix,

@@ -290,6 +290,31 @@ def random_uniform_rows(n: int = 16_777_216, per_row: int = 16, seed: int = 5, d
     return CSR(n, row_ptr, cols.reshape(-1), vals, f"uniform{per_row}_{n}")
 
 
+def banded_random_rows(n: int, per_row: int, half_band: int, seed: int = 6, dtype=np.float64) -> CSR:
+    """Exactly ``per_row`` distinct, sorted columns per row, uniform in the band
+    [i - half_band, i + half_band] clipped to [0, n); values U(-1, 1).  Wide rows with a
+    local x footprint: the shape for which several threads share a row."""
+    rng = np.random.default_rng(seed)
+    rows = np.arange(n, dtype=np.int64)
+    lo = np.maximum(rows - half_band, 0)
+    hi = np.minimum(rows + half_band, n - 1)
+    per_row = int(min(per_row, int((hi - lo + 1).min())))
+    span = (hi - lo + 1)[:, None]
+    cols = lo[:, None] + (rng.random((n, per_row)) * span).astype(np.int64)
+    cols.sort(axis=1)
+    bad = np.nonzero((cols[:, 1:] == cols[:, :-1]).any(axis=1))[0]
+    while bad.size:
+        redo = lo[bad, None] + (rng.random((bad.size, per_row)) * span[bad]).astype(np.int64)
+        redo.sort(axis=1)
+        cols[bad] = redo
+        bad = bad[(redo[:, 1:] == redo[:, :-1]).any(axis=1)]
+    nnz = n * per_row
+    _check_index_range(n, nnz)
+    row_ptr = (np.arange(n + 1, dtype=np.int64) * per_row).astype(np.int32)
+    vals = (rng.random(nnz) * 2.0 - 1.0).astype(dtype)
+    return CSR(n, row_ptr, cols.reshape(-1).astype(np.int32), vals, f"band{per_row}_{n}")
+
+
 # --------------------------------------------------------------------------- #
 # tiny matrices for pins
 # --------------------------------------------------------------------------- #
@@ -383,6 +408,13 @@ WORKLOADS = {
     "uniform16_16m": dict(fn=random_uniform_rows, kw=dict(n=16_777_216, per_row=16, seed=5),
                           dtype=np.float32, seed_x=101,
                           desc="random uniform, 16 nnz/row, n=16,777,216"),
+    # wide rows, few of them: the regime of several threads per row
+    "band120_256k": dict(fn=banded_random_rows, kw=dict(n=262_144, per_row=120, half_band=4096, seed=6),
+                         dtype=np.float64, seed_x=101,
+                         desc="banded random, 120 nnz/row in a band of +-4096, n=262,144"),
+    "band128_32k": dict(fn=banded_random_rows, kw=dict(n=32_768, per_row=128, half_band=2048, seed=7),
+                        dtype=np.float64, seed_x=101,
+                        desc="banded random, 128 nnz/row in a band of +-2048, n=32,768"),
     # small versions of the same shapes (several tiles and a ragged tail)
     "lap2d_small": dict(fn=laplacian_2d, kw=dict(nx=67, ny=45), dtype=np.float64, seed_x=101,
                         desc="2D 5-point Laplacian 67x45"),
@@ -393,6 +425,8 @@ WORKLOADS = {
     "powerlaw_small": dict(fn=power_law, kw=dict(n=60_001, zipf_max=3000, n_dense=4, dense_lo=9000,
                                                  dense_hi=40000, seed=4),
                            dtype=np.float64, seed_x=101, desc="power law, n=60,001 with 4 dense rows"),
+    "band_small": dict(fn=banded_random_rows, kw=dict(n=20_011, per_row=96, half_band=700, seed=8),
+                       dtype=np.float64, seed_x=101, desc="banded random 96/row, n=20,011"),
     "uniform16_small": dict(fn=random_uniform_rows, kw=dict(n=100_003, per_row=16, seed=5),
                             dtype=np.float32, seed_x=101, desc="random uniform 16/row, n=100,003"),
 }
