@@ -567,6 +567,50 @@ def run_cg(args):
         A.close()
 
 
+def run_orderings(args):
+    """The matrix in its given numbering and in the permuted bases (row length, reverse
+    Cuthill-McKee): build time (ordering included) and time per apply, one JSON line each."""
+    import torch
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+    from workloads import make_workload
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = load_peaks()
+    csr, x_np = make_workload(args.workload)
+    sv = csr.vals.dtype.itemsize
+    beff = effective_bytes(csr.n, csr.nnz, sv)
+    dev = torch.device("cuda", 0)
+    rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
+    x = torch.from_numpy(x_np).to(dev)
+    for ordering in (None, "row_length", "rcm"):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=args.format, ordering=ordering)
+        build_ms = (time.perf_counter() - t0) * 1e3
+        xp = A.to_basis(x)
+        yp = torch.empty_like(xp)
+        apply_c = spmv._abi.lib.spmv_apply
+        call = (A._h, xp.data_ptr(), yp.data_ptr(), None)
+        for _ in range(args.warmup):
+            apply_c(*call)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = max(args.steps // 100, 20)
+        e0.record()
+        for _ in range(steps):
+            apply_c(*call)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        d = A.describe()
+        print(json.dumps({"workload": args.workload, "ordering": ordering or "given", "format": d["format"],
+                          "kernels": d["kernels"], "build_ms": build_ms, "us_per_apply": ms * 1e3,
+                          "effective_gbs": beff / ms / 1e6, "frac": beff / ms / 1e6 / peak,
+                          "peak": f"{peak} GB/s {peak_kind}", "slots_per_nnz": d["slots"] / max(csr.nnz, 1)}),
+              flush=True)
+        A.close()
+
+
 def run_sweep(args):
     """One JSON line per storage format on the chosen workload (format comparison)."""
     import numpy as np
@@ -629,6 +673,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
     ap.add_argument("--nrhs", type=int, default=0,
                     help="with --sweep: time the multi-vector apply with this many right-hand sides instead")
+    ap.add_argument("--orderings", action="store_true",
+                    help="time the workload in its given numbering and in the row-length / RCM permuted bases")
     ap.add_argument("--cg", type=int, default=0, metavar="ITERS",
                     help="time conjugate gradients (ITERS fixed steps per run) instead of the bench line")
     args = ap.parse_args(argv)
@@ -637,6 +683,8 @@ def main(argv=None):
         run_reference(args)
     elif args.cg > 0:
         run_cg(args)
+    elif args.orderings:
+        run_orderings(args)
     elif args.sweep and args.nrhs > 0:
         run_multi(args)
     elif args.sweep:

@@ -239,6 +239,57 @@ SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const vo
 SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double rtol, int32_t max_iter, void *stream,
                      int32_t *iterations, double *relative_residual);
 
+/*
+ * Orderings of the permuted basis (spmv_build_permuted).  perm maps a position of the
+ * basis to an original index (new -> old).
+ *   NATURAL     the identity.
+ *   ROW_LENGTH  rows by length, longest first, ties in index order: the sort of the
+ *               GPGPU spMVM paper's pJDS format, over the whole matrix.
+ *   RCM         reverse Cuthill-McKee on the graph of A + A^T (an edge for every stored
+ *               entry off the diagonal): vertices of degree 0 first in index order, each
+ *               component started at its unvisited vertex of least (degree, index),
+ *               neighbours appended by (degree, index), the whole order reversed.  It
+ *               brings entries next to the diagonal, so the gathers of x stay within a
+ *               narrow window.  Build cost grows with the number of breadth-first levels
+ *               and of connected components (each is a few kernel launches).
+ *   USER        the caller's permutation.
+ */
+typedef enum {
+    SPMV_ORDER_NATURAL = 0,
+    SPMV_ORDER_ROW_LENGTH = 1,
+    SPMV_ORDER_RCM = 2,
+    SPMV_ORDER_USER = 3
+} spmv_ordering;
+
+/*
+ * Build a handle for the matrix in a permuted basis, B = P A P^T: row and column i of
+ * B are row and column perm[i] of A.  The GPGPU spMVM paper (pJDS section) notes that a
+ * Krylov solver needs the permutation only before the first and after the last
+ * iteration, all products in between running on permuted vectors; this is that mode.
+ * Every apply, scaled apply, multi-vector apply and spmv_cg of the handle works in the
+ * permuted basis (x and y are permuted vectors); spmv_permute_vector moves vectors in
+ * and out, spmv_get_permutation returns perm, spmv_to_csr returns B.
+ *   n .. format, params, stream  as spmv_build_from_csr_ex (A is validated first).
+ *   ordering   spmv_ordering; perm (ordering USER only): device int32[n], a permutation
+ *              of 0..n-1 (checked: SPMV_ERR_INVALID_ARG otherwise).
+ * The ordering and B are computed on the device.  Returns NULL on error.
+ */
+SPMV_API spmv_handle_t spmv_build_permuted(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
+                                           const void *vals, int dtype, int format,
+                                           const spmv_format_params *params, int ordering, const int32_t *perm,
+                                           void *stream);
+
+/* perm (device int32[n]) = the handle's basis order, new -> old (the identity for a
+ * handle built by spmv_build_from_csr).  Synchronises `stream`. */
+SPMV_API int spmv_get_permutation(spmv_handle_t h, int32_t *perm, void *stream);
+
+/*
+ * Move a vector between the original basis and the handle's: direction 0 (into the
+ * basis) dst[i] = src[perm[i]]; direction 1 (back) dst[perm[i]] = src[i].  src and dst
+ * are device arrays of n values of the handle's type and must not alias.  Asynchronous.
+ */
+SPMV_API int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int direction, void *stream);
+
 /* Release every device buffer of the handle.  NULL is accepted and ignored. */
 SPMV_API void spmv_destroy(spmv_handle_t h);
 

@@ -13,6 +13,7 @@ from __future__ import annotations
 from . import _abi
 from ._abi import (  # noqa: F401
     FORMATS,
+    ORDERINGS,
     SpmvError,
     spmv_apply,
     spmv_apply_ex,
@@ -28,13 +29,16 @@ from ._abi import (  # noqa: F401
     spmv_destroy,
     spmv_error_string,
     spmv_get_layout,
+    spmv_get_permutation,
+    spmv_build_permuted,
+    spmv_permute_vector,
     spmv_get_slots,
     spmv_last_error,
     spmv_last_error_message,
     spmv_to_csr,
 )
 
-__all__ = ["SpmvMatrix", "SpmvError", "FORMATS"] + [n for n in _abi.EXPORTS]
+__all__ = ["SpmvMatrix", "SpmvError", "FORMATS", "ORDERINGS"] + [n for n in _abi.EXPORTS]
 
 
 class SpmvMatrix:
@@ -47,10 +51,14 @@ class SpmvMatrix:
         self.dtype = dtype
 
     @classmethod
-    def from_csr(cls, row_ptr, col_idx, vals, format: str = "auto", stream=None, **params) -> "SpmvMatrix":
+    def from_csr(cls, row_ptr, col_idx, vals, format: str = "auto", stream=None, ordering=None,
+                 **params) -> "SpmvMatrix":
         """Build from device CSR tensors (int32 row_ptr/col_idx, float64/float32 vals).
 
-        ``params``: C, sigma, K, spill_csr, long_row_threshold, subwarp (see spmv.h).
+        ``params``: C, sigma, K, spill_csr, long_row_threshold, subwarp, row_threads,
+        row_group_mode (see spmv.h).  ``ordering`` ("natural", "row_length", "rcm", or an
+        int32 CUDA tensor holding a permutation): build B = P A P^T and work in that
+        permuted basis (see ``to_basis`` / ``from_basis``).
         """
         import torch
 
@@ -64,7 +72,15 @@ class SpmvMatrix:
         if vals.numel() != nnz:
             raise ValueError("vals and col_idx differ in length")
         code = _abi.dtype_code(vals.dtype)
-        h = spmv_build_from_csr_ex(n, nnz, row_ptr, col_idx, vals, code, format, params, stream)
+        if ordering is None:
+            h = spmv_build_from_csr_ex(n, nnz, row_ptr, col_idx, vals, code, format, params, stream)
+        elif isinstance(ordering, torch.Tensor):
+            if not (ordering.is_cuda and ordering.dtype == torch.int32 and ordering.numel() == n):
+                raise TypeError("a user ordering must be an int32 CUDA tensor of n entries")
+            h = spmv_build_permuted(n, nnz, row_ptr, col_idx, vals, code, format, params, "user",
+                                    ordering.contiguous(), stream)
+        else:
+            h = spmv_build_permuted(n, nnz, row_ptr, col_idx, vals, code, format, params, ordering, None, stream)
         return cls(h, n, nnz, vals.dtype)
 
     def _check_vec(self, v, name):
@@ -160,6 +176,32 @@ class SpmvMatrix:
         sp = torch.empty(d["n_slices"] + 1, dtype=torch.int64, device=dev)
         spmv_get_layout(self._h, perm, sp)
         return perm, sp
+
+    def permutation(self):
+        """The basis order as an int32 CUDA tensor (position -> original index)."""
+        import torch
+
+        perm = torch.empty(self.n, dtype=torch.int32, device=torch.device("cuda", torch.cuda.current_device()))
+        spmv_get_permutation(self._h, perm)
+        return perm
+
+    def to_basis(self, v, out=None, stream=None):
+        """A vector of the original basis in the handle's basis: out[i] = v[perm[i]]."""
+        import torch
+
+        self._check_vec(v, "v")
+        out = torch.empty_like(v) if out is None else out
+        spmv_permute_vector(self._h, v, out, 0, stream)
+        return out
+
+    def from_basis(self, v, out=None, stream=None):
+        """A vector of the handle's basis back in the original one: out[perm[i]] = v[i]."""
+        import torch
+
+        self._check_vec(v, "v")
+        out = torch.empty_like(v) if out is None else out
+        spmv_permute_vector(self._h, v, out, 1, stream)
+        return out
 
     def slots(self):
         """(col, val): the sliced part's slot arrays as CUDA tensors."""

@@ -27,7 +27,11 @@ EXPORTS = (
     "spmv_apply_host", "spmv_apply_profiled", "spmv_destroy", "spmv_last_error",
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
     "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
+    "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector",
 )
+
+#: spmv_ordering codes
+ORDERINGS = {"natural": 0, "row_length": 1, "rcm": 2, "user": 3}
 
 
 class SpmvError(RuntimeError):
@@ -93,6 +97,13 @@ def _load():
     lib.spmv_apply_multi.restype = c_int
     lib.spmv_cg.argtypes = [vp, vp, vp, f64, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(f64)]
     lib.spmv_cg.restype = c_int
+    lib.spmv_build_permuted.argtypes = [i64, i64, vp, vp, vp, c_int, c_int, ctypes.POINTER(FormatParams), c_int, vp,
+                                        vp]
+    lib.spmv_build_permuted.restype = vp
+    lib.spmv_get_permutation.argtypes = [vp, vp, vp]
+    lib.spmv_get_permutation.restype = c_int
+    lib.spmv_permute_vector.argtypes = [vp, vp, vp, c_int, vp]
+    lib.spmv_permute_vector.restype = c_int
     del i32
     return lib
 
@@ -183,6 +194,26 @@ def spmv_build_from_csr_ex(n, nnz, row_ptr, col_idx, vals, dtype, fmt, params=No
     if not h:
         _raise_last()
     return h
+
+
+def spmv_build_permuted(n, nnz, row_ptr, col_idx, vals, dtype, fmt, params=None, ordering="rcm", perm=None,
+                        stream=None) -> int:
+    """Handle for B = P A P^T in the given ordering (see spmv.h)."""
+    p = params if isinstance(params, FormatParams) else make_params(**(params or {}))
+    h = lib.spmv_build_permuted(int(n), int(nnz), _ptr(row_ptr), _ptr(col_idx), _ptr(vals), int(dtype),
+                                int(FORMATS.get(fmt, fmt)), ctypes.byref(p), int(ORDERINGS.get(ordering, ordering)),
+                                _ptr(perm), _stream(stream))
+    if not h:
+        _raise_last()
+    return h
+
+
+def spmv_get_permutation(h, perm, stream=None) -> None:
+    _check(lib.spmv_get_permutation(h, _ptr(perm), _stream(stream)))
+
+
+def spmv_permute_vector(h, src, dst, direction, stream=None) -> None:
+    _check(lib.spmv_permute_vector(h, _ptr(src), _ptr(dst), int(direction), _stream(stream)))
 
 
 def spmv_apply(h, x, y, stream=None) -> None:

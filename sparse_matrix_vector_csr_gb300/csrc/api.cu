@@ -116,6 +116,16 @@ int check_fits(double bytes, const char *what) {
     return SPMV_OK;
 }
 
+const char *ordering_name(int o) {
+    switch (o) {
+        case SPMV_ORDER_NATURAL: return "natural";
+        case SPMV_ORDER_ROW_LENGTH: return "row_length";
+        case SPMV_ORDER_RCM: return "rcm";
+        case SPMV_ORDER_USER: return "user";
+        default: return "?";
+    }
+}
+
 const char *format_name(int f) {
     switch (f) {
         case SPMV_FMT_AUTO: return "auto";
@@ -941,6 +951,95 @@ spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int32_t *row_
     return build_impl(n, nnz, row_ptr, col_idx, vals, dtype, format, params, static_cast<cudaStream_t>(stream));
 }
 
+spmv_handle_t spmv_build_permuted(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
+                                  const void *vals, int dtype, int format, const spmv_format_params *params,
+                                  int ordering, const int32_t *perm, void *stream) {
+    clear_error();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto fail = [](int status, const std::string &msg) -> spmv_handle_t {
+        set_error(status, msg);
+        return nullptr;
+    };
+    if (n < 0 || nnz < 0 || n >= (int64_t(1) << 31) || nnz >= (int64_t(1) << 31))
+        return fail(SPMV_ERR_INVALID_ARG, "n and nnz must lie in [0, 2^31)");
+    if (dtype != SPMV_F64 && dtype != SPMV_F32) return fail(SPMV_ERR_INVALID_ARG, "dtype must be SPMV_F64 or SPMV_F32");
+    if (ordering < SPMV_ORDER_NATURAL || ordering > SPMV_ORDER_USER) return fail(SPMV_ERR_INVALID_ARG, "unknown ordering");
+    if (!row_ptr || (nnz > 0 && (!col_idx || !vals))) return fail(SPMV_ERR_INVALID_ARG, "NULL matrix array");
+    if (ordering == SPMV_ORDER_USER && n > 0 && !perm) return fail(SPMV_ERR_INVALID_ARG, "ordering USER needs perm");
+    if (check_device_pointer(row_ptr, "row_ptr") != SPMV_OK) return nullptr;
+    if (nnz > 0 && (check_device_pointer(col_idx, "col_idx") != SPMV_OK ||
+                    check_device_pointer(vals, "vals") != SPMV_OK))
+        return nullptr;
+    if (ordering == SPMV_ORDER_USER && n > 0 && check_device_pointer(perm, "perm") != SPMV_OK) return nullptr;
+    const size_t vb = value_bytes(dtype);
+    Temp temp;
+    int32_t *len = nullptr, *status = nullptr, *order = nullptr, *b_ptr = nullptr, *b_col = nullptr;
+    void *b_val = nullptr;
+    if (temp.get(&len, n) || temp.get(&status, 3) || temp.get(&order, n) || temp.get(&b_ptr, n + 1) ||
+        temp.get(&b_col, nnz) || temp.get(reinterpret_cast<char **>(&b_val), nnz * static_cast<int64_t>(vb)))
+        return nullptr;
+    // A must be valid before any ordering kernel indexes through it
+    int32_t st[3] = {0, 0, 0};
+    if (cudaMemsetAsync(status, 0, sizeof(st), s) != cudaSuccess ||
+        launch_validate(n, nnz, row_ptr, col_idx, len, status, s) != cudaSuccess ||
+        cudaMemcpyAsync(st, status, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        set_cuda_error(cudaGetLastError(), "validating the CSR");
+        return nullptr;
+    }
+    if (st[0]) return fail(SPMV_ERR_BAD_CSR, "row_ptr is not a valid CSR row pointer");
+    if (st[1]) return fail(SPMV_ERR_BAD_CSR, "a column index lies outside [0, n)");
+    if (compute_ordering(ordering, n, nnz, row_ptr, col_idx, st[2], perm, order, s) != SPMV_OK) return nullptr;
+    if (permute_csr(dtype, n, nnz, row_ptr, col_idx, vals, order, b_ptr, b_col, b_val, s) != SPMV_OK) return nullptr;
+    spmv_handle_t h = build_impl(n, nnz, b_ptr, b_col, b_val, dtype, format, params, s);
+    if (!h) return nullptr;
+    h->ordering = ordering;
+    if (n > 0) {
+        if (dev_alloc_n(h, &h->basis_perm, n) != SPMV_OK ||
+            cudaMemcpyAsync(h->basis_perm, order, sizeof(int32_t) * n, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            if (spmv_last_error() == SPMV_OK) set_cuda_error(cudaGetLastError(), "storing the permutation");
+            free_handle(h);
+            return nullptr;
+        }
+    }
+    return h;
+}
+
+int spmv_get_permutation(spmv_handle_t h, int32_t *perm, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (h->n == 0) return SPMV_OK;
+    if (!perm) return set_error(SPMV_ERR_INVALID_ARG, "NULL perm");
+    SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_device_pointer(perm, "perm"));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->basis_perm) {
+        SPMV_TRY_CUDA(cudaMemcpyAsync(perm, h->basis_perm, sizeof(int32_t) * h->n, cudaMemcpyDeviceToDevice, s));
+    } else {
+        std::vector<int32_t> iota(static_cast<size_t>(h->n));
+        for (int64_t i = 0; i < h->n; ++i) iota[i] = static_cast<int32_t>(i);
+        SPMV_TRY_CUDA(cudaMemcpyAsync(perm, iota.data(), sizeof(int32_t) * h->n, cudaMemcpyHostToDevice, s));
+    }
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
+int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int direction, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (direction != 0 && direction != 1) return set_error(SPMV_ERR_INVALID_ARG, "direction must be 0 or 1");
+    if (h->n == 0) return SPMV_OK;
+    if (!src || !dst) return set_error(SPMV_ERR_INVALID_ARG, "NULL src or dst");
+    if (src == dst) return set_error(SPMV_ERR_INVALID_ARG, "src and dst must not alias");
+    SPMV_TRY(check_current_device(h));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!h->basis_perm) {
+        SPMV_TRY_CUDA(cudaMemcpyAsync(dst, src, value_bytes(h->dtype) * h->n, cudaMemcpyDeviceToDevice, s));
+        return SPMV_OK;
+    }
+    SPMV_TRY_CUDA(launch_permute_vector(h->dtype, h->n, h->basis_perm, src, dst, direction, s));
+    return SPMV_OK;
+}
+
 int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream) {
     if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
     if (h->n == 0) return SPMV_OK;
@@ -1141,6 +1240,8 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
            sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,
            (long long)sl.stored_entries, (long long)sl.ld, sl.max_width, sl.perm ? "true" : "false");
     append(o, "\"x_evict_last\":%s,", sl.keep_x ? "true" : "false");
+    append(o, "\"ordering\":\"%s\",\"permuted_basis\":%s,", ordering_name(h->ordering),
+           h->basis_perm ? "true" : "false");
     append(o, "\"n_long_rows\":%lld,\"long_nnz\":%lld,", (long long)h->n_long_rows, (long long)h->long_nnz);
     append(o, "\"segment\":\"%s\",\"segment_rows\":%lld,\"segment_nnz\":%lld,\"segment_ctas\":%lld,",
            sg.kind == 0 ? "none" : sg.kind == 1 ? "csr_merge_path" : sg.kind == 2 ? "coo" : "row_split",

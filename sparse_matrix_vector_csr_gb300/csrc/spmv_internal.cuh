@@ -143,6 +143,10 @@ struct spmv_handle_s {
     void *tmp_x = nullptr;
     void *tmp_y = nullptr;
 
+    // permuted basis (spmv_build_permuted): position -> original index; nullptr = identity
+    int32_t *basis_perm = nullptr;
+    int ordering = SPMV_ORDER_NATURAL;
+
     std::vector<std::string> kernels;  // launch sequence of one apply
     std::vector<void *> allocations;
 };
@@ -266,6 +270,17 @@ cudaError_t launch_segmented(int dtype, const Segmented &sg, const void *x, void
 cudaError_t launch_carry_fixup(int dtype, const Segmented &sg, void *y, cudaStream_t s);
 // multi-vector apply on the sliced layout (NV = 2, 4, 8 right-hand sides, row-major X/Y) -- sellmm.cu
 bool sell_multi_supported(const Sliced &sl);
+// Orderings of the permuted basis (order.cu).  compute_ordering fills perm (new -> old)
+// for an already validated CSR (max_len = its longest row); permute_csr writes
+// B = P A P^T (row i of B = row perm[i] of A, columns renamed through the inverse).
+int compute_ordering(int ordering, int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col,
+                     int32_t max_len, const int32_t *user_perm, int32_t *perm, cudaStream_t s);
+int permute_csr(int dtype, int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col, const void *val,
+                const int32_t *perm, int32_t *out_ptr, int32_t *out_col, void *out_val, cudaStream_t s);
+// direction 0: dst[i] = src[perm[i]]; 1: dst[perm[i]] = src[i]
+cudaError_t launch_permute_vector(int dtype, int64_t n, const int32_t *perm, const void *src, void *dst,
+                                  int direction, cudaStream_t s);
+
 // G = sl.group threads per row (sellg.cu); long rows (len = -1) are left to launch_rowsplit.
 cudaError_t launch_sellg_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s,
                                const Scale *scale = nullptr);

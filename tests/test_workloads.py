@@ -98,3 +98,17 @@ def test_banded_rows_shape():
     c = csr.col_idx.reshape(csr.n, 40)
     assert (np.diff(c, axis=1) > 0).all()  # distinct and sorted inside each row
     assert (np.abs(csr.vals) <= 1).all()
+
+
+def test_relabelled_laplacian_is_the_same_operator():
+    from workloads import laplacian_3d_relabelled
+    A = laplacian_3d(7, 5, 4)
+    B = laplacian_3d_relabelled(7, 5, 4, seed=1)
+    lab = B.meta["labels"]
+    DA = np.zeros((A.n, A.n))
+    DB = np.zeros((A.n, A.n))
+    for r in range(A.n):
+        DA[r, A.col_idx[A.row_ptr[r]:A.row_ptr[r + 1]]] = A.vals[A.row_ptr[r]:A.row_ptr[r + 1]]
+        DB[r, B.col_idx[B.row_ptr[r]:B.row_ptr[r + 1]]] = B.vals[B.row_ptr[r]:B.row_ptr[r + 1]]
+    assert np.array_equal(DB[np.ix_(lab, lab)], DA)  # point p of A is label lab[p] of B
+    assert (np.diff(B.col_idx.reshape(-1)[:7]) != 0).all()

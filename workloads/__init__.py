@@ -8,6 +8,7 @@ from .generators import (  # noqa: F401
     laplacian_1d,
     laplacian_2d,
     laplacian_3d,
+    laplacian_3d_relabelled,
     hmep_like,
     power_law,
     random_uniform_rows,

@@ -125,6 +125,35 @@ def laplacian_3d(nx: int, ny: int, nz: int, dtype=np.float64) -> CSR:
     return _csr_from_mask(n, cols, mask, vals, dtype, f"lap3d_{nx}x{ny}x{nz}", {"grid": (nx, ny, nz)})
 
 
+def laplacian_3d_relabelled(nx: int, ny: int, nz: int, seed: int = 9, dtype=np.float64) -> CSR:
+    """The 7-point Dirichlet Laplacian with its grid points numbered in a seeded random
+    order: grid point p gets the label lab[p] (a random bijection), its row is lab[p],
+    and its neighbours q appear as columns lab[q].  Columns sorted ascending.  The same
+    operator as ``laplacian_3d`` with its locality destroyed: the input for which a
+    bandwidth-reducing ordering matters."""
+    n = nx * ny * nz
+    lab = np.random.default_rng(seed).permutation(n).astype(np.int64)
+    idx = np.arange(n, dtype=np.int64)
+    i = idx % nx
+    j = (idx // nx) % ny
+    k = idx // (nx * ny)
+    offs = np.array([-nx * ny, -nx, -1, 0, 1, nx, nx * ny], dtype=np.int64)
+    nb = idx[:, None] + offs[None, :]
+    mask = np.stack([k > 0, j > 0, i > 0, np.ones(n, bool), i < nx - 1, j < ny - 1, k < nz - 1], axis=1)
+    val_row = np.array([-1.0, -1.0, -1.0, 6.0, -1.0, -1.0, -1.0])
+    rows = np.broadcast_to(lab[:, None], nb.shape)[mask]
+    cols = lab[np.where(mask, nb, 0)][mask]
+    vals = np.broadcast_to(val_row[None, :], nb.shape)[mask]
+    order = np.lexsort((cols, rows))
+    rows, cols, vals = rows[order], cols[order], vals[order]
+    row_ptr = np.zeros(n + 1, dtype=np.int64)
+    np.add.at(row_ptr, rows + 1, 1)
+    row_ptr = np.cumsum(row_ptr)
+    _check_index_range(n, int(row_ptr[-1]))
+    return CSR(n, row_ptr.astype(np.int32), cols.astype(np.int32), vals.astype(dtype),
+               f"lap3d_{nx}x{ny}x{nz}_relabelled", {"grid": (nx, ny, nz), "labels": lab})
+
+
 # --------------------------------------------------------------------------- #
 # HMEp-shaped
 # --------------------------------------------------------------------------- #
@@ -409,6 +438,9 @@ WORKLOADS = {
                           dtype=np.float32, seed_x=101,
                           desc="random uniform, 16 nnz/row, n=16,777,216"),
     # wide rows, few of them: the regime of several threads per row
+    "lap3d_128_relabelled": dict(fn=laplacian_3d_relabelled, kw=dict(nx=128, ny=128, nz=128, seed=9),
+                                 dtype=np.float64, seed_x=101,
+                                 desc="3D 7-point Laplacian 128^3 with randomly numbered grid points"),
     "band120_256k": dict(fn=banded_random_rows, kw=dict(n=262_144, per_row=120, half_band=4096, seed=6),
                          dtype=np.float64, seed_x=101,
                          desc="banded random, 120 nnz/row in a band of +-4096, n=262,144"),
@@ -425,6 +457,8 @@ WORKLOADS = {
     "powerlaw_small": dict(fn=power_law, kw=dict(n=60_001, zipf_max=3000, n_dense=4, dense_lo=9000,
                                                  dense_hi=40000, seed=4),
                            dtype=np.float64, seed_x=101, desc="power law, n=60,001 with 4 dense rows"),
+    "lap3d_relabelled_small": dict(fn=laplacian_3d_relabelled, kw=dict(nx=37, ny=29, nz=23, seed=9),
+                                   dtype=np.float64, seed_x=101, desc="3D Laplacian 37x29x23, random numbering"),
     "band_small": dict(fn=banded_random_rows, kw=dict(n=20_011, per_row=96, half_band=700, seed=8),
                        dtype=np.float64, seed_x=101, desc="banded random 96/row, n=20,011"),
     "uniform16_small": dict(fn=random_uniform_rows, kw=dict(n=100_003, per_row=16, seed=5),
