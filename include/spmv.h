@@ -173,12 +173,25 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
 SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
 
 /*
- * y_host = A x_host with host arrays: copies x to the device, applies, copies y
- * back and waits for the stream.  Page-locked (pinned) host buffers give the full
- * copy bandwidth.  The device staging buffers are allocated by the first call on
- * a handle and kept until spmv_destroy.
+ * y_host = A x_host with host arrays: copies x to the device, applies, moves y back
+ * and waits for the stream.  Page-locked (pinned) host buffers give the full copy
+ * bandwidth.  When y_host is page-locked and the handle's plan writes each row of y
+ * once (SELL / ELLPACK-R without a separate accumulating pass), the kernels store y
+ * straight into it, so the transfer back overlaps the product; otherwise y is staged
+ * and copied.  The device staging buffers are allocated by the first call on a handle
+ * and kept until spmv_destroy.
  */
 SPMV_API int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *stream);
+
+/*
+ * y_host = A x_host with page-locked host arrays (cudaHostAlloc, or cudaHostRegister'ed)
+ * read and written by the kernels themselves through their device mapping: no staging
+ * copy.  On a GPU attached to its CPU by a coherent link (Grace + Blackwell over
+ * NVLink-C2C) the gathers of x and the stores of y cross the link while the matrix
+ * streams from HBM, instead of two copy-engine transfers around the product.  Waits
+ * for the stream.  SPMV_ERR_INVALID_ARG if either array is not page-locked host memory.
+ */
+SPMV_API int spmv_apply_mapped(spmv_handle_t h, const void *x_host, void *y_host, void *stream);
 
 /*
  * As spmv_apply, but records CUDA events around each kernel it launches, waits for

@@ -18,6 +18,7 @@ from ._abi import (  # noqa: F401
     spmv_apply,
     spmv_apply_ex,
     spmv_apply_host,
+    spmv_apply_mapped,
     spmv_apply_multi,
     spmv_apply_profiled,
     spmv_build_from_csr,
@@ -146,6 +147,19 @@ class SpmvMatrix:
         if y_host is None:
             y_host = np.empty_like(x_host)
         spmv_apply_host(self._h, x_host, y_host)
+        return y_host
+
+    def apply_mapped(self, x_host, y_host=None):
+        """y = A x for page-locked host tensors (``tensor.pin_memory()``), read and written
+        by the kernels through their device mapping, with no staging copies."""
+        import torch
+
+        for name, t in (("x_host", x_host), ("y_host", y_host)):
+            if t is not None and not (isinstance(t, torch.Tensor) and t.is_pinned() and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous page-locked host tensor")
+        if y_host is None:
+            y_host = torch.empty_like(x_host).pin_memory()
+        spmv_apply_mapped(self._h, x_host, y_host)
         return y_host
 
     def apply_profiled(self, x, y, stream=None):

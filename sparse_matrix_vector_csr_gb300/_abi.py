@@ -27,7 +27,7 @@ EXPORTS = (
     "spmv_apply_host", "spmv_apply_profiled", "spmv_destroy", "spmv_last_error",
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
     "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
-    "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector",
+    "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector", "spmv_apply_mapped",
 )
 
 #: spmv_ordering codes
@@ -70,6 +70,8 @@ def _load():
     lib.spmv_apply.restype = c_int
     lib.spmv_apply_host.argtypes = [vp, vp, vp, vp]
     lib.spmv_apply_host.restype = c_int
+    lib.spmv_apply_mapped.argtypes = [vp, vp, vp, vp]
+    lib.spmv_apply_mapped.restype = c_int
     lib.spmv_apply_profiled.argtypes = [vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), c_int]
     lib.spmv_apply_profiled.restype = c_int
     lib.spmv_destroy.argtypes = [vp]
@@ -222,6 +224,11 @@ def spmv_apply(h, x, y, stream=None) -> None:
 
 def spmv_apply_host(h, x_host, y_host, stream=None) -> None:
     _check(lib.spmv_apply_host(h, _ptr(x_host), _ptr(y_host), _stream(stream)))
+
+
+def spmv_apply_mapped(h, x_host, y_host, stream=None) -> None:
+    """y_host = A x_host, the kernels reading and writing page-locked host arrays directly."""
+    _check(lib.spmv_apply_mapped(h, _ptr(x_host), _ptr(y_host), _stream(stream)))
 
 
 def spmv_apply_profiled(h, x, y, stream=None, cap: int = 16) -> list:

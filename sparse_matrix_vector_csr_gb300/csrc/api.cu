@@ -1055,11 +1055,51 @@ int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *str
     SPMV_TRY(check_current_device(h));
     const size_t bytes = static_cast<size_t>(h->n) * value_bytes(h->dtype);
     if (!h->x_stage) SPMV_TRY(dev_alloc(h, &h->x_stage, bytes));
-    if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     SPMV_TRY_CUDA(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
-    SPMV_TRY(enqueue(h, h->x_stage, h->y_stage, s, nullptr));
-    SPMV_TRY_CUDA(cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s));
+    // A plan that writes every row of y exactly once (one sliced launch, no accumulating
+    // pass) stores y straight into page-locked host memory: the transfer back then runs
+    // inside the product instead of after it.
+    void *y_direct = nullptr;
+    if (fused_epilogue(h)) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, y_host) == cudaSuccess && attr.type == cudaMemoryTypeHost)
+            y_direct = attr.devicePointer;
+        (void)cudaGetLastError();
+    }
+    if (y_direct) {
+        SPMV_TRY(enqueue(h, h->x_stage, y_direct, s, nullptr));
+    } else {
+        if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
+        SPMV_TRY(enqueue(h, h->x_stage, h->y_stage, s, nullptr));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s));
+    }
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
+// Device address of page-locked host memory (cudaHostAlloc / cudaHostRegister), or an error.
+int mapped_pointer(const void *host, const char *name, void **dev) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, host);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+        (void)cudaGetLastError();
+        return set_error(SPMV_ERR_INVALID_ARG, std::string(name) + " is not page-locked host memory");
+    }
+    *dev = attr.devicePointer;
+    return SPMV_OK;
+}
+
+int spmv_apply_mapped(spmv_handle_t h, const void *x_host, void *y_host, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (h->n == 0) return SPMV_OK;
+    if (!x_host || !y_host) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    SPMV_TRY(check_current_device(h));
+    void *xd = nullptr, *yd = nullptr;
+    SPMV_TRY(mapped_pointer(x_host, "x_host", &xd));
+    SPMV_TRY(mapped_pointer(y_host, "y_host", &yd));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    SPMV_TRY(enqueue(h, xd, yd, s, nullptr));
     SPMV_TRY_CUDA(cudaStreamSynchronize(s));
     return SPMV_OK;
 }

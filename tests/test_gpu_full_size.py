@@ -101,3 +101,45 @@ def test_full_size_integer_x_bit_exact():
     ref = oracle.spmv(csr, x)
     with build(csr, "auto") as A:
         assert_parity(run(A, x), ref, np.float64, exact=True, label="lap2d_256 integer x")
+
+
+# --------------------------------------------------------------------------- #
+# maximum sizes: more than 2^31 slots (64-bit slot offsets in the fill, the apply
+# and the round trip), integer data, every row compared bit for bit
+# --------------------------------------------------------------------------- #
+
+
+def _wide_rows_matrix(n, long_every, long_len, seed):
+    """n rows of one entry each, except every `long_every`-th row (and the last) with
+    `long_len` distinct sorted columns; integer values in [-3, 3]."""
+    from workloads import CSR
+
+    rng = np.random.default_rng(seed)
+    lens = np.ones(n, np.int64)
+    lens[::long_every] = long_len
+    lens[-1] = long_len
+    row_ptr = np.zeros(n + 1, np.int64)
+    np.cumsum(lens, out=row_ptr[1:])
+    cols = rng.integers(0, n, size=int(row_ptr[-1]), dtype=np.int32)
+    long_rows = np.nonzero(lens == long_len)[0]
+    # distinct inside a row: 6007 is odd, so j -> 6007 j is one-to-one modulo n = 2^k
+    base = np.sort((long_rows[:, None] * 7919 + np.arange(long_len)[None, :] * 6007) % n, axis=1)
+    cols[(row_ptr[long_rows][:, None] + np.arange(long_len)[None, :]).ravel()] = base.ravel()
+    vals = rng.integers(-3, 4, size=cols.size, dtype=np.int8).astype(np.float64)
+    return CSR(n, row_ptr.astype(np.int32), cols.astype(np.int32), vals)
+
+
+@pytest.mark.parametrize("fmt,params,long_every", [
+    ("ell_r", {"long_row_threshold": 0}, 1 << 21),
+    ("ell_r", {"long_row_threshold": 0, "row_threads": 4}, 1 << 21),
+    ("sell", {"C": 64, "sigma": 1, "long_row_threshold": 0}, 64),
+])
+def test_more_than_2_31_slots(fmt, params, long_every):
+    n, long_len = 1 << 22, 600
+    csr = _wide_rows_matrix(n, long_every, long_len, seed=11)
+    x = integer_x(n, seed=12)
+    with build(csr, fmt, **params) as A:
+        d = A.describe()
+        assert d["slots"] > 2 ** 31, d["slots"]
+        y = run(A, x)
+        assert_parity(y, oracle.spmv(csr, x), np.float64, exact=True, label=f"{fmt} {params}")
