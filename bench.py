@@ -623,6 +623,69 @@ def run_orderings(args):
         A.close()
 
 
+def run_graph(args):
+    """Applies captured in a CUDA graph (R = 100 per graph) against the same applies
+    launched one by one: the launch-bound small configurations.  One JSON line per
+    value type."""
+    import numpy as np
+    import torch
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+    from workloads import make_workload
+
+    torch.cuda.set_device(0)
+    peak, peak_kind = load_peaks()
+    dtypes = [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+    per_graph = 100
+    for dt in dtypes:
+        csr, x_np = make_workload(args.workload, dtype=dt)
+        sv = csr.vals.dtype.itemsize
+        beff = effective_bytes(csr.n, csr.nnz, sv)
+        dev = torch.device("cuda", 0)
+        rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
+        x = torch.from_numpy(x_np).to(dev)
+        y = torch.empty_like(x)
+        A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=args.format)
+        apply_c = spmv._abi.lib.spmv_apply
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(max(args.warmup, 3)):
+                apply_c(A._h, x.data_ptr(), y.data_ptr(), s.cuda_stream)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream().cuda_stream
+            for _ in range(per_graph):
+                apply_c(A._h, x.data_ptr(), y.data_ptr(), cap)
+        reps = max(args.steps // per_graph, 10)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_graph = e0.elapsed_time(e1) / (reps * per_graph)
+        e0.record()
+        for _ in range(reps * per_graph):
+            apply_c(A._h, x.data_ptr(), y.data_ptr(), None)
+        e1.record()
+        torch.cuda.synchronize()
+        ms_eager = e0.elapsed_time(e1) / (reps * per_graph)
+        print(json.dumps({"workload": args.workload, "dtype": "f64" if sv == 8 else "f32",
+                          "format": A.describe()["format"], "kernels": A.describe()["kernels"],
+                          "applies_per_graph": per_graph, "us_per_apply_graph": ms_graph * 1e3,
+                          "us_per_apply_eager": ms_eager * 1e3, "gflops_graph": 2.0 * csr.nnz / ms_graph / 1e6,
+                          "effective_gbs_graph": beff / ms_graph / 1e6, "frac_graph": beff / ms_graph / 1e6 / peak,
+                          "peak": f"{peak} GB/s {peak_kind}", "bytes_per_apply": beff,
+                          "note": "inputs smaller than L2: this measures launch and L2, not HBM"}), flush=True)
+        A.close()
+
+
 def run_sweep(args):
     """One JSON line per storage format on the chosen workload (format comparison)."""
     import numpy as np
@@ -685,6 +748,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
     ap.add_argument("--nrhs", type=int, default=0,
                     help="with --sweep: time the multi-vector apply with this many right-hand sides instead")
+    ap.add_argument("--graph", action="store_true",
+                    help="time applies captured in a CUDA graph against one-by-one launches (small configurations)")
     ap.add_argument("--orderings", action="store_true",
                     help="time the workload in its given numbering and in the row-length / RCM permuted bases")
     ap.add_argument("--cg", type=int, default=0, metavar="ITERS",
@@ -697,6 +762,8 @@ def main(argv=None):
         run_cg(args)
     elif args.orderings:
         run_orderings(args)
+    elif args.graph:
+        run_graph(args)
     elif args.sweep and args.nrhs > 0:
         run_multi(args)
     elif args.sweep:

@@ -113,6 +113,10 @@ typedef enum {
  *                       column-grouped (column-major slots, a warp per 32 rows and
  *                       residue class of entries mod G, G warps per row combined in
  *                       shared memory; G <= 8).  Automatic = 1.
+ *   x_policy            L2 policy of the x gathers in the sliced formats: 0 = plain
+ *                       read-only loads, 1 = evict-last hint (x stays in L2 while the
+ *                       matrix streams past it).  Automatic = 0 (the hint measured
+ *                       slower once consecutive applies overlap).
  */
 typedef struct {
     int32_t C;
@@ -123,6 +127,7 @@ typedef struct {
     int32_t subwarp;
     int32_t row_threads;
     int32_t row_group_mode;
+    int32_t x_policy;
 } spmv_format_params;
 
 typedef enum {

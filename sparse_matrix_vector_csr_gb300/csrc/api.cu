@@ -749,14 +749,13 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
             return set_error(SPMV_ERR_INVALID_ARG, "unknown format");
     }
     if (h->sliced.present) {
-        // Hint the x gathers to stay in L2 when x is small against it (float64 with
-        // x <= L2 / 4): the matrix stream then cannot evict x between applies.
-        int l2 = 0;
-        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device) != cudaSuccess) {
-            (void)cudaGetLastError();
-            l2 = 0;
-        }
-        h->sliced.keep_x = h->dtype == SPMV_F64 && static_cast<double>(n) * 8.0 <= 0.25 * l2;
+        // x gathers: plain read-only loads unless asked otherwise.  With consecutive
+        // applies overlapped by programmatic dependent launch, an L2 evict-last hint on
+        // x measured slower on every workload (3D Laplacian 128^3, float64: 31.2 against
+        // 30.8 us per apply; small L2-resident matrices 3-7 % slower).
+        if (prm.x_policy > 1) return set_error(SPMV_ERR_INVALID_ARG, "x_policy must be 0 or 1");
+        h->sliced.keep_x = prm.x_policy == 1;
+        h->params.x_policy = h->sliced.keep_x ? 1 : 0;
     }
     if (h->seg.kind == 1) h->kernels.push_back("merge_path");
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
@@ -937,6 +936,7 @@ int spmv_default_params(spmv_format_params *p) {
     p->subwarp = -1;
     p->row_threads = -1;
     p->row_group_mode = -1;
+    p->x_policy = -1;
     return SPMV_OK;
 }
 
