@@ -115,8 +115,9 @@ typedef enum {
  *                       shared memory; G <= 8).  Automatic = 1.
  *   x_policy            L2 policy of the x gathers in the sliced formats: 0 = plain
  *                       read-only loads, 1 = evict-last hint (x stays in L2 while the
- *                       matrix streams past it).  Automatic = 0 (the hint measured
- *                       slower once consecutive applies overlap).
+ *                       matrix streams past it).  Automatic: 1 for float64 when the rows
+ *                       are sorted (sigma > 1), x is at most a quarter of L2 and the
+ *                       matrix stream is larger than L2; otherwise 0.
  */
 typedef struct {
     int32_t C;

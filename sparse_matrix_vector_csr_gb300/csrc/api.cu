@@ -749,12 +749,23 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
             return set_error(SPMV_ERR_INVALID_ARG, "unknown format");
     }
     if (h->sliced.present) {
-        // x gathers: plain read-only loads unless asked otherwise.  With consecutive
-        // applies overlapped by programmatic dependent launch, an L2 evict-last hint on
-        // x measured slower on every workload (3D Laplacian 128^3, float64: 31.2 against
-        // 30.8 us per apply; small L2-resident matrices 3-7 % slower).
+        // x gathers: an L2 evict-last hint keeps x resident while the matrix streams
+        // past it.  It pays when the rows are sorted (their gathers reach across all of
+        // x for the whole kernel) with float64 x at most L2 / 4 and a matrix stream
+        // larger than L2 (power-law 4M: 177.5 against 180.0 us).  In natural order the
+        // gathers are local and plain loads are faster (3D Laplacian 128^3: 30.8 against
+        // 31.2 us; small L2-resident matrices 3-7 %).
         if (prm.x_policy > 1) return set_error(SPMV_ERR_INVALID_ARG, "x_policy must be 0 or 1");
-        h->sliced.keep_x = prm.x_policy == 1;
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device) != cudaSuccess) {
+            (void)cudaGetLastError();
+            l2 = 0;
+        }
+        const double stream_bytes = static_cast<double>(h->sliced.slots) * (value_bytes(h->dtype) + 4);
+        h->sliced.keep_x = prm.x_policy >= 0 ? prm.x_policy == 1
+                                             : h->dtype == SPMV_F64 && h->sliced.perm != nullptr &&
+                                                   static_cast<double>(n) * 8.0 <= 0.25 * l2 &&
+                                                   stream_bytes > static_cast<double>(l2);
         h->params.x_policy = h->sliced.keep_x ? 1 : 0;
     }
     if (h->seg.kind == 1) h->kernels.push_back("merge_path");
