@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kSellBlock, 6)
 // at every step it reads one contiguous run of 32 slots of column j.  The G warps that
 // share a set of 32 rows add their partial sums in shared memory, in warp order.
 template <typename T, int G, bool K>
-__global__ void __launch_bounds__(kSellBlock, 6)
+__global__ void __launch_bounds__(kSellBlock, (G == 8 && sizeof(T) == 8) ? 5 : 6)  // no spills at G = 8, float64
     k_sellcg(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     constexpr int U = 4;
     constexpr int kSets = kSellBlock / 32 / G;  // sets of 32 rows per block
