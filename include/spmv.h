@@ -3,10 +3,10 @@
  *
  * The library computes y = A x for a square n x n sparse matrix A handed over in
  * compressed sparse row (CSR) form: row_ptr[n+1], col_idx[nnz], vals[nnz].
- * Problem statement: "Sparse matrix-vector multiplication (spMVM) is often the
- * dominating component" of iterative solvers -- GPGPU spMVM paper (arXiv 1112.5588),
- * introduction; the CSR arrays are the Ap/Aj/Ax of "Development of Krylov and AMG
- * linear solvers for large-scale sparse matrices on GPUs", matrix formats, Figure 3.
+ * The GPGPU spMVM paper (arXiv 1112.5588, introduction) identifies this product as
+ * the part of iterative sparse solvers that usually takes most of the time; the CSR
+ * arrays are the Ap/Aj/Ax of "Development of Krylov and AMG linear solvers for
+ * large-scale sparse matrices on GPUs", matrix formats, Figure 3.
  *
  * A build call converts the CSR input, on the device, into one of the storage
  * formats the pages describe and returns an opaque handle; apply calls reuse it.
@@ -77,7 +77,7 @@ typedef enum { SPMV_F64 = 0, SPMV_F32 = 1 } spmv_dtype;
  *      kernels of the scite report's abstract).  Suited to irregular matrices.
  *  SPMV_FMT_AUTO        the builder picks one of the above from the row lengths.
  * In every format, rows longer than the long-row threshold are taken out and
- * handled by a load-balanced merge-path pass (the "very long rows" class of the
+ * handled by a load-balanced merge-path pass (the class of the longest rows in the
  * Trilinos issue; merge-path split as the Trilinos issue attributes to the vendor
  * library), so no single thread walks a very long row.
  */

@@ -4,10 +4,10 @@
 // ELLPACK-R section; the "early stopping" quoted in the scite report
 // "Load-balancing Sparse Matrix Vector Product Kernels on GPUs").
 //
-// Long rows leave the sliced layout for the row-split pass (the "very long rows"
-// scheme of the Trilinos issue on unpackAndCombine: over rows, then over blocks of
-// entries within a row, then over entries within a block): every long row is cut
-// into chunks of at most kSplitChunk entries and one warp reduces one chunk.  A row
+// Long rows leave the sliced layout for the row-split pass (the Trilinos issue on
+// unpackAndCombine treats its longest class of rows with three levels of parallelism:
+// rows, pieces of a row, and the entries of a piece): every long row is cut into
+// chunks of at most kSplitChunk entries and one warp reduces one chunk.  A row
 // with a single chunk is written at once; for longer rows the warp that completes
 // the last chunk sums the row's partials (in double, in chunk order) -- it learns it
 // is last from a per-row integer counter.  Work per warp is bounded whatever the

@@ -14,7 +14,7 @@ available here:
   large-scale sparse matrices on GPUs" (numerical experiments section).
 * :func:`hmep_like` copies the shape the GPGPU spMVM paper (arXiv 1112.5588,
   test-matrix section) gives for HMEp: dimension 6.2e6, about 15 non-zeros per
-  row, contiguous off-diagonals of length 15,000.
+  row, off-diagonals made of unbroken runs 15,000 entries long.
 * :func:`power_law` is an irregular matrix with a few nearly dense rows, the case
   "Load-balancing Sparse Matrix Vector Product Kernels on GPUs" (abstract) and the
   Trilinos issue (description) single out.
