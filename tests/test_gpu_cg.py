@@ -5,7 +5,7 @@ rounding: each product within 1e-12 * sum |a_ij x_j| per row, each dot product i
 its summation order (about n * 2^-53 relative).  Over k <= 12 steps on the 67 x 45
 Laplacian (condition number about 1.2e3) these differences grow at most by a factor
 of order kappa per step sequence, far below the 1e-9 relative bound used for the
-fixed-step comparison.  Converged runs are judged by the true residual, recomputed
+fixed-step comparison.  Converged runs are checked through the true residual, recomputed
 with the oracle's product, and by an iteration count within one step of the oracle's
 (the stopping decision is the same double comparison on both sides, so only a
 residual lying within rounding of the threshold can move it).
