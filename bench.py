@@ -325,6 +325,36 @@ def cpu_baseline(csr, x_np, budget_s=8.0):
             "seconds": dt}
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def cpu_openmp_baseline(csr, x_np, schedule):
+    """The plain OpenMP CSR product (oracle/csr_omp.c) on every host core: median of 11
+    applies of the full workload after one warm-up."""
+    import oracle
+
+    oracle.omp_spmv(csr, x_np, schedule)
+    times = []
+    for _ in range(11):
+        t0 = time.perf_counter()
+        _, used = oracle.omp_spmv(csr, x_np, schedule)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return {"value": 2.0 * csr.nnz / t / 1e9, "unit": UNIT, "cores": used, "cpu": cpu_model(),
+            "kind": "openmp_csr", "schedule": schedule, "ms_per_apply": t * 1e3,
+            "sample": "the full workload, median of 11 applies, value-type sums"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -428,6 +458,8 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(csr64, x64)
+        line["cpu_openmp"] = cpu_openmp_baseline(csr64, x64,
+                                                 "dynamic" if args.workload.startswith("powerlaw") else "static")
     print(json.dumps(line), flush=True)
 
 

@@ -14,6 +14,8 @@ Contents
 * :func:`spmv_scaled`, :func:`spmm` -- y = alpha A x + beta y and its multi-vector
   form Y = alpha A X + beta Y, from the long double product above.
 * :func:`check_rows` -- the acceptance rule for a computed y.
+* :func:`omp_spmv` -- not an oracle: the plain OpenMP CSR product the bench reports as
+  the multi-core CPU baseline (``csr_omp.c``).
 * :mod:`oracle.cg` -- conjugate gradients (Hestenes-Stiefel) in float64 on the
   product above, for the solver built on the library.
 
@@ -44,6 +46,40 @@ def build(out_path: str = _LIB_PATH, mutation: int = 0) -> str:
         cmd.insert(1, f"-DORACLE_MUTATION={int(mutation)}")
     subprocess.run(cmd, check=True)
     return out_path
+
+
+_OMP_SRC = os.path.join(_HERE, "csr_omp.c")
+_OMP_PATH = os.path.join(_HERE, "libcsr_omp.so")
+_omp = None
+
+
+def build_omp(out_path: str = _OMP_PATH) -> str:
+    """Compile the multi-core CPU baseline (gcc -fopenmp).  Returns the library path."""
+    subprocess.run(["gcc", "-O3", "-fopenmp", "-std=c11", "-shared", "-fPIC", "-o", out_path, _OMP_SRC],
+                   check=True)
+    return out_path
+
+
+def omp_spmv(csr, x, schedule: str = "static", threads: int = 0):
+    """y = A x by the OpenMP CSR baseline (value-type sums, stored order).  Returns
+    (y, threads used)."""
+    global _omp
+    with _lock:
+        if _omp is None:
+            if not os.path.exists(_OMP_PATH) or os.path.getmtime(_OMP_PATH) < os.path.getmtime(_OMP_SRC):
+                build_omp()
+            lib = ctypes.CDLL(_OMP_PATH)
+            lib.csr_omp_spmv.restype = ctypes.c_int
+            lib.csr_omp_spmv.argtypes = [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+            _omp = lib
+    dt = np.dtype(csr.vals.dtype)
+    x = np.ascontiguousarray(x, dtype=dt)
+    y = np.empty(csr.n, dt)
+    used = _omp.csr_omp_spmv(csr.n, csr.row_ptr.ctypes.data, csr.col_idx.ctypes.data if csr.nnz else None,
+                             csr.vals.ctypes.data if csr.nnz else None, _dtype_code(dt), x.ctypes.data,
+                             y.ctypes.data, 1 if schedule == "dynamic" else 0, int(threads))
+    return y, int(used)
 
 
 def _bind(path: str):

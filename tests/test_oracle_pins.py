@@ -279,3 +279,15 @@ def test_spmm_matches_dense(k):
     ref = oracle.spmm(csr, X, -1.0, 2.0, Y)
     assert ref["y"].shape == (40, k)
     assert np.array_equal(ref["y"], -1.0 * (dense_of(csr) @ X) + 2.0 * Y)
+
+
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_openmp_baseline_agrees_with_oracle(schedule, dtype):
+    """The multi-core CPU baseline of the bench computes the same product (value-type sums)."""
+    from workloads import make_workload
+    csr, x = make_workload("powerlaw_small", dtype=dtype)
+    y, used = oracle.omp_spmv(csr, x, schedule)
+    ok, worst, row = oracle.check_rows(y, oracle.spmv(csr, x), dtype)
+    assert ok, (worst, row)
+    assert used >= 1
