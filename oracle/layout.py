@@ -109,17 +109,21 @@ def slot_offset(q, j, stride: int, group: int = 1, interleaved: bool = False):
 
 
 def sell_slots(csr, C: int, sigma: int, exclude=None, group: int = 1, interleaved: bool = False,
-               ell_ld: int | None = None) -> tuple:
+               ell_ld: int | None = None, group_val: int | None = None, round_to: int | None = None) -> tuple:
     """The slot arrays (column, value) of a sliced layout built from ``csr``.
 
     SELL (``ell_ld`` None): slices of C sorted positions with ``sell_layout`` widths.
     ELLPACK (``ell_ld`` given): one slice, rows in natural order, leading dimension
     ``ell_ld``, width = the longest stored row.  Widths are rounded up to whole groups
-    in the column-grouped (interleaved) layout only.  Excluded
-    rows and padding slots hold column 0 and value 0.
+    in the column-grouped (interleaved) layout only (to ``round_to`` when given).
+    ``group_val``: the value array grouped differently from the index array (the
+    16-byte vector layout: indices in groups of 4, values in groups of 16 bytes).
+    Excluded rows and padding slots hold column 0 and value 0.
     """
     lens = row_lengths(csr.row_ptr)
-    round_to = group if interleaved else 1  # only the column-grouped layout stores whole groups
+    if round_to is None:
+        round_to = group if interleaved else 1  # only the column-grouped layout stores whole groups
+    gv = group if group_val is None else group_val
     if ell_ld is None:
         lay = sell_layout(lens, C, sigma, exclude=exclude, group=round_to)
         perm, stored, starts, stride = lay["perm"], lay["sorted_lens"], lay["slice_ptr"], C
@@ -143,9 +147,8 @@ def sell_slots(csr, C: int, sigma: int, exclude=None, group: int = 1, interleave
     P = np.repeat(np.arange(perm.size), reps)
     J = np.arange(P.size) - np.repeat(np.cumsum(reps) - reps, reps)
     src = csr.row_ptr[perm[P]].astype(np.int64) + J
-    off = base[P] + slot_offset(q[P], J, stride, group, interleaved)
-    col[off] = csr.col_idx[src]
-    val[off] = csr.vals[src]
+    col[base[P] + slot_offset(q[P], J, stride, group, interleaved)] = csr.col_idx[src]
+    val[base[P] + slot_offset(q[P], J, stride, gv, interleaved)] = csr.vals[src]
     return col, val
 
 

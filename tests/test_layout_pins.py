@@ -215,3 +215,25 @@ def test_ell_slots_brute_force(group, interleaved):
     got = layout.sell_slots(csr, 0, 1, group=group, interleaved=interleaved, ell_ld=96)
     exp = _brute_slots(csr, 0, 1, None, group, interleaved, ell_ld=96)
     assert np.array_equal(got[0], exp[0]) and np.array_equal(got[1], exp[1])
+
+
+@pytest.mark.parametrize("C,gval", [(32, 2), (64, 4)])
+def test_vector_layout_slots_brute_force(C, gval):
+    """The 16-byte vector layout: indices in groups of 4, values in groups of gval (2
+    doubles or 4 floats), slice widths rounded to a multiple of 4."""
+    from workloads import random_csr
+    csr = random_csr(140, density=0.07, seed=9)
+    lens = layout.row_lengths(csr.row_ptr)
+    got = layout.sell_slots(csr, C, 1, group=4, interleaved=True, group_val=gval, round_to=4)
+    lay = layout.sell_layout(lens, C, 1, group=4)
+    col = np.zeros(int(lay["slice_ptr"][-1]), np.int32)
+    val = np.zeros(col.size, csr.vals.dtype)
+    for p_, r in enumerate(lay["perm"]):
+        s_, q = divmod(p_, C)
+        wc = _walk_offsets(C, int(lay["widths"][s_]), 4, True)
+        wv = _walk_offsets(C, int(lay["widths"][s_]), gval, True)
+        for j in range(int(lay["sorted_lens"][p_])):
+            col[lay["slice_ptr"][s_] + wc[(q, j)]] = csr.col_idx[csr.row_ptr[r] + j]
+            val[lay["slice_ptr"][s_] + wv[(q, j)]] = csr.vals[csr.row_ptr[r] + j]
+    assert np.array_equal(got[0], col) and np.array_equal(got[1], val)
+
