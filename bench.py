@@ -108,6 +108,8 @@ def kernel_source(kernel: str) -> str:
         name = "vector.cu"
     elif "_g" in kernel and kernel.split("_g")[-1][:-1].isdigit():  # G threads per row: sell_g4i, ell_r_g8r, ...
         name = "sellg.cu"
+    elif kernel.endswith("_v"):  # 16-byte vector loads: sell_v, ell_r_v, hyb_ell_v
+        name = "sellv.cu"
     else:
         name = KERNEL_SOURCES.get(kernel, "")
     return os.path.join(ROOT, "sparse_matrix_vector_csr_gb300", "csrc", name)
@@ -517,7 +519,8 @@ SWEEP_FORMATS = [
     ("sell", {"row_threads": 16}), ("sell", {"row_threads": 32}), ("sell", {"row_threads": 4, "row_group_mode": 0}),
     ("sell", {"row_threads": 8, "row_group_mode": 0}), ("sell", {"row_threads": 2, "row_group_mode": 2}),
     ("sell", {"row_threads": 4, "row_group_mode": 2}), ("sell", {"row_threads": 8, "row_group_mode": 2}),
-    ("ell_r", {"row_threads": 4}),
+    ("ell_r", {"row_threads": 4}), ("sell", {"vector_loads": 1}), ("sell", {"C": 64, "vector_loads": 1}),
+    ("sell", {"sigma": 1 << 30, "vector_loads": 1}),
 ]
 
 

@@ -118,6 +118,11 @@ typedef enum {
  *                       matrix streams past it).  Automatic: 1 for float64 when the rows
  *                       are sorted (sigma > 1), x is at most a quarter of L2 and the
  *                       matrix stream is larger than L2; otherwise 0.
+ *   vector_loads        1 = one thread per row reads its row 4 entries at a time with
+ *                       16-byte loads (indices in groups of 4, values in 16-byte groups,
+ *                       slice widths rounded up to a multiple of 4); 0 = element loads.
+ *                       Takes one thread per row (an automatic row_threads becomes 1; an
+ *                       explicit row_threads > 1 is SPMV_ERR_UNSUPPORTED).  Automatic = 0.
  */
 typedef struct {
     int32_t C;
@@ -129,6 +134,7 @@ typedef struct {
     int32_t row_threads;
     int32_t row_group_mode;
     int32_t x_policy;
+    int32_t vector_loads;
 } spmv_format_params;
 
 typedef enum {

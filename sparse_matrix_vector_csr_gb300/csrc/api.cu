@@ -168,6 +168,7 @@ struct BuildCtx {
     int32_t group = 1;       // threads per row of the sliced apply
     int group_mode = 0;      // 0 row-grouped, 1 interleaved slots, 2 column-grouped
     bool interleaved = false;
+    bool vec = false;        // one thread per row, 16-byte vector loads
     Temp temp;
 };
 
@@ -339,8 +340,15 @@ int plan_sliced(BuildCtx &c, const int32_t *lens, int32_t C, int64_t sigma, int6
     sl.group = c.group;
     sl.log2g = bits_for(static_cast<uint64_t>(c.group)) - 1;
     sl.group_mode = c.group_mode;
-    sl.interleaved = c.interleaved;
-    const int32_t round_to = c.interleaved ? c.group : 1;
+    sl.interleaved = c.interleaved || c.vec;
+    sl.vec = c.vec;
+    if (c.vec) {  // indices in groups of 4 (16 bytes), values in 16-byte groups (2 doubles or 4 floats)
+        sl.log2k_col = 2;
+        sl.log2k_val = value_bytes(h->dtype) == 8 ? 1 : 2;
+    } else if (c.interleaved) {
+        sl.log2k_col = sl.log2k_val = sl.log2g;
+    }
+    const int32_t round_to = c.vec ? 4 : c.interleaved ? c.group : 1;
     if (ell_ld > 0) {
         sl.C = static_cast<int32_t>(std::min<int64_t>(ell_ld, INT32_MAX));
         sl.ld = ell_ld;
@@ -471,8 +479,8 @@ int build_sell_like(BuildCtx &c, int format, int32_t C, int64_t sigma) {
     SPMV_TRY(fill_sliced(c));
     SPMV_TRY(build_long_rows(c, 0));
     const std::string name = format == SPMV_FMT_ELL_R ? "ell_r" : "sell";
-    if (c.group > 1) {  // grouped kernel, then the long rows' chunks in a launch of their own
-        h->kernels.push_back(name + group_suffix(c));
+    if (c.group > 1 || c.vec) {  // grouped / vector kernel, then the long rows' chunks in a launch of their own
+        h->kernels.push_back(name + (c.vec ? std::string("_v") : group_suffix(c)));
         if (h->seg.kind == 3) h->kernels.push_back("rowsplit_chunks");
     } else {
         h->kernels.push_back(h->seg.kind == 3 ? name + "+rowsplit" : name);
@@ -501,7 +509,7 @@ int build_hyb(BuildCtx &c, int32_t K, int spill_csr) {
     const int64_t m = start[2] - start[1];
     SPMV_TRY(build_segment(c, rows + start[1], m, K, spill_csr ? 1 : 2, 1));
     h->sliced.stored_entries = h->nnz - h->seg.nnz;
-    h->kernels.push_back("hyb_ell" + (c.group > 1 ? group_suffix(c) : std::string()));
+    h->kernels.push_back("hyb_ell" + (c.vec ? std::string("_v") : c.group > 1 ? group_suffix(c) : std::string()));
     return SPMV_OK;
 }
 
@@ -694,6 +702,7 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
         int32_t g = prm.row_threads;
         if (g > 0 && (g > 32 || (g & (g - 1))))
             return set_error(SPMV_ERR_INVALID_ARG, "row_threads must be 1, 2, 4, 8, 16 or 32");
+        if (g <= 0 && prm.vector_loads == 1) g = 1;  // vector loads: one thread per row
         if (g <= 0) {
             int sms = 0;
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -710,9 +719,14 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
         c.group = g;
         c.group_mode = mode;
         c.interleaved = mode == 1;
+        if (prm.vector_loads > 1) return set_error(SPMV_ERR_INVALID_ARG, "vector_loads must be 0 or 1");
+        if (prm.vector_loads == 1 && g > 1)
+            return set_error(SPMV_ERR_UNSUPPORTED, "vector loads take one thread per row (row_threads 1)");
+        c.vec = prm.vector_loads == 1;
     }
     h->params.row_threads = c.group;
     h->params.row_group_mode = c.group_mode;
+    h->params.vector_loads = c.vec ? 1 : 0;
 
     switch (format) {
         case SPMV_FMT_CSR_VECTOR: {
@@ -804,7 +818,7 @@ struct Recorder {
 
 // Formats whose kernels write y exactly once per row (so alpha/beta fold into that write).
 bool fused_epilogue(spmv_handle_t h) {
-    if (h->sliced.group > 1) return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
+    if (h->sliced.group > 1 || h->sliced.vec) return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
     return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && (h->seg.kind == 0 || h->seg.kind == 3);
 }
 
@@ -828,9 +842,12 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
             SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
-    } else if (h->sliced.present && h->sliced.group > 1) {
-        // G threads per row, then the long rows' chunks
-        SPMV_TRY_CUDA(launch_sellg_apply(h->dtype, h->sliced, h->n, x, y, s, scale));
+    } else if (h->sliced.present && (h->sliced.group > 1 || h->sliced.vec)) {
+        // G threads per row or vector loads, then the long rows' chunks
+        if (h->sliced.vec)
+            SPMV_TRY_CUDA(launch_sellv_apply(h->dtype, h->sliced, h->n, x, y, s, scale));
+        else
+            SPMV_TRY_CUDA(launch_sellg_apply(h->dtype, h->sliced, h->n, x, y, s, scale));
         if (rec) SPMV_TRY(rec->mark(s));
         if (split) {
             SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
@@ -948,6 +965,7 @@ int spmv_default_params(spmv_format_params *p) {
     p->row_threads = -1;
     p->row_group_mode = -1;
     p->x_policy = -1;
+    p->vector_loads = -1;
     return SPMV_OK;
 }
 
@@ -1285,7 +1303,8 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     append(o, "\"C\":%d,\"sigma\":%lld,\"K\":%d,\"spill_csr\":%d,\"long_row_threshold\":%d,\"subwarp\":%d,",
            h->params.C, (long long)h->params.sigma, h->params.K, h->params.spill_csr, h->params.long_row_threshold,
            h->params.subwarp);
-    append(o, "\"row_threads\":%d,\"row_group_mode\":%d,", h->params.row_threads, h->params.row_group_mode);
+    append(o, "\"row_threads\":%d,\"row_group_mode\":%d,\"vector_loads\":%d,", h->params.row_threads,
+           h->params.row_group_mode, h->params.vector_loads);
     append(o, "\"sliced\":%s,\"n_slices\":%lld,\"slots\":%lld,\"padded_entries\":%lld,\"stored_entries\":%lld,"
               "\"ld\":%lld,\"max_width\":%d,\"permuted\":%s,",
            sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,

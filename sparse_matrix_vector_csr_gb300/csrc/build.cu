@@ -380,7 +380,8 @@ __global__ void k_slice_widths(const int32_t *__restrict__ len_sorted, int64_t n
 }
 
 template <typename T>
-__global__ void k_fill_sliced(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride, int log2g, bool interleaved,
+__global__ void k_fill_sliced(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride, int log2k_col, int log2k_val,
+                              bool interleaved,
                               const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ width,
                               const int32_t *__restrict__ len_sorted, const int32_t *__restrict__ perm,
                               const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_in,
@@ -394,13 +395,14 @@ __global__ void k_fill_sliced(int64_t n_pos, int log2C, uint32_t cmask, int64_t 
         int64_t src = 0;
         if (L > 0) src = row_ptr[perm ? perm[p] : p];
         for (int32_t j = 0; j < w; ++j) {
-            const int64_t slot = slot_of(base, q, j, stride, log2g, interleaved);
+            const int64_t sc = slot_of(base, q, j, stride, log2k_col, interleaved);
+            const int64_t sv = slot_of(base, q, j, stride, log2k_val, interleaved);
             if (j < L) {
-                col_out[slot] = col_in[src + j];
-                val_out[slot] = val_in[src + j];
+                col_out[sc] = col_in[src + j];
+                val_out[sv] = val_in[src + j];
             } else {
-                col_out[slot] = 0;
-                val_out[slot] = T(0);
+                col_out[sc] = 0;
+                val_out[sv] = T(0);
             }
         }
     }
@@ -513,8 +515,8 @@ __global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, const i
 // to_csr
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void k_sliced_to_csr(int64_t n, int64_t n_pos, int log2C, uint32_t cmask, int64_t stride, int log2g,
-                                bool interleaved, const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ len_sorted,
+__global__ void k_sliced_to_csr(int64_t n, int64_t n_pos, int log2C, uint32_t cmask, int64_t stride, int log2k_col,
+                                int log2k_val, bool interleaved, const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ len_sorted,
                                 const int32_t *__restrict__ perm, const int32_t *__restrict__ col,
                                 const T *__restrict__ val, const int32_t *__restrict__ out_ptr,
                                 int32_t *__restrict__ out_col, T *__restrict__ out_val) {
@@ -525,9 +527,8 @@ __global__ void k_sliced_to_csr(int64_t n, int64_t n_pos, int log2C, uint32_t cm
         const int64_t base = slice_ptr[p >> log2C], q = static_cast<int64_t>(p & cmask);
         int64_t dst = out_ptr[r];
         for (int32_t j = 0; j < L; ++j) {
-            const int64_t slot = slot_of(base, q, j, stride, log2g, interleaved);
-            out_col[dst + j] = col[slot];
-            out_val[dst + j] = val[slot];
+            out_col[dst + j] = col[slot_of(base, q, j, stride, log2k_col, interleaved)];
+            out_val[dst + j] = val[slot_of(base, q, j, stride, log2k_val, interleaved)];
         }
     }
 }
@@ -651,13 +652,15 @@ cudaError_t launch_fill_sliced(int dtype, const Sliced &sl, const int32_t *row_p
     if (sl.n_pos <= 0 || sl.slots <= 0) return cudaSuccess;
     unsigned g = grid_for(sl.n_pos, kBlock, 1 << 20);
     if (dtype == SPMV_F64)
-        k_fill_sliced<double><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g, sl.interleaved,
+        k_fill_sliced<double><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2k_col, sl.log2k_val,
+                                                   sl.interleaved,
                                                    sl.slice_ptr, sl.width,
                                                    sl.len, sl.perm, row_ptr, col_in,
                                                    static_cast<const double *>(val_in), sl.col,
                                                    static_cast<double *>(sl.val));
     else
-        k_fill_sliced<float><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g, sl.interleaved,
+        k_fill_sliced<float><<<g, kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2k_col, sl.log2k_val,
+                                                  sl.interleaved,
                                                   sl.slice_ptr, sl.width,
                                                   sl.len, sl.perm, row_ptr, col_in,
                                                   static_cast<const float *>(val_in), sl.col,
@@ -722,13 +725,13 @@ cudaError_t launch_sliced_to_csr(int dtype, int64_t n, const Sliced &sl, const i
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
     unsigned g = grid_for(sl.n_pos, kBlock, 1 << 20);
     if (dtype == SPMV_F64)
-        k_sliced_to_csr<double><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g,
-                                                     sl.interleaved, sl.slice_ptr,
+        k_sliced_to_csr<double><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2k_col,
+                                                     sl.log2k_val, sl.interleaved, sl.slice_ptr,
                                                      sl.len, sl.perm, sl.col, static_cast<const double *>(sl.val),
                                                      out_ptr, out_col, static_cast<double *>(out_val));
     else
-        k_sliced_to_csr<float><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2g,
-                                                    sl.interleaved, sl.slice_ptr,
+        k_sliced_to_csr<float><<<g, kBlock, 0, s>>>(n, sl.n_pos, sl.log2C, sl.cmask, sl.stride, sl.log2k_col,
+                                                    sl.log2k_val, sl.interleaved, sl.slice_ptr,
                                                     sl.len, sl.perm, sl.col, static_cast<const float *>(sl.val),
                                                     out_ptr, out_col, static_cast<float *>(out_val));
     return cudaGetLastError();

@@ -50,7 +50,10 @@ struct Sliced {
     int32_t group = 1;             // threads per row in the apply (1, 2, 4, ..., 32)
     int log2g = 0;
     int group_mode = 0;            // with group > 1: 0 row-grouped, 1 interleaved, 2 column-grouped
-    bool interleaved = false;      // slot layout, see slot_of() (group_mode 1)
+    bool interleaved = false;      // slot layout, see slot_of() (group_mode 1 or vec)
+    bool vec = false;              // one thread per row reading 16-byte vectors of its row
+    int log2k_col = 0;             // interleaved slots: index groups of 2^log2k_col
+    int log2k_val = 0;             //                    value groups of 2^log2k_val
     int64_t *slice_ptr = nullptr;  // [n_slices + 1]
     int32_t *width = nullptr;      // [n_slices]
     int32_t *len = nullptr;        // [n_pos] entries stored at each position
@@ -281,6 +284,10 @@ int permute_csr(int dtype, int64_t n, int64_t nnz, const int32_t *row_ptr, const
 cudaError_t launch_permute_vector(int dtype, int64_t n, const int32_t *perm, const void *src, void *dst,
                                   int direction, cudaStream_t s);
 
+// One thread per row with 16-byte vector loads (sellv.cu, sl.vec); long rows are left to
+// launch_rowsplit.
+cudaError_t launch_sellv_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s,
+                               const Scale *scale = nullptr);
 // G = sl.group threads per row (sellg.cu); long rows (len = -1) are left to launch_rowsplit.
 cudaError_t launch_sellg_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s,
                                const Scale *scale = nullptr);

@@ -83,6 +83,11 @@ FORMAT_CASES = [
     ("ell_r", {"row_threads": 16}),
     ("hyb", {"row_threads": 4, "K": 3, "spill_csr": 0}),
     ("sell", {"row_threads": 1}),
+    # one thread per row with 16-byte vector loads
+    ("sell", {"vector_loads": 1}),
+    ("sell", {"C": 64, "sigma": 1 << 30, "vector_loads": 1, "long_row_threshold": 8}),
+    ("ell_r", {"vector_loads": 1}),
+    ("hyb", {"vector_loads": 1, "K": 5}),
 ]
 
 

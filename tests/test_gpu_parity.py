@@ -190,7 +190,8 @@ def test_sell_layout_matches_definition(name, C, sigma):
 
 SLOT_CASES = [("sell", 32, 1, 1, 0), ("sell", 64, 256, 1, 0), ("sell", 32, 1, 4, 1), ("sell", 32, 1 << 30, 8, 1),
               ("sell", 64, 1, 8, 0), ("sell", 32, 4096, 32, 1), ("ell_r", 0, 1, 1, 0), ("ell_r", 0, 1, 4, 1),
-              ("ell_r", 0, 1, 2, 0), ("sell", 32, 1, 4, 2), ("ell_r", 0, 1, 8, 2)]
+              ("ell_r", 0, 1, 2, 0), ("sell", 32, 1, 4, 2), ("ell_r", 0, 1, 8, 2),
+              ("sell", 32, 1, 1, "vec"), ("sell", 64, 1 << 30, 1, "vec"), ("ell_r", 0, 1, 1, "vec")]
 
 
 @pytest.mark.parametrize("fmt,C,sigma,g,il", SLOT_CASES, ids=[f"{f}-C{c}-s{s}-g{g}-i{i}" for f, c, s, g, i in SLOT_CASES])
@@ -200,17 +201,23 @@ def test_slot_arrays_match_definition(name, fmt, C, sigma, g, il):
     oracle's layout definition: bit-exact index and byte work."""
     csr, _, _ = small(name)
     lens = layout.row_lengths(csr.row_ptr)
-    kw = {"row_threads": g, "row_group_mode": il}
+    vec = il == "vec"
+    kw = {"row_threads": g, "row_group_mode": 0 if vec else il, "vector_loads": 1 if vec else 0}
     if fmt == "sell":
         kw.update(C=C, sigma=sigma)
     with build(csr, fmt, **kw) as A:
         d = A.describe()
-        assert d["row_threads"] == g and d["row_group_mode"] == il
+        assert d["row_threads"] == g and d["vector_loads"] == int(vec)
         exclude = layout.long_rows(lens, d["long_row_threshold"])
-        if fmt == "sell":
-            exp = layout.sell_slots(csr, C, min(sigma, csr.n), exclude=exclude, group=g, interleaved=il == 1)
+        if vec:  # indices in 4s, values in 16-byte groups, widths a multiple of 4
+            opts = dict(group=4, interleaved=True, group_val=16 // csr.vals.dtype.itemsize, round_to=4)
         else:
-            exp = layout.sell_slots(csr, 0, 1, exclude=exclude, group=g, interleaved=il == 1, ell_ld=d["ld"])
+            assert d["row_group_mode"] == il
+            opts = dict(group=g, interleaved=il == 1)
+        if fmt == "sell":
+            exp = layout.sell_slots(csr, C, min(sigma, csr.n), exclude=exclude, **opts)
+        else:
+            exp = layout.sell_slots(csr, 0, 1, exclude=exclude, ell_ld=d["ld"], **opts)
         col, val = A.slots()
         assert col.numel() == exp[0].size == d["slots"]
         assert np.array_equal(col.cpu().numpy(), exp[0])
