@@ -31,7 +31,15 @@ if ROOT not in sys.path:
 METRIC = "SpMV GFLOP/s and effective HBM GB/s (fraction of GB300 peak), fp64 & fp32"
 UNIT = "GFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
-L2_BYTES = 129e6
+L2_BYTES = 129e6  # replaced by the device's own figure once a GPU is selected (device_l2_bytes)
+
+
+def device_l2_bytes(torch) -> float:
+    """L2 size of the current device in bytes (the GB300 figure if the query fails)."""
+    try:
+        return float(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except (AttributeError, RuntimeError):
+        return L2_BYTES
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -265,7 +273,7 @@ def measure_device(torch, spmv, csr, x_np, steps, warmup, sampler=None, fmt="aut
     splits = [A.apply_profiled(x, y) for _ in range(20)]
     per_kernel = [statistics.median(s[i] for s in splits) for i in range(len(splits[0]))]
     # cold: L2 flushed before every apply (flush outside the events)
-    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    flush = torch.empty(int(2 * device_l2_bytes(torch)) // 4, dtype=torch.float32, device=dev)
     cold = []
     for _ in range(30):
         flush.fill_(1.0)
@@ -394,6 +402,7 @@ def run_ours(args):
 
     if rank != 0:
         return
+    l2_bytes = device_l2_bytes(torch)
     peak, peak_kind = load_peaks()
 
     def summarize(tag, sv):
@@ -441,8 +450,9 @@ def run_ours(args):
             "workload": WORKLOADS[args.workload]["desc"] + f" (nnz={nnz}), float64 headline, float32 beside it",
             "n": n, "nnz": nnz, "format": s64["format"]["format"], "parallelism": "replicas" if world > 1 else "single",
             "l2": (f"inputs larger than L2: one apply streams {effective_bytes(n, nnz, 8) / 1e6:.0f} MB (f64) / "
-                   f"{effective_bytes(n, nnz, 4) / 1e6:.0f} MB (f32) > {L2_BYTES / 1e6:.0f} MB L2, applies back to "
+                   f"{effective_bytes(n, nnz, 4) / 1e6:.0f} MB (f32) > {l2_bytes / 1e6:.0f} MB L2, applies back to "
                    "back; cold_* fields flush L2 before every apply"),
+            "l2_bytes": int(l2_bytes),
         },
         "effective_gbs": s64["effective_gbs"],
         "roofline": s64["roofline"],
