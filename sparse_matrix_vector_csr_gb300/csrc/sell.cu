@@ -60,10 +60,12 @@ __device__ __forceinline__ void load_slots(const int32_t *__restrict__ cp, const
 //          used by the single-slice ELLPACK-R / HYB-ELL layout and other slice heights.
 // Entries are processed U at a time: U column indices and values (predicated on the
 // row length, so padding is never touched), then the U gathers, then U FMAs.
-template <typename T, int CS, bool K>
+// UW > 0 replaces U (the short-row variant below loads a whole row of up to UW entries
+// before the dependency wait).
+template <typename T, int CS, bool K, int UW = 0>
 __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
                                          const T *__restrict__ x, T *__restrict__ y, const Epi &ep) {
-    constexpr int U = SellChunk<T, CS>::U;
+    constexpr int U = UW > 0 ? UW : SellChunk<T, CS>::U;
     const int w = __ldg(a.len + p);
     const uint64_t up = static_cast<uint64_t>(p);
     const int64_t slot = CS > 0 ? __ldg(a.slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
@@ -171,6 +173,18 @@ __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
     if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y, ep);
 }
 
+// Short rows on a small matrix (fewer row positions than one wave of threads, every row
+// at most kShortRow entries): each thread loads its whole row before grid_wait(), so
+// between back-to-back applies the matrix read overlaps the previous apply entirely.
+// With less than a wave there is no occupancy to protect, hence 64 registers.
+template <typename T, int CS, bool K>
+__global__ void __launch_bounds__(kSellBlock, 4)
+    k_sell_short(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
+    allow_dependents();
+    const int64_t p = gtid();
+    if (p < a.n_pos) sell_row<T, CS, K, kShortRow>(p, a, val, x, y, ep);
+}
+
 // Sliced rows and row-split chunks in one launch: the first split_ctas CTAs take
 // eight chunks each (one per warp), the rest take kSellBlock row positions each.
 // Float64 gets 40 registers (6 blocks per SM): at 32 the chunk code spills, and the
@@ -218,6 +232,8 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
                                   static_cast<const T *>(sg->val), split_ctas, x, y, ep);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
+    if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax)
+        return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K>, sell_args(sl, n), val, x, y, ep);
     return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y, ep);
 }
 

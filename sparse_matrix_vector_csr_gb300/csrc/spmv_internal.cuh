@@ -22,6 +22,8 @@ constexpr int kMergeIpt = 8;                // path items per thread
 constexpr int kMergeItems = kMergeThreads * kMergeIpt;
 constexpr int kHistCap = 4096;              // row-length histogram: buckets 0..kHistCap-1, last = ">= kHistCap"
 constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows are sorted in one CTA
+constexpr int kShortRow = 8;                 // rows this short on a small matrix: whole-row loads
+constexpr int64_t kShortRowsMax = 152 * 2048;  // "small": fewer row positions than one wave of threads
 constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows
 
 // ----------------------------------------------------------------------------
