@@ -13,6 +13,7 @@ from .generators import (  # noqa: F401
     power_law,
     random_uniform_rows,
     banded_random_rows,
+    convection_diffusion,
     random_csr,
     identity,
     permutation_matrix,

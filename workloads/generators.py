@@ -154,6 +154,31 @@ def laplacian_3d_relabelled(nx: int, ny: int, nz: int, seed: int = 9, dtype=np.f
                f"lap3d_{nx}x{ny}x{nz}_relabelled", {"grid": (nx, ny, nz), "labels": lab})
 
 
+def convection_diffusion(dims, c: float = 0.5, dtype=np.float64) -> CSR:
+    """Upwind convection-diffusion on a Dirichlet grid (1 to 3 dimensions), flow along the
+    first axis: the Laplacian stencil (diagonal 2d, neighbours -1) plus c on the diagonal
+    and -c on the upstream neighbour.  Nonsymmetric, diagonally dominant (an M-matrix).
+    Row r = i0 + n0 (i1 + n1 i2); columns sorted ascending."""
+    dims = tuple(int(d) for d in dims)
+    n = int(np.prod(dims))
+    idx = np.arange(n, dtype=np.int64)
+    coord, rest = [], idx
+    for d in dims:
+        coord.append(rest % d)
+        rest = rest // d
+    strides = np.cumprod((1,) + dims[:-1])
+    offs, masks, vals = [], [], []
+    for a in reversed(range(len(dims))):
+        offs.append(-strides[a]); masks.append(coord[a] > 0); vals.append(-1.0 - (c if a == 0 else 0.0))
+    offs.append(0); masks.append(np.ones(n, bool)); vals.append(2.0 * len(dims) + c)
+    for a in range(len(dims)):
+        offs.append(strides[a]); masks.append(coord[a] < dims[a] - 1); vals.append(-1.0)
+    cols = idx[:, None] + np.array(offs, dtype=np.int64)[None, :]
+    mask = np.stack(masks, axis=1)
+    vfull = np.broadcast_to(np.array(vals)[None, :], cols.shape)
+    return _csr_from_mask(n, cols, mask, vfull, dtype, "convdiff_" + "x".join(map(str, dims)), {"grid": dims, "c": c})
+
+
 # --------------------------------------------------------------------------- #
 # HMEp-shaped
 # --------------------------------------------------------------------------- #
@@ -441,6 +466,8 @@ WORKLOADS = {
     "lap3d_128_relabelled": dict(fn=laplacian_3d_relabelled, kw=dict(nx=128, ny=128, nz=128, seed=9),
                                  dtype=np.float64, seed_x=101,
                                  desc="3D 7-point Laplacian 128^3 with randomly numbered grid points"),
+    "convdiff3d_128": dict(fn=convection_diffusion, kw=dict(dims=(128, 128, 128), c=0.5), dtype=np.float64,
+                           seed_x=101, desc="3D upwind convection-diffusion 128^3 (nonsymmetric), n=2,097,152"),
     "band120_256k": dict(fn=banded_random_rows, kw=dict(n=262_144, per_row=120, half_band=4096, seed=6),
                          dtype=np.float64, seed_x=101,
                          desc="banded random, 120 nnz/row in a band of +-4096, n=262,144"),
@@ -459,6 +486,8 @@ WORKLOADS = {
                            dtype=np.float64, seed_x=101, desc="power law, n=60,001 with 4 dense rows"),
     "lap3d_relabelled_small": dict(fn=laplacian_3d_relabelled, kw=dict(nx=37, ny=29, nz=23, seed=9),
                                    dtype=np.float64, seed_x=101, desc="3D Laplacian 37x29x23, random numbering"),
+    "convdiff_small": dict(fn=convection_diffusion, kw=dict(dims=(41, 33, 19), c=0.5), dtype=np.float64,
+                           seed_x=101, desc="3D convection-diffusion 41x33x19"),
     "band_small": dict(fn=banded_random_rows, kw=dict(n=20_011, per_row=96, half_band=700, seed=8),
                        dtype=np.float64, seed_x=101, desc="banded random 96/row, n=20,011"),
     "uniform16_small": dict(fn=random_uniform_rows, kw=dict(n=100_003, per_row=16, seed=5),
