@@ -575,8 +575,9 @@ def run_multi(args):
 
 
 def run_cg(args):
-    """Conjugate gradients (spmv_cg) on a Laplacian: time per iteration from two fixed-step
-    runs, then one solve to 1e-6; one JSON line per value type."""
+    """Krylov solver on the device (spmv_cg, or spmv_bicgstab with --solver bicgstab): time
+    per iteration from two fixed-step runs, then one solve to 1e-6; one JSON line per value
+    type."""
     import numpy as np
     import torch
 
@@ -593,13 +594,14 @@ def run_cg(args):
         b = torch.from_numpy(b_np).to(dev)
         x = torch.zeros_like(b)
         A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=args.format)
-        A.cg(b, x, rtol=0.0, max_iter=max(args.warmup, 3))
+        solve = A.bicgstab if args.solver == "bicgstab" else A.cg
+        solve(b, x, rtol=0.0, max_iter=max(args.warmup, 3))
 
         def timed(iters):
             x.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            _, it, _ = A.cg(b, x, rtol=0.0, max_iter=iters)
+            _, it, _ = solve(b, x, rtol=0.0, max_iter=iters)
             e1.record()
             torch.cuda.synchronize()
             assert it == iters
@@ -610,14 +612,21 @@ def run_cg(args):
         x.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        _, it, res = A.cg(b, x, rtol=1e-6, max_iter=100000)
+        _, it, res = solve(b, x, rtol=1e-6, max_iter=100000)
         solve_s = time.perf_counter() - t0
-        # algorithmic bytes of one iteration: the product, p.q (2 vectors read), the r
-        # update (q, r read; r written), the x and p updates (p, x, r read; x, p written)
-        bytes_iter = effective_bytes(csr.n, csr.nnz, sv) + 10 * csr.n * sv
-        print(json.dumps({"workload": args.workload, "dtype": "f64" if sv == 8 else "f32", "solver": "cg",
+        # algorithmic bytes of one iteration.  CG: the product, p.q (2 vectors read), the r
+        # update (q, r read; r written), the x and p updates (p, x, r read; x, p written).
+        # BiCGSTAB: two products, p update (4 vectors), r_hat.v (2), s (3), t.s and t.t (2),
+        # x and r updates with r.r and r_hat.r (5 read, 2 written).
+        if args.solver == "bicgstab":
+            bytes_iter = 2 * effective_bytes(csr.n, csr.nnz, sv) + 18 * csr.n * sv
+            launches = 7
+        else:
+            bytes_iter = effective_bytes(csr.n, csr.nnz, sv) + 10 * csr.n * sv
+            launches = 4
+        print(json.dumps({"workload": args.workload, "dtype": "f64" if sv == 8 else "f32", "solver": args.solver,
                           "format": A.describe()["format"], "us_per_iteration": ms_iter * 1e3,
-                          "launches_per_iteration": 4, "bytes_per_iteration": bytes_iter,
+                          "launches_per_iteration": launches, "bytes_per_iteration": bytes_iter,
                           "effective_gbs": bytes_iter / ms_iter / 1e6, "frac": bytes_iter / ms_iter / 1e6 / peak,
                           "peak": f"{peak} GB/s {peak_kind}", "solve_rtol": 1e-6, "solve_iterations": it,
                           "solve_relative_residual": res, "solve_wall_ms": solve_s * 1e3}), flush=True)
@@ -798,7 +807,8 @@ def main(argv=None):
     ap.add_argument("--orderings", action="store_true",
                     help="time the workload in its given numbering and in the row-length / RCM permuted bases")
     ap.add_argument("--cg", type=int, default=0, metavar="ITERS",
-                    help="time conjugate gradients (ITERS fixed steps per run) instead of the bench line")
+                    help="time the Krylov solver (ITERS fixed steps per run) instead of the bench line")
+    ap.add_argument("--solver", choices=["cg", "bicgstab"], default="cg", help="with --cg: which solver")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -265,6 +265,17 @@ SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double rtol, int32
                      int32_t *iterations, double *relative_residual);
 
 /*
+ * Solve A x = b by BiCGSTAB (van der Vorst), unpreconditioned, with the shadow residual
+ * r_hat = r_0: the nonsymmetric Krylov solver the Krylov/AMG paper uses for its 3D
+ * Poisson tests.  Two products per step on this handle plus device vector kernels.
+ * Arguments, stopping rule, arithmetic, workspace (7 vectors) and errors as spmv_cg;
+ * SPMV_ERR_UNSUPPORTED (after filling the outputs) on a breakdown: (r_hat, r) = 0,
+ * (r_hat, A p) = 0, or omega = 0 before convergence.
+ */
+SPMV_API int spmv_bicgstab(spmv_handle_t h, const void *b, void *x, double rtol, int32_t max_iter, void *stream,
+                           int32_t *iterations, double *relative_residual);
+
+/*
  * Orderings of the permuted basis (spmv_build_permuted).  perm maps a position of the
  * basis to an original index (new -> old).
  *   NATURAL     the identity.

@@ -32,6 +32,7 @@ from ._abi import (  # noqa: F401
     spmv_get_layout,
     spmv_get_permutation,
     spmv_build_permuted,
+    spmv_bicgstab,
     spmv_permute_vector,
     spmv_get_slots,
     spmv_last_error,
@@ -136,6 +137,19 @@ class SpmvMatrix:
             x = torch.zeros_like(b)
         self._check_vec(x, "x")
         it, res = spmv_cg(self._h, b, x, rtol, max_iter, stream)
+        return x, it, res
+
+    def bicgstab(self, b, x=None, rtol=1e-8, max_iter=1000, stream=None):
+        """Solve A x = b by BiCGSTAB on the device (any nonsingular A for which it does not
+        break down).  ``x`` is the initial guess (zeros when not given) and is updated in
+        place.  Returns (x, iterations, relative_residual)."""
+        import torch
+
+        self._check_vec(b, "b")
+        if x is None:
+            x = torch.zeros_like(b)
+        self._check_vec(x, "x")
+        it, res = spmv_bicgstab(self._h, b, x, rtol, max_iter, stream)
         return x, it, res
 
     __matmul__ = apply

@@ -212,6 +212,201 @@ __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
     }
 }
 
+// ---------------------------------------------------------------------------
+// BiCGSTAB (van der Vorst), unpreconditioned, shadow residual r_hat = r_0
+// ---------------------------------------------------------------------------
+struct BiScalars {
+    double rho[2];  // (r_hat, r) for the step of matching parity
+    double rv;      // (r_hat, v)
+    double ts, tt;  // (t, s), (t, t)
+    double rr[2];   // (r, r) after the step of matching parity
+    double bb;
+    double alpha, omega;
+};
+
+// Two sums at once: every block stores both of its block sums, the last block adds
+// each in block order.
+__device__ __forceinline__ bool finish_sum2(double a, double b, double *partial, uint32_t *arrivals, double &ta,
+                                            double &tb) {
+    __shared__ bool is_last;
+    if (threadIdx.x == 0) {
+        partial[2 * blockIdx.x] = a;
+        partial[2 * blockIdx.x + 1] = b;
+        __threadfence();
+        is_last = atomicAdd(arrivals, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!is_last) return false;
+    __threadfence();
+    double sa = 0.0, sb = 0.0;
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) {
+        sa += __ldcg(partial + 2 * i);
+        sb += __ldcg(partial + 2 * i + 1);
+    }
+    ta = block_sum(sa);
+    __syncthreads();  // warp_sum is reused
+    tb = block_sum(sb);
+    if (threadIdx.x == 0) *arrivals = 0;
+    return true;
+}
+
+// p = r + beta (p - omega v), beta = (rho_k / rho_{k-1}) (alpha / omega)
+template <typename T, int U>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_bi_p(int64_t units, const BiScalars *sc, Control *ctl, int cur, const Pack<T> *__restrict__ r,
+           const Pack<T> *__restrict__ v, Pack<T> *__restrict__ p) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop) return;
+    const double rho = sc->rho[cur];
+    if (!(rho != 0.0)) {  // (r_hat, r) = 0 (or NaN): breakdown
+        if (blockIdx.x == 0 && threadIdx.x == 0) ctl->stop = 2;
+        return;
+    }
+    const T beta = static_cast<T>((rho / sc->rho[cur ^ 1]) * (sc->alpha / sc->omega));
+    const T omega = static_cast<T>(sc->omega);
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t u0 = gtid(); u0 < units; u0 += U * st) {
+        Pack<T> pr[U], pv[U], pp[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (u0 + k * st < units) pr[k] = r[u0 + k * st], pv[k] = v[u0 + k * st], pp[k] = p[u0 + k * st];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            if (u0 + k * st < units) {
+#pragma unroll
+                for (int l = 0; l < Pack<T>::L; ++l)
+                    pp[k].v[l] = fma(beta, fma(-omega, pv[k].v[l], pp[k].v[l]), pr[k].v[l]);
+                p[u0 + k * st] = pp[k];
+            }
+        }
+    }
+}
+
+// alpha = rho_k / (r_hat, v); s = r - alpha v
+template <typename T, int U>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_bi_s(int64_t units, BiScalars *sc, Control *ctl, int cur, const Pack<T> *__restrict__ r,
+           const Pack<T> *__restrict__ v, Pack<T> *__restrict__ s_out) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop) return;
+    const double rv = sc->rv;
+    if (!(rv != 0.0)) {  // (r_hat, A p) = 0: breakdown
+        if (blockIdx.x == 0 && threadIdx.x == 0) ctl->stop = 2;
+        return;
+    }
+    const double alpha_d = sc->rho[cur] / rv;
+    if (blockIdx.x == 0 && threadIdx.x == 0) sc->alpha = alpha_d;
+    const T alpha = static_cast<T>(alpha_d);
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t u0 = gtid(); u0 < units; u0 += U * st) {
+        Pack<T> pr[U], pv[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (u0 + k * st < units) pr[k] = r[u0 + k * st], pv[k] = v[u0 + k * st];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            if (u0 + k * st < units) {
+#pragma unroll
+                for (int l = 0; l < Pack<T>::L; ++l) pr[k].v[l] = fma(-alpha, pv[k].v[l], pr[k].v[l]);
+                s_out[u0 + k * st] = pr[k];
+            }
+        }
+    }
+}
+
+// (t, s) and (t, t) in one pass
+template <typename T, int U>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_bi_tt(int64_t units, BiScalars *sc, Control *ctl, const Pack<T> *__restrict__ t, const Pack<T> *__restrict__ s,
+            double *__restrict__ partial) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop) return;
+    using A = typename Acc<T>::type;
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    A ts = 0, tt = 0;
+    for (int64_t u0 = gtid(); u0 < units; u0 += U * st) {
+        Pack<T> pt[U], ps[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (u0 + k * st < units) pt[k] = t[u0 + k * st], ps[k] = s[u0 + k * st];
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (u0 + k * st < units)
+#pragma unroll
+                for (int l = 0; l < Pack<T>::L; ++l) {
+                    ts = fma(static_cast<A>(pt[k].v[l]), static_cast<A>(ps[k].v[l]), ts);
+                    tt = fma(static_cast<A>(pt[k].v[l]), static_cast<A>(pt[k].v[l]), tt);
+                }
+    }
+    const double bts = block_sum(static_cast<double>(ts));
+    __syncthreads();  // warp_sum is reused
+    const double btt = block_sum(static_cast<double>(tt));
+    double a, b;
+    if (finish_sum2(bts, btt, partial, &ctl->arrivals, a, b) && threadIdx.x == 0) {
+        sc->ts = a;
+        sc->tt = b;
+    }
+}
+
+// omega = (t, s) / (t, t); x += alpha p + omega s; r = s - omega t; then (r, r), the next
+// rho = (r_hat, r) and the stopping test
+template <typename T, int U>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_bi_xr(int64_t units, BiScalars *sc, Control *ctl, int cur, double stop_rr, const Pack<T> *__restrict__ p,
+            const Pack<T> *__restrict__ s, const Pack<T> *__restrict__ t, const Pack<T> *__restrict__ r_hat,
+            Pack<T> *__restrict__ x, Pack<T> *__restrict__ r, double *__restrict__ partial) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop) return;
+    using A = typename Acc<T>::type;
+    const double tt_d = sc->tt;
+    const double omega_d = tt_d > 0.0 ? sc->ts / tt_d : 0.0;
+    const T alpha = static_cast<T>(sc->alpha), omega = static_cast<T>(omega_d);
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    A rr = 0, rho = 0;
+    for (int64_t u0 = gtid(); u0 < units; u0 += U * st) {
+        Pack<T> pp[U], ps[U], pt[U], px[U], ph[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (u0 + k * st < units) {
+                pp[k] = p[u0 + k * st], ps[k] = s[u0 + k * st], pt[k] = t[u0 + k * st];
+                px[k] = x[u0 + k * st], ph[k] = r_hat[u0 + k * st];
+            }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            if (u0 + k * st < units) {
+#pragma unroll
+                for (int l = 0; l < Pack<T>::L; ++l) {
+                    px[k].v[l] = fma(omega, ps[k].v[l], fma(alpha, pp[k].v[l], px[k].v[l]));
+                    const T rn = fma(-omega, pt[k].v[l], ps[k].v[l]);
+                    ps[k].v[l] = rn;
+                    rr = fma(static_cast<A>(rn), static_cast<A>(rn), rr);
+                    rho = fma(static_cast<A>(ph[k].v[l]), static_cast<A>(rn), rho);
+                }
+                x[u0 + k * st] = px[k];
+                r[u0 + k * st] = ps[k];
+            }
+        }
+    }
+    const double brr = block_sum(static_cast<double>(rr));
+    __syncthreads();  // warp_sum is reused
+    const double brho = block_sum(static_cast<double>(rho));
+    double a, b;
+    if (finish_sum2(brr, brho, partial, &ctl->arrivals, a, b) && threadIdx.x == 0) {
+        sc->rr[cur ^ 1] = a;
+        sc->rho[cur ^ 1] = b;
+        sc->omega = omega_d;
+        ctl->iterations += 1;
+        if (!(a > stop_rr))
+            ctl->stop = 1;             // converged (NaN stops too)
+        else if (omega_d == 0.0)
+            ctl->stop = 2;             // omega = 0 before convergence: breakdown
+    }
+}
+
 template <typename... P, typename... A>
 cudaError_t launch(void (*kernel)(P...), cudaStream_t s, A... args) {
     cudaLaunchAttribute attr[1];
@@ -302,6 +497,84 @@ int cg(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, cudaStr
     return SPMV_OK;
 }
 
+template <typename T>
+int bicgstab(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, cudaStream_t s, int32_t *iterations,
+             double *relative_residual) {
+    constexpr int kUnroll = 2;  // up to five operands a kernel: 2 packs each in flight
+    using P = Pack<T>;
+    const int64_t n = h->n;
+    const size_t vec = static_cast<size_t>(n) * sizeof(T);
+    const size_t vec_pad = (vec + 255) / 256 * 256;
+    const int64_t units = static_cast<int64_t>(vec_pad / sizeof(P));
+    // workspace: r, r_hat, p, v, s, t, x (zero-padded) | 2 x block partials | scalars | control
+    StreamBuffer ws;
+    ws.s = s;
+    const size_t bytes = 7 * vec_pad + 2 * kRedBlocks * sizeof(double) + sizeof(BiScalars) + sizeof(Control);
+    SPMV_TRY_CUDA(cudaMallocAsync(&ws.ptr, bytes, s));
+    SPMV_TRY_CUDA(cudaMemsetAsync(ws.ptr, 0, bytes, s));
+    char *base = static_cast<char *>(ws.ptr);
+    P *r = reinterpret_cast<P *>(base);
+    P *rh = reinterpret_cast<P *>(base + vec_pad);
+    P *p = reinterpret_cast<P *>(base + 2 * vec_pad);
+    P *v = reinterpret_cast<P *>(base + 3 * vec_pad);
+    P *sv = reinterpret_cast<P *>(base + 4 * vec_pad);
+    P *t = reinterpret_cast<P *>(base + 5 * vec_pad);
+    P *xw = reinterpret_cast<P *>(base + 6 * vec_pad);
+    double *partial = reinterpret_cast<double *>(base + 7 * vec_pad);
+    BiScalars *sc = reinterpret_cast<BiScalars *>(partial + 2 * kRedBlocks);
+    Control *ctl = reinterpret_cast<Control *>(sc + 1);
+    const P *cr = r, *crh = rh, *cp = p, *cv = v, *csv = sv, *ct = t;
+
+    // bb = b.b; r = b - A x; r_hat = r; rho_0 = (r_hat, r); rr_0 = (r, r); rho_-1 = alpha = omega = 1
+    SPMV_TRY_CUDA(cudaMemcpyAsync(r, b, vec, cudaMemcpyDeviceToDevice, s));
+    SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, cr, cr, partial, ctl, &sc->bb));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(xw, x, vec, cudaMemcpyDeviceToDevice, s));
+    SPMV_TRY(spmv_apply_ex(h, -1.0, xw, 1.0, r, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(rh, r, vec, cudaMemcpyDeviceToDevice, s));
+    SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, cr, cr, partial, ctl, &sc->rr[0]));
+    SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, crh, cr, partial, ctl, &sc->rho[0]));
+    const double one = 1.0;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&sc->rho[1], &one, sizeof(double), cudaMemcpyHostToDevice, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&sc->alpha, &one, sizeof(double), cudaMemcpyHostToDevice, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&sc->omega, &one, sizeof(double), cudaMemcpyHostToDevice, s));
+    BiScalars hs{};
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&hs, sc, sizeof(hs), cudaMemcpyDeviceToHost, s));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    const double denom = hs.bb > 0.0 ? hs.bb : 1.0;  // b = 0: absolute residual
+    const double stop_rr = rtol * rtol * denom;
+
+    int32_t launched = 0;
+    Control hc{};
+    if (max_iter > 0 && hs.rr[0] > stop_rr) {
+        while (launched < max_iter) {
+            const int32_t block = std::min<int32_t>(kCheckEvery, max_iter - launched);
+            for (int32_t j = 0; j < block; ++j, ++launched) {
+                const int cur = launched & 1;
+                SPMV_TRY_CUDA(launch(k_bi_p<T, kUnroll>, s, units, static_cast<const BiScalars *>(sc), ctl, cur, cr,
+                                     cv, p));
+                SPMV_TRY(spmv_apply(h, p, v, s));
+                SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, crh, cv, partial, ctl, &sc->rv));
+                SPMV_TRY_CUDA(launch(k_bi_s<T, kUnroll>, s, units, sc, ctl, cur, cr, cv, sv));
+                SPMV_TRY(spmv_apply(h, sv, t, s));
+                SPMV_TRY_CUDA(launch(k_bi_tt<T, kUnroll>, s, units, sc, ctl, ct, csv, partial));
+                SPMV_TRY_CUDA(launch(k_bi_xr<T, kUnroll>, s, units, sc, ctl, cur, stop_rr, cp, csv, ct, crh, xw, r,
+                                     partial));
+            }
+            SPMV_TRY_CUDA(cudaMemcpyAsync(&hc, ctl, sizeof(hc), cudaMemcpyDeviceToHost, s));
+            SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+            if (hc.stop) break;
+        }
+        SPMV_TRY_CUDA(cudaMemcpyAsync(x, xw, vec, cudaMemcpyDeviceToDevice, s));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(&hs, sc, sizeof(hs), cudaMemcpyDeviceToHost, s));
+        SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    }
+    const double rr = hs.rr[hc.iterations & 1];
+    if (iterations) *iterations = hc.iterations;
+    if (relative_residual) *relative_residual = std::sqrt(rr / denom);
+    if (hc.stop == 2) return set_error(SPMV_ERR_UNSUPPORTED, "BiCGSTAB broke down (rho, (r_hat, Ap) or omega is 0)");
+    return SPMV_OK;
+}
+
 }  // namespace
 }  // namespace spmv
 
@@ -322,4 +595,21 @@ extern "C" SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double 
                           relative_residual);
     return cg<float>(h, static_cast<const float *>(b), static_cast<float *>(x), rtol, max_iter, s, iterations,
                      relative_residual);
+}
+
+extern "C" SPMV_API int spmv_bicgstab(spmv_handle_t h, const void *b, void *x, double rtol, int32_t max_iter,
+                                      void *stream, int32_t *iterations, double *relative_residual) {
+    if (iterations) *iterations = 0;
+    if (relative_residual) *relative_residual = 0.0;
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (max_iter < 0 || !(rtol >= 0.0)) return set_error(SPMV_ERR_INVALID_ARG, "need max_iter >= 0 and rtol >= 0");
+    if (h->n == 0) return SPMV_OK;
+    if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
+    if (b == x) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not alias");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->dtype == SPMV_F64)
+        return bicgstab<double>(h, static_cast<const double *>(b), static_cast<double *>(x), rtol, max_iter, s,
+                                iterations, relative_residual);
+    return bicgstab<float>(h, static_cast<const float *>(b), static_cast<float *>(x), rtol, max_iter, s, iterations,
+                           relative_residual);
 }
