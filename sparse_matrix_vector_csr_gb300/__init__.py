@@ -58,7 +58,7 @@ class SpmvMatrix:
         """Build from device CSR tensors (int32 row_ptr/col_idx, float64/float32 vals).
 
         ``params``: C, sigma, K, spill_csr, long_row_threshold, subwarp, row_threads,
-        row_group_mode (see spmv.h).  ``ordering`` ("natural", "row_length", "rcm", or an
+        row_group_mode, x_policy, vector_loads, host_blocks (see spmv.h).  ``ordering`` ("natural", "row_length", "rcm", or an
         int32 CUDA tensor holding a permutation): build B = P A P^T and work in that
         permuted basis (see ``to_basis`` / ``from_basis``).
         """

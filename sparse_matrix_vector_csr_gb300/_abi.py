@@ -52,6 +52,7 @@ class FormatParams(ctypes.Structure):
         ("row_group_mode", ctypes.c_int32),
         ("x_policy", ctypes.c_int32),
         ("vector_loads", ctypes.c_int32),
+        ("host_blocks", ctypes.c_int32),
     ]
 
 
@@ -165,13 +166,14 @@ def dtype_code(dtype) -> int:
 
 
 def make_params(C=-1, sigma=-1, K=-1, spill_csr=-1, long_row_threshold=-1, subwarp=-1, row_threads=-1,
-                row_group_mode=-1, x_policy=-1, vector_loads=-1) -> FormatParams:
+                row_group_mode=-1, x_policy=-1, vector_loads=-1, host_blocks=-1) -> FormatParams:
     p = FormatParams()
     lib.spmv_default_params(ctypes.byref(p))
     p.C, p.sigma, p.K = int(C), int(sigma), int(K)
     p.spill_csr, p.long_row_threshold, p.subwarp = int(spill_csr), int(long_row_threshold), int(subwarp)
     p.row_threads, p.row_group_mode, p.x_policy = int(row_threads), int(row_group_mode), int(x_policy)
     p.vector_loads = int(vector_loads)
+    p.host_blocks = int(host_blocks)
     return p
 
 

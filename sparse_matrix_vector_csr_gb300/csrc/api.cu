@@ -727,6 +727,9 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     h->params.row_threads = c.group;
     h->params.row_group_mode = c.group_mode;
     h->params.vector_loads = c.vec ? 1 : 0;
+    if (prm.host_blocks > kMaxHostBlocks)
+        return set_error(SPMV_ERR_INVALID_ARG, "host_blocks must be at most " + std::to_string(kMaxHostBlocks));
+    h->params.host_blocks = prm.host_blocks <= 1 ? 0 : prm.host_blocks;
 
     switch (format) {
         case SPMV_FMT_CSR_VECTOR: {
@@ -795,6 +798,9 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
 
 void free_handle(spmv_handle_t h) {
     if (!h) return;
+    for (cudaEvent_t e : h->host_events) cudaEventDestroy(e);
+    if (h->host_in) cudaStreamDestroy(h->host_in);
+    if (h->host_out) cudaStreamDestroy(h->host_out);
     for (void *p : h->allocations) cudaFree(p);
     delete h;
 }
@@ -947,6 +953,146 @@ void append(std::string &out, const char *fmt, ...) {
     out += buf;
 }
 
+// ---------------------------------------------------------------------------
+// spmv_apply_host pipeline
+// ---------------------------------------------------------------------------
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+bool page_locked(const void *p) {
+    cudaPointerAttributes attr;
+    const bool ok = cudaPointerGetAttributes(&attr, p) == cudaSuccess && attr.type == cudaMemoryTypeHost;
+    (void)cudaGetLastError();
+    return ok;
+}
+
+// The rows at sorted positions [p0, p1) as a sliced part of their own (one thread per
+// row, column-major slots).  SELL: p0 is a multiple of C, so the view starts at slice
+// p0 / C.  One-slice ELL: slot = slice start + j * ld + position, so the view moves the
+// slot arrays by p0 instead.  Launched without programmatic dependent launch: its
+// start waits on an event of the copy stream.
+Sliced sliced_view(const Sliced &sl, int dtype, int64_t p0, int64_t p1) {
+    Sliced v = sl;
+    v.n_pos = p1 - p0;
+    v.len = sl.len + p0;
+    if (sl.perm) v.perm = sl.perm + p0;
+    if (sl.log2C < 31) {
+        v.slice_ptr = sl.slice_ptr + (p0 >> sl.log2C);
+    } else {
+        v.col = sl.col + p0;
+        v.val = static_cast<char *>(sl.val) + p0 * static_cast<int64_t>(value_bytes(dtype));
+    }
+    v.pdl = false;
+    return v;
+}
+
+// Decides, on the first spmv_apply_host call of a handle, whether its calls run
+// pipelined, and prepares the blocks, streams and events (host_pipe = 1), or not
+// (host_pipe = -1).  Synchronises s once (the column reach goes to the host).
+// Off unless host_blocks asks for it.  On a host link where every copy carries about
+// 8 us of fixed latency and each direction drops to about 154 GB/s while the other is
+// busy, the pipeline can hide little more than the product's own time.
+int host_pipe_setup(spmv_handle_t h, cudaStream_t s) {
+    h->host_pipe = -1;
+    const Sliced &sl = h->sliced;
+    const int req = h->params.host_blocks;
+    if (req <= 0 || h->n == 0) return SPMV_OK;
+    if (!sl.present || !fused_epilogue(h) || h->seg.kind != 0 || sl.group != 1 || sl.vec || sl.interleaved)
+        return SPMV_OK;
+    // blocks are whole slices (whole warps for ELL) and, when rows are sorted, whole
+    // sort windows, so a block's rows are exactly the rows [p0, p1)
+    int64_t unit = sl.log2C < 31 ? sl.C : 32;
+    if (sl.perm) {  // sorted within windows of min(sigma, n) rows starting at row 0
+        const int64_t w = std::min<int64_t>(sl.sigma, h->n);
+        if (w <= 0 || w >= h->n) return SPMV_OK;
+        unit = unit / gcd64(unit, w) * w;
+        if (unit >= sl.n_pos) return SPMV_OK;
+    }
+    const int64_t block = ceil_div(ceil_div(sl.n_pos, req), unit) * unit;
+    const int64_t nb = ceil_div(sl.n_pos, block);
+    if (nb < 2) return SPMV_OK;
+
+    void *d_max = nullptr;
+    SPMV_TRY(dev_alloc(h, &d_max, static_cast<size_t>(nb) * sizeof(int32_t)));
+    SPMV_TRY_CUDA(cudaMemsetAsync(d_max, 0xff, static_cast<size_t>(nb) * sizeof(int32_t), s));
+    SPMV_TRY_CUDA(launch_block_max_col(sl, block, static_cast<int32_t *>(d_max), s));
+    std::vector<int32_t> reach(static_cast<size_t>(nb));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(reach.data(), d_max, reach.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    std::vector<int32_t> need(reach.size());
+    for (size_t b = 0; b < reach.size(); ++b)  // pieces of x share the blocks' boundaries
+        need[b] = reach[b] < 0 ? -1 : static_cast<int32_t>(reach[b] / block);
+
+    if (!h->host_in) SPMV_TRY_CUDA(cudaStreamCreateWithFlags(&h->host_in, cudaStreamNonBlocking));
+    if (!h->host_out) SPMV_TRY_CUDA(cudaStreamCreateWithFlags(&h->host_out, cudaStreamNonBlocking));
+    while (h->host_events.size() < static_cast<size_t>(2 * nb + 3)) {
+        cudaEvent_t e;
+        SPMV_TRY_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        h->host_events.push_back(e);
+    }
+    h->host_block = block;
+    h->host_need = std::move(need);
+    h->host_pipe = 1;
+    return SPMV_OK;
+}
+
+// One pipelined spmv_apply_host: x in by pieces on host_in, block b on s once piece
+// need[b] is in (pieces arrive in order), its rows of y out on host_out; s waits for
+// both copy streams and is synchronised.  Events: [0, nb) pieces of x in, [nb, 2 nb)
+// blocks done, 2 nb start, 2 nb + 1 all of x in, 2 nb + 2 all of y out.  (Blocks that
+// store y straight into the page-locked y_host instead measured slower: those stores
+// overlap the incoming copies less than a second copy engine does.)
+int apply_host_pipelined(spmv_handle_t h, const void *x_host, void *y_host, cudaStream_t s) {
+    const Sliced &sl = h->sliced;
+    const int64_t vb = static_cast<int64_t>(value_bytes(h->dtype));
+    const int64_t n = h->n, block = h->host_block;
+    const int64_t nb = static_cast<int64_t>(h->host_need.size());
+    cudaEvent_t *ev = h->host_events.data();
+    const char *xh = static_cast<const char *>(x_host);
+    char *yh = static_cast<char *>(y_host);
+    char *xs = static_cast<char *>(h->x_stage);
+    char *ys = static_cast<char *>(h->y_stage);
+    SPMV_TRY_CUDA(cudaEventRecord(ev[2 * nb], s));
+    SPMV_TRY_CUDA(cudaStreamWaitEvent(h->host_in, ev[2 * nb], 0));
+    SPMV_TRY_CUDA(cudaStreamWaitEvent(h->host_out, ev[2 * nb], 0));
+    for (int64_t c = 0; c < nb; ++c) {
+        const int64_t r0 = c * block, r1 = std::min(n, r0 + block);
+        if (r1 > r0)
+            SPMV_TRY_CUDA(cudaMemcpyAsync(xs + r0 * vb, xh + r0 * vb, static_cast<size_t>((r1 - r0) * vb),
+                                          cudaMemcpyHostToDevice, h->host_in));
+        SPMV_TRY_CUDA(cudaEventRecord(ev[c], h->host_in));
+    }
+    SPMV_TRY_CUDA(cudaEventRecord(ev[2 * nb + 1], h->host_in));
+    for (int64_t b = 0; b < nb; ++b) {
+        const int64_t p0 = b * block, p1 = std::min(sl.n_pos, p0 + block);
+        const int32_t need = h->host_need[static_cast<size_t>(b)];
+        if (need >= 0) SPMV_TRY_CUDA(cudaStreamWaitEvent(s, ev[need], 0));
+        const Sliced v = sliced_view(sl, h->dtype, p0, p1);
+        // natural order: the view's position p is row p0 + p; sorted: perm gives the row
+        if (sl.perm)
+            SPMV_TRY_CUDA(launch_sell_apply(h->dtype, v, n, nullptr, xs, ys, s, nullptr));
+        else
+            SPMV_TRY_CUDA(launch_sell_apply(h->dtype, v, n - p0, nullptr, xs, ys + p0 * vb, s, nullptr));
+        SPMV_TRY_CUDA(cudaEventRecord(ev[nb + b], s));
+        SPMV_TRY_CUDA(cudaStreamWaitEvent(h->host_out, ev[nb + b], 0));
+        const int64_t r1 = std::min(n, p1);
+        if (r1 > p0)
+            SPMV_TRY_CUDA(cudaMemcpyAsync(yh + p0 * vb, ys + p0 * vb, static_cast<size_t>((r1 - p0) * vb),
+                                          cudaMemcpyDeviceToHost, h->host_out));
+    }
+    SPMV_TRY_CUDA(cudaEventRecord(ev[2 * nb + 2], h->host_out));
+    SPMV_TRY_CUDA(cudaStreamWaitEvent(s, ev[2 * nb + 1], 0));
+    SPMV_TRY_CUDA(cudaStreamWaitEvent(s, ev[2 * nb + 2], 0));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    return SPMV_OK;
+}
+
 }  // namespace
 }  // namespace spmv
 
@@ -966,6 +1112,7 @@ int spmv_default_params(spmv_format_params *p) {
     p->row_group_mode = -1;
     p->x_policy = -1;
     p->vector_loads = -1;
+    p->host_blocks = -1;
     return SPMV_OK;
 }
 
@@ -1085,6 +1232,13 @@ int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *str
     const size_t bytes = static_cast<size_t>(h->n) * value_bytes(h->dtype);
     if (!h->x_stage) SPMV_TRY(dev_alloc(h, &h->x_stage, bytes));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->host_pipe == 0) SPMV_TRY(host_pipe_setup(h, s));
+    if (h->host_pipe == 1 && page_locked(x_host) && page_locked(y_host)) {
+        if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
+        h->host_last_blocks = static_cast<int>(h->host_need.size());
+        return apply_host_pipelined(h, x_host, y_host, s);
+    }
+    h->host_last_blocks = 0;
     SPMV_TRY_CUDA(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
     // A plan that writes every row of y exactly once (one sliced launch, no accumulating
     // pass) stores y straight into page-locked host memory: the transfer back then runs
@@ -1310,6 +1464,9 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
            sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,
            (long long)sl.stored_entries, (long long)sl.ld, sl.max_width, sl.perm ? "true" : "false");
     append(o, "\"x_evict_last\":%s,", sl.keep_x ? "true" : "false");
+    // host_blocks: the parameter (0 = off); host_pipeline_blocks: blocks of the last
+    // spmv_apply_host call (0 = unpipelined, -1 = no call yet)
+    append(o, "\"host_blocks\":%d,\"host_pipeline_blocks\":%d,", h->params.host_blocks, h->host_last_blocks);
     append(o, "\"ordering\":\"%s\",\"permuted_basis\":%s,", ordering_name(h->ordering),
            h->basis_perm ? "true" : "false");
     append(o, "\"n_long_rows\":%lld,\"long_nnz\":%lld,", (long long)h->n_long_rows, (long long)h->long_nnz);

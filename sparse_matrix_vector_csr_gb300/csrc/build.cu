@@ -551,6 +551,27 @@ __global__ void k_segment_to_csr(int64_t m, const int32_t *__restrict__ rows, co
     }
 }
 
+// ---------------------------------------------------------------------------
+// column reach of blocks of rows (the spmv_apply_host pipeline)
+// ---------------------------------------------------------------------------
+// One thread per sorted position walks its row's column-major slots; a warp's 32
+// positions lie in one block (block is a multiple of 32), so a warp maximum and one
+// atomic per warp give the block's largest column.
+__global__ void k_block_max_col(int64_t n_pos, int log2C, uint32_t cmask, int64_t stride,
+                                const int64_t *__restrict__ slice_ptr, const int32_t *__restrict__ len,
+                                const int32_t *__restrict__ col, int64_t block, int32_t *__restrict__ out) {
+    const int64_t p = gtid();
+    int32_t m = -1;
+    if (p < n_pos) {
+        const int32_t w = len[p];
+        const int64_t base = slice_ptr[p >> log2C] + (p & cmask);
+        for (int32_t j = 0; j < w; ++j) m = max(m, col[base + j * stride]);
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0 && m >= 0 && p < n_pos) atomicMax(out + p / block, m);
+}
+
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -749,6 +770,14 @@ cudaError_t launch_segment_to_csr(int dtype, const Segmented &sg, const int32_t 
         k_segment_to_csr<float><<<g, kBlock, 0, s>>>(sg.n_rows, sg.rows, sg.ptr, sg.col,
                                                      static_cast<const float *>(sg.val), sg.dst_offset, out_ptr,
                                                      out_col, static_cast<float *>(out_val));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_max_col(const Sliced &sl, int64_t block, int32_t *out, cudaStream_t s) {
+    if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
+    if (block <= 0 || block % 32 != 0 || sl.group != 1 || sl.interleaved || sl.vec) return cudaErrorInvalidValue;
+    k_block_max_col<<<grid_for(sl.n_pos, kBlock, INT_MAX), kBlock, 0, s>>>(sl.n_pos, sl.log2C, sl.cmask, sl.stride,
+                                                                          sl.slice_ptr, sl.len, sl.col, block, out);
     return cudaGetLastError();
 }
 

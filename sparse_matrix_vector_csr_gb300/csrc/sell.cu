@@ -218,7 +218,7 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
     const int64_t sell_ctas = ceil_div(sl.n_pos, kSellBlock);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = sl.pdl ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kSellBlock);
     cfg.dynamicSmemBytes = 0;

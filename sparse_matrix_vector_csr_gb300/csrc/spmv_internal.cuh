@@ -25,6 +25,7 @@ constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows
 constexpr int kShortRow = 8;                 // rows this short on a small matrix: whole-row loads
 constexpr int64_t kShortRowsMax = 152 * 2048;  // "small": fewer row positions than one wave of threads
 constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows
+constexpr int kMaxHostBlocks = 1024;         // row blocks of the spmv_apply_host pipeline, at most
 
 // ----------------------------------------------------------------------------
 // format parts
@@ -56,6 +57,8 @@ struct Sliced {
     bool vec = false;              // one thread per row reading 16-byte vectors of its row
     int log2k_col = 0;             // interleaved slots: index groups of 2^log2k_col
     int log2k_val = 0;             //                    value groups of 2^log2k_val
+    bool pdl = true;               // launch with programmatic dependent launch (off for views
+                                   // whose start waits on an event of another stream)
     int64_t *slice_ptr = nullptr;  // [n_slices + 1]
     int32_t *width = nullptr;      // [n_slices]
     int32_t *len = nullptr;        // [n_pos] entries stored at each position
@@ -144,6 +147,16 @@ struct spmv_handle_s {
     // spmv_apply_host staging
     void *x_stage = nullptr;
     void *y_stage = nullptr;
+    // spmv_apply_host pipeline: decided by the first call (0 = not yet, 1 = pipelined,
+    // -1 = not pipelined); row positions per block; for every block, the last piece of x
+    // its columns reach (-1 = the block has no entries); copy streams and events
+    int host_pipe = 0;
+    int64_t host_block = 0;
+    std::vector<int32_t> host_need;
+    int host_last_blocks = -1;  // blocks of the last spmv_apply_host call (0 = unpipelined)
+    cudaStream_t host_in = nullptr;
+    cudaStream_t host_out = nullptr;
+    std::vector<cudaEvent_t> host_events;
     // one column of x and of y, for scaled / multi-vector applies without a fused path
     void *tmp_x = nullptr;
     void *tmp_y = nullptr;
@@ -288,6 +301,12 @@ cudaError_t launch_permute_vector(int dtype, int64_t n, const int32_t *perm, con
 
 // One thread per row with 16-byte vector loads (sellv.cu, sl.vec); long rows are left to
 // launch_rowsplit.
+// out[b] = the largest column index stored in the rows at sorted positions
+// [b * block, (b + 1) * block) of a one-thread-per-row, column-major sliced layout
+// (out must hold -1 on entry; it stays -1 for a block without entries).  block is a
+// multiple of 32 and of the slice height.
+cudaError_t launch_block_max_col(const Sliced &sl, int64_t block, int32_t *out, cudaStream_t s);
+
 cudaError_t launch_sellv_apply(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, cudaStream_t s,
                                const Scale *scale = nullptr);
 // G = sl.group threads per row (sellg.cu); long rows (len = -1) are left to launch_rowsplit.
