@@ -101,3 +101,26 @@ def test_product_and_oracle_share_nothing():
     csrc = os.path.join(PKG, "csrc")
     for f in os.listdir(csrc):
         assert "oracle" not in open(os.path.join(csrc, f)).read().lower()
+
+
+def test_params_struct_layout_matches_header(tmp_path):
+    """The binding's spmv_format_params has the C struct's size and field offsets (gcc
+    compiles the header and prints them), and spmv_default_params fills every field with
+    -1 (automatic)."""
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    fields = [f for f, _ in spmv._abi.FormatParams._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "spmv.h"\nint main(void) {\n'
+                   '  printf("size %zu\\n", sizeof(spmv_format_params));\n'
+                   + "".join(f'  printf("{f} %zu\\n", offsetof(spmv_format_params, {f}));\n' for f in fields)
+                   + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(ln.split() for ln in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                    check=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(spmv._abi.FormatParams)
+    for f in fields:
+        assert int(got[f]) == getattr(spmv._abi.FormatParams, f).offset, f
+    p = spmv.spmv_default_params()
+    assert all(getattr(p, f) == -1 for f in fields), {f: getattr(p, f) for f in fields}
