@@ -1,8 +1,10 @@
 """Randomised plans: seeded random matrices (sizes across several tiles with ragged
 tails, empty and full rows, duplicates, unsorted rows, a few long rows) built with
-random formats and parameters, in both value types, against the oracle: the product
-within the per-row tolerance, the round trip to CSR array for array, and y = alpha A x +
-beta y.  Every case is seeded, so a failure names a reproducible configuration."""
+random formats and parameters (threads per row and their mode, vector loads, the x
+cache policy, row blocks of the pipelined host path), in both value types, against the
+oracle: the product within the per-row tolerance, the round trip to CSR array for
+array, y = alpha A x + beta y, and the host-array apply bit for bit equal to the device
+apply.  Every case is seeded, so a failure names a reproducible configuration."""
 import numpy as np
 import pytest
 
@@ -23,6 +25,12 @@ def random_plan(rng):
         g = int(rng.choice([1, 2, 4, 8, 16, 32]))
         p["row_threads"] = g
         p["row_group_mode"] = int(rng.choice([0, 1, 2] if g <= 8 else [0, 1]))
+    elif fmt in ("sell", "ell_r", "hyb") and rng.random() < 0.6:
+        p["vector_loads"] = 1
+    if fmt in ("sell", "ell_r", "hyb") and rng.random() < 0.3:
+        p["x_policy"] = int(rng.integers(0, 2))
+    if fmt in ("sell", "ell_r") and rng.random() < 0.7:
+        p["host_blocks"] = int(rng.choice([2, 3, 5, 16]))
     if fmt in ("sell", "ell_r", "csr_vector") and rng.random() < 0.5:
         p["long_row_threshold"] = int(rng.choice([0, 4, 16, 100]))
     if fmt == "csr_vector" and rng.random() < 0.4:
@@ -51,7 +59,7 @@ def random_matrix(rng, seed):
     return csr
 
 
-@pytest.mark.parametrize("seed", range(120))
+@pytest.mark.parametrize("seed", range(160))
 def test_random_plan(seed):
     torch = torch_cuda()
     rng = np.random.default_rng(1000 + seed)
@@ -74,3 +82,7 @@ def test_random_plan(seed):
         A.apply(xd, yd, alpha=alpha, beta=beta)
         torch.cuda.synchronize()
         assert_parity(yd.cpu().numpy(), oracle.spmv_scaled(csr, x, alpha, beta, y0), dtype, label=label + " scaled")
+        xh = torch.from_numpy(x).pin_memory()
+        yh = torch.full_like(xh, float("nan")).pin_memory()
+        A.apply_host(xh.numpy(), yh.numpy())
+        assert np.array_equal(yh.numpy().view(np.uint8), y.cpu().numpy().view(np.uint8)), label + " host"
