@@ -190,7 +190,8 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
 /*
  * y = A x, overwriting y (no scaling, no accumulation into the old y).
  * x and y are device arrays of n elements of the handle's value type, in the
- * caller's original row order (any row permutation of the format is internal).
+ * caller's original row order (any row permutation of the format is internal);
+ * overlapping x and y are refused with SPMV_ERR_INVALID_ARG.
  * Asynchronous on `stream`: returns after enqueueing 1 to 4 kernel launches.
  * The handle holds a small scratch array for the merge-path pass, so two applies
  * of the SAME handle must not run concurrently (on different streams); applies of
@@ -212,7 +213,8 @@ SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
  *    into it, so the transfer back overlaps the product;
  *  - staged: x copied in, product, y copied out.
  * The result is the same in every way (the same kernel sums each row in the same
- * order).  The device staging buffers, streams and events are created by the first
+ * order).  x_host and y_host may be the same array (in place); such a call runs
+ * unpipelined, with all of x on the device before any of y moves.  The device staging buffers, streams and events are created by the first
  * call on a handle and kept until spmv_destroy.
  */
 SPMV_API int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *stream);
@@ -223,7 +225,8 @@ SPMV_API int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, 
  * copy.  On a GPU attached to its CPU by a coherent link (Grace + Blackwell over
  * NVLink-C2C) the gathers of x and the stores of y cross the link while the matrix
  * streams from HBM, instead of two copy-engine transfers around the product.  Waits
- * for the stream.  SPMV_ERR_INVALID_ARG if either array is not page-locked host memory.
+ * for the stream.  SPMV_ERR_INVALID_ARG if either array is not page-locked host memory or
+ * the two overlap.
  */
 SPMV_API int spmv_apply_mapped(spmv_handle_t h, const void *x_host, void *y_host, void *stream);
 
@@ -243,7 +246,8 @@ SPMV_API int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *
  * Krylov iterations of the Krylov/AMG paper (BiCGSTAB algorithm) combine SpMV with
  * vector updates.  SELL and ELLPACK-R handles fold alpha and beta into the kernel's
  * single write of each row; the other formats compute A x into a scratch column of
- * the handle first.  Asynchronous; same stream rules as spmv_apply.
+ * the handle first.  x and y must not overlap.  Asynchronous; same stream rules as
+ * spmv_apply.
  */
 SPMV_API int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double beta, void *y, void *stream);
 
@@ -255,7 +259,8 @@ SPMV_API int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double 
  * one or two wide loads (SELL handles, slice height 32 or 64; X aligned to
  * min(16, 8 * value size) bytes with ldx a multiple of that); other formats and
  * left-over columns go one column at a time through scratch columns of the handle.
- * beta == 0: Y is not read.  k = 0 is a no-op.  Asynchronous.
+ * beta == 0: Y is not read.  k = 0 is a no-op.  X and Y must not overlap (their spans
+ * of (n - 1) * ld + k elements; SPMV_ERR_INVALID_ARG otherwise).  Asynchronous.
  */
 SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, int64_t ldx, double beta,
                               void *Y, int64_t ldy, void *stream);

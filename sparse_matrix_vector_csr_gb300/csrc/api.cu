@@ -965,6 +965,17 @@ int64_t gcd64(int64_t a, int64_t b) {
     return a;
 }
 
+// [a, a + abytes) and [b, b + bbytes) share a byte
+bool spans_overlap(const void *a, size_t abytes, const void *b, size_t bbytes) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + bbytes && pb < pa + abytes;
+}
+
+bool vectors_alias(spmv_handle_t h, const void *x, const void *y) {
+    const size_t bytes = static_cast<size_t>(h->n) * value_bytes(h->dtype);
+    return spans_overlap(x, bytes, y, bytes);
+}
+
 bool page_locked(const void *p) {
     cudaPointerAttributes attr;
     const bool ok = cudaPointerGetAttributes(&attr, p) == cudaSuccess && attr.type == cudaMemoryTypeHost;
@@ -1220,6 +1231,7 @@ int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream) {
     if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
     if (h->n == 0) return SPMV_OK;
     if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    if (vectors_alias(h, x, y)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
     SPMV_TRY(check_current_device(h));
     return enqueue(h, x, y, static_cast<cudaStream_t>(stream), nullptr);
 }
@@ -1233,7 +1245,8 @@ int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *str
     if (!h->x_stage) SPMV_TRY(dev_alloc(h, &h->x_stage, bytes));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->host_pipe == 0) SPMV_TRY(host_pipe_setup(h, s));
-    if (h->host_pipe == 1 && page_locked(x_host) && page_locked(y_host)) {
+    // in place (x_host and y_host overlapping): unpipelined, where all of x is in before y moves
+    if (h->host_pipe == 1 && page_locked(x_host) && page_locked(y_host) && !vectors_alias(h, x_host, y_host)) {
         if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
         h->host_last_blocks = static_cast<int>(h->host_need.size());
         return apply_host_pipelined(h, x_host, y_host, s);
@@ -1279,6 +1292,7 @@ int spmv_apply_mapped(spmv_handle_t h, const void *x_host, void *y_host, void *s
     if (!x_host || !y_host) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
     SPMV_TRY(check_current_device(h));
     void *xd = nullptr, *yd = nullptr;
+    if (vectors_alias(h, x_host, y_host)) return set_error(SPMV_ERR_INVALID_ARG, "x_host and y_host overlap");
     SPMV_TRY(mapped_pointer(x_host, "x_host", &xd));
     SPMV_TRY(mapped_pointer(y_host, "y_host", &yd));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1291,6 +1305,7 @@ int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, f
     if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
     if (h->n == 0) return 0;
     if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    if (vectors_alias(h, x, y)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
     SPMV_TRY(check_current_device(h));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Recorder rec;
@@ -1309,6 +1324,7 @@ int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double beta, voi
     if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
     if (h->n == 0) return SPMV_OK;
     if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
+    if (vectors_alias(h, x, y)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
     SPMV_TRY(check_current_device(h));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (alpha == 1.0 && beta == 0.0) return enqueue(h, x, y, s, nullptr);
@@ -1322,6 +1338,12 @@ int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, in
     if (k < 0 || ldx < k || ldy < k) return set_error(SPMV_ERR_INVALID_ARG, "need 0 <= k <= ldx and k <= ldy");
     if (h->n == 0 || k == 0) return SPMV_OK;
     if (!X || !Y) return set_error(SPMV_ERR_INVALID_ARG, "NULL X or Y");
+    {
+        const size_t vb0 = value_bytes(h->dtype);
+        const size_t xspan = static_cast<size_t>((h->n - 1) * ldx + k) * vb0;
+        const size_t yspan = static_cast<size_t>((h->n - 1) * ldy + k) * vb0;
+        if (spans_overlap(X, xspan, Y, yspan)) return set_error(SPMV_ERR_INVALID_ARG, "X and Y overlap");
+    }
     SPMV_TRY(check_current_device(h));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (k == 1 && ldx == 1 && ldy == 1) return spmv_apply_ex(h, alpha, X, beta, Y, stream);  // contiguous vectors

@@ -151,3 +151,36 @@ def test_pipeline_at_size_and_default_off():
         d = A.describe()
         assert d["host_blocks"] == 0 and d["host_pipeline_blocks"] == 0
         assert np.array_equal(y0.view(np.uint8), y.view(np.uint8))
+
+
+def test_overlapping_vectors():
+    """Overlapping x and y are refused by the device and mapped entry points; the host
+    path computes in place (unpipelined even with host_blocks set)."""
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    torch = torch_cuda()
+    csr, x = make_workload("lap3d_small")
+    ref = oracle.spmv(csr, x)
+    with build(csr, "sell", host_blocks=4) as A:
+        xd = torch.from_numpy(x).cuda()
+        for y in (xd, xd[1:]):  # the same array, and one shifted by an element
+            with pytest.raises(spmv.SpmvError) as ei:
+                spmv.spmv_apply(A._h, xd, y)
+            assert ei.value.status == -1
+        with pytest.raises(spmv.SpmvError):
+            spmv.spmv_apply_ex(A._h, 2.0, xd, 1.0, xd)
+        X = torch.zeros(csr.n, 4, dtype=xd.dtype, device="cuda")
+        with pytest.raises(spmv.SpmvError):
+            spmv.spmv_apply_multi(A._h, 2, 1.0, X, 4, 0.0, X[:, 2:], 4)
+        Y = torch.zeros_like(X)
+        spmv.spmv_apply_multi(A._h, 2, 1.0, X, 4, 0.0, Y, 4)  # disjoint: accepted
+        xt = torch.from_numpy(x).pin_memory()
+        with pytest.raises(spmv.SpmvError):
+            spmv.spmv_apply_mapped(A._h, xt, xt)
+        buf = xt.clone().pin_memory()
+        A.apply_host(buf.numpy(), buf.numpy())  # in place
+        assert A.describe()["host_pipeline_blocks"] == 0
+        assert_parity(buf.numpy(), ref, csr.dtype, label="in place")
+        y = host_apply(A, x)
+        assert A.describe()["host_pipeline_blocks"] == 4
+        assert np.array_equal(y.view(np.uint8), buf.numpy().view(np.uint8))
