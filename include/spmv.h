@@ -273,7 +273,7 @@ SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const vo
  *
  *   b     device vector, length n, the handle's value type; read only.
  *   x     device vector, length n: the initial guess on entry, the iterate on return.
- *         Must not alias b.
+ *         Must not overlap b.
  *   rtol  stop at the first iteration k with ||r_k||_2 <= rtol * ||b||_2, where r_k is
  *         the recurrence residual (||b|| is replaced by 1 when b = 0).  rtol = 0 runs
  *         exactly max_iter iterations unless the residual reaches 0.
@@ -282,11 +282,12 @@ SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const vo
  *         ||r_k|| / ||b|| at the end.
  *
  * Arithmetic: vectors in the value type; every dot product and the step lengths in
- * double, reduced in a fixed order (results are reproducible).  Workspace (3 vectors)
- * is taken from the stream-ordered pool of `stream` and returned before the call ends.
+ * double, reduced in a fixed order (results are reproducible).  Workspace (4 vectors:
+ * r, p, A p and the iterate) is taken from the stream-ordered pool of `stream` and
+ * returned before the call ends.
  * Synchronises `stream`.  Returns SPMV_ERR_UNSUPPORTED (after filling the outputs) if
  * p.Ap <= 0 at some step, i.e. A is not positive definite; SPMV_ERR_INVALID_ARG for a
- * NULL handle or vector, aliasing, max_iter < 0 or rtol < 0 / NaN.
+ * NULL handle or vector, overlapping b and x, max_iter < 0 or rtol < 0 / NaN.
  */
 SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double rtol, int32_t max_iter, void *stream,
                      int32_t *iterations, double *relative_residual);
@@ -349,7 +350,7 @@ SPMV_API int spmv_get_permutation(spmv_handle_t h, int32_t *perm, void *stream);
 /*
  * Move a vector between the original basis and the handle's: direction 0 (into the
  * basis) dst[i] = src[perm[i]]; direction 1 (back) dst[perm[i]] = src[i].  src and dst
- * are device arrays of n values of the handle's type and must not alias.  Asynchronous.
+ * are device arrays of n values of the handle's type and must not overlap.  Asynchronous.
  */
 SPMV_API int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int direction, void *stream);
 

@@ -1216,7 +1216,7 @@ int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int directi
     if (direction != 0 && direction != 1) return set_error(SPMV_ERR_INVALID_ARG, "direction must be 0 or 1");
     if (h->n == 0) return SPMV_OK;
     if (!src || !dst) return set_error(SPMV_ERR_INVALID_ARG, "NULL src or dst");
-    if (src == dst) return set_error(SPMV_ERR_INVALID_ARG, "src and dst must not alias");
+    if (vectors_alias(h, src, dst)) return set_error(SPMV_ERR_INVALID_ARG, "src and dst must not overlap");
     SPMV_TRY(check_current_device(h));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!h->basis_perm) {

@@ -580,6 +580,15 @@ int bicgstab(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, c
 
 using namespace spmv;
 
+namespace {
+// two vectors of the handle's n values share a byte
+bool overlapping(spmv_handle_t h, const void *a, const void *b) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    const uintptr_t bytes = static_cast<uintptr_t>(h->n) * value_bytes(h->dtype);
+    return pa < pb + bytes && pb < pa + bytes;
+}
+}  // namespace
+
 extern "C" SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double rtol, int32_t max_iter,
                                 void *stream, int32_t *iterations, double *relative_residual) {
     if (iterations) *iterations = 0;
@@ -588,7 +597,7 @@ extern "C" SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double 
     if (max_iter < 0 || !(rtol >= 0.0)) return set_error(SPMV_ERR_INVALID_ARG, "need max_iter >= 0 and rtol >= 0");
     if (h->n == 0) return SPMV_OK;
     if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
-    if (b == x) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not alias");
+    if (overlapping(h, b, x)) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not overlap");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->dtype == SPMV_F64)
         return cg<double>(h, static_cast<const double *>(b), static_cast<double *>(x), rtol, max_iter, s, iterations,
@@ -605,7 +614,7 @@ extern "C" SPMV_API int spmv_bicgstab(spmv_handle_t h, const void *b, void *x, d
     if (max_iter < 0 || !(rtol >= 0.0)) return set_error(SPMV_ERR_INVALID_ARG, "need max_iter >= 0 and rtol >= 0");
     if (h->n == 0) return SPMV_OK;
     if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
-    if (b == x) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not alias");
+    if (overlapping(h, b, x)) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not overlap");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->dtype == SPMV_F64)
         return bicgstab<double>(h, static_cast<const double *>(b), static_cast<double *>(x), rtol, max_iter, s,

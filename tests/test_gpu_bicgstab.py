@@ -105,9 +105,10 @@ def test_zero_rhs_and_errors():
         x, it, res = device_solve(A, np.zeros(csr.n), rtol=1e-8, max_iter=50)
         assert it == 0 and res == 0.0 and not x.any()
         b = torch.ones(csr.n, dtype=torch.float64, device="cuda")
-        with pytest.raises(spmv.SpmvError) as ei:
-            spmv.spmv_bicgstab(A._h, b, b, 1e-8, 10)
-        assert ei.value.status == -1
+        for xx in (b, b[1:]):  # the same array, and one shifted by an element
+            with pytest.raises(spmv.SpmvError) as ei:
+                spmv.spmv_bicgstab(A._h, b, xx, 1e-8, 10)
+            assert ei.value.status == -1
         with pytest.raises(spmv.SpmvError):
             A.bicgstab(b, torch.zeros_like(b), max_iter=-1)
 
