@@ -2,7 +2,9 @@
 
 The oracle evaluates sampled rows one by one (random rows, both ends, every long row); the
 Laplacians are also checked on every row against their closed forms, and the 2D Laplacian
-bit-exactly on integer x.
+bit-exactly on integer x.  Each tolerance check records its worst error ratio,
+|y - y_ref| / (tau * sum |a_ij x_j|) over the checked rows, as the test property
+``worst_error_ratio`` and on a ``worst error ratio`` output line.
 """
 import numpy as np
 import pytest
@@ -12,6 +14,11 @@ from tests.gpu_util import assert_parity, build, run
 from workloads import integer_x, make_workload
 
 pytestmark = pytest.mark.gpu
+
+
+def record_worst(record_property, label, worst):
+    record_property("worst_error_ratio", worst)
+    print(f"worst error ratio {label}: {worst:.3e}")
 
 
 def sample_rows(csr, k=20000, seed=0, extra=()):
@@ -43,7 +50,7 @@ def stencil_expect(grid, f):
 @pytest.mark.parametrize("name,dtype", [("lap3d_128", np.float64), ("lap3d_128", np.float32),
                                         ("hmep_6p2m", np.float64), ("powerlaw_4m", np.float64),
                                         ("uniform16_16m", np.float32), ("lap2d_256", np.float64)])
-def test_full_size_sampled_rows(name, dtype):
+def test_full_size_sampled_rows(name, dtype, record_property):
     csr, x = make_workload(name, dtype=dtype)
     extra = []
     if name.startswith("powerlaw"):
@@ -54,28 +61,31 @@ def test_full_size_sampled_rows(name, dtype):
     with build(csr, "auto") as A:
         y = run(A, x)
         assert np.all(np.isfinite(y))
-        assert_parity(y[rows], ref, dtype, label=f"{name} {np.dtype(dtype).name} ({A.describe()['format']})")
+        label = f"{name} {np.dtype(dtype).name} ({A.describe()['format']})"
+        record_worst(record_property, label, assert_parity(y[rows], ref, dtype, label=label))
 
 
 @pytest.mark.parametrize("fmt,params", [("csr_vector", {}), ("ell_r", {}), ("sell", {"C": 64, "sigma": 256}),
                                         ("hyb", {}), ("hyb", {"spill_csr": 0}), ("merge", {})])
-def test_full_size_uniform_every_format(fmt, params):
+def test_full_size_uniform_every_format(fmt, params, record_property):
     """The random uniform workload is the one swept over every format."""
     csr, x = make_workload("uniform16_16m")
     rows = sample_rows(csr, k=5000, seed=1)
     ref = oracle.spmv(csr, x, rows=rows)
     with build(csr, fmt, **params) as A:
-        assert_parity(run(A, x)[rows], ref, np.float32, label=f"uniform16 {fmt} {params}")
+        label = f"uniform16_16m float32 ({fmt} {params})"
+        record_worst(record_property, label, assert_parity(run(A, x)[rows], ref, np.float32, label=label))
 
 
 @pytest.mark.parametrize("fmt", ["merge", "hyb", "csr_vector"])
-def test_full_size_powerlaw_other_formats(fmt):
+def test_full_size_powerlaw_other_formats(fmt, record_property):
     csr, x = make_workload("powerlaw_4m")
     lens = np.diff(csr.row_ptr.astype(np.int64))
     rows = sample_rows(csr, k=5000, seed=2, extra=np.argsort(-lens)[:64])
     ref = oracle.spmv(csr, x, rows=rows)
     with build(csr, fmt) as A:
-        assert_parity(run(A, x)[rows], ref, np.float64, label=f"powerlaw {fmt}")
+        label = f"powerlaw_4m float64 ({fmt})"
+        record_worst(record_property, label, assert_parity(run(A, x)[rows], ref, np.float64, label=label))
 
 
 def test_full_size_laplacian_closed_forms():
