@@ -1489,6 +1489,12 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     // host_blocks: the parameter (0 = off); host_pipeline_blocks: blocks of the last
     // spmv_apply_host call (0 = unpipelined, -1 = no call yet)
     append(o, "\"host_blocks\":%d,\"host_pipeline_blocks\":%d,", h->params.host_blocks, h->host_last_blocks);
+    // once pipelined: rows per block, and for each block the last piece of x it waits for
+    if (h->host_pipe == 1) {
+        append(o, "\"host_pipeline_block_rows\":%lld,\"host_pipeline_reach\":[", (long long)h->host_block);
+        for (size_t b = 0; b < h->host_need.size(); ++b) append(o, b ? ",%d" : "%d", h->host_need[b]);
+        o += "],";
+    }
     append(o, "\"ordering\":\"%s\",\"permuted_basis\":%s,", ordering_name(h->ordering),
            h->basis_perm ? "true" : "false");
     append(o, "\"n_long_rows\":%lld,\"long_nnz\":%lld,", (long long)h->n_long_rows, (long long)h->long_nnz);

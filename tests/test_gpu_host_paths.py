@@ -91,6 +91,36 @@ def test_pipelined_apply_host(name, fmt, params, blocks):
         assert np.array_equal(y2.view(np.uint8), device_apply(A, x2).view(np.uint8))
 
 
+def expected_reach(csr, block):
+    """For each block of `block` rows, the piece of x (same boundaries) holding its largest column."""
+    nb = -(-csr.n // block)
+    out = []
+    for b in range(nb):
+        lo, hi = csr.row_ptr[b * block], csr.row_ptr[min(csr.n, (b + 1) * block)]
+        out.append(int(csr.col_idx[lo:hi].max()) // block if hi > lo else -1)
+    return out
+
+
+REACH_CASES = [(name, fmt, params) for name in ("lap3d_small", "lap3d_relabelled_small", "hmep_small")
+               for fmt, params in PIPE_CASES[:5]] + [("powerlaw_small", fmt, params) for fmt, params in PIPE_CASES[:4]]
+
+
+@pytest.mark.parametrize("name,fmt,params", REACH_CASES, ids=[f"{n}-{case_id((f, p))}" for n, f, p in REACH_CASES])
+def test_pipeline_block_reach(name, fmt, params):
+    """The device's column reach of every block (which piece of x the block waits for)
+    equals the largest column of the block's rows, computed here from the CSR."""
+    csr, x = make_workload(name)
+    with build(csr, fmt, host_blocks=6, long_row_threshold=0, **params) as A:
+        host_apply(A, x)
+        d = A.describe()
+        assert d["host_pipeline_blocks"] >= 2, d
+        block = d["host_pipeline_block_rows"]
+        reach = d["host_pipeline_reach"]
+        assert len(reach) == d["host_pipeline_blocks"]
+        exp = expected_reach(csr, block)
+        assert reach[:len(exp)] == exp and all(r == -1 for r in reach[len(exp):])
+
+
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 def test_pipelined_reach_far_columns(dtype):
     """Rows that reach the last piece of x (a random matrix with empty rows and
