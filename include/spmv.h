@@ -92,7 +92,8 @@ typedef enum {
 
 /*
  * Tuning parameters; a negative value (or 0 where noted) means "choose automatically".
- *   C                   SELL slice height: 32 or 64 (warp-size multiple).
+ *   C                   SELL slice height: a power of two from 32 to 1024 (a whole number of
+ *                       warps; 32 and 64 have compiled-in addressing).  Automatic = 32.
  *   sigma               SELL sort window in rows: 1 = no sort, >= n = global sort (pJDS).
  *   K                   HYB ELL width.  Automatic: the smallest K with
  *                       (value_bytes + 8) * #{rows longer than K} <= ld * (value_bytes + 4).
