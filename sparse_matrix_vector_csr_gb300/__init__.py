@@ -93,6 +93,24 @@ class SpmvMatrix:
         if v.dtype != self.dtype or v.numel() != self.n:
             raise ValueError(f"{name} must hold {self.n} values of {self.dtype}")
 
+    def _check_host(self, v, name, writable=False):
+        """A host array of n values of the handle's type, contiguous: a numpy array or a
+        CPU tensor (the copies read and write exactly n values through its pointer)."""
+        import numpy as np
+        import torch
+
+        if isinstance(v, torch.Tensor):
+            ok = not v.is_cuda and v.is_contiguous() and v.dtype == self.dtype and v.numel() == self.n
+        elif isinstance(v, np.ndarray):
+            want = np.float64 if self.dtype == torch.float64 else np.float32
+            ok = (v.flags.c_contiguous and v.dtype == want and v.size == self.n
+                  and (v.flags.writeable or not writable))
+        else:
+            ok = False
+        if not ok:
+            raise ValueError(f"{name} must be a contiguous host array of {self.n} values of {self.dtype}"
+                             + (", writable" if writable else ""))
+
     def apply(self, x, y=None, stream=None, alpha=1.0, beta=0.0):
         """y = alpha * A x + beta * y (default y = A x) on the current (or given) stream;
         allocates y when not given (then beta must be 0)."""
@@ -158,8 +176,10 @@ class SpmvMatrix:
         """y = A x for numpy host arrays (pinned memory recommended)."""
         import numpy as np
 
+        self._check_host(x_host, "x_host")
         if y_host is None:
             y_host = np.empty_like(x_host)
+        self._check_host(y_host, "y_host", writable=True)
         spmv_apply_host(self._h, x_host, y_host)
         return y_host
 
@@ -173,6 +193,8 @@ class SpmvMatrix:
                 raise TypeError(f"{name} must be a contiguous page-locked host tensor")
         if y_host is None:
             y_host = torch.empty_like(x_host).pin_memory()
+        self._check_host(x_host, "x_host")
+        self._check_host(y_host, "y_host")
         spmv_apply_mapped(self._h, x_host, y_host)
         return y_host
 

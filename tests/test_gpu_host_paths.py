@@ -214,3 +214,23 @@ def test_overlapping_vectors():
         y = host_apply(A, x)
         assert A.describe()["host_pipeline_blocks"] == 4
         assert np.array_equal(y.view(np.uint8), buf.numpy().view(np.uint8))
+
+
+def test_host_arrays_checked():
+    """Host arrays of the wrong length, type or layout are refused before any copy."""
+    torch = torch_cuda()
+    csr, x = make_workload("lap2d_small")
+    with build(csr) as A:
+        good = np.empty_like(x)
+        for bad_x in (x[:-1], x.astype(np.float32), np.stack([x, x], axis=1)[:, 0], [0.0] * csr.n):
+            with pytest.raises(ValueError):
+                A.apply_host(bad_x, good)
+        ro = np.empty_like(x)
+        ro.flags.writeable = False
+        with pytest.raises(ValueError):
+            A.apply_host(x, ro)
+        xt = torch.from_numpy(x).pin_memory()
+        with pytest.raises(ValueError):
+            A.apply_mapped(xt, torch.empty(csr.n - 1, dtype=xt.dtype).pin_memory())
+        y = A.apply_host(x)
+        assert_parity(y, oracle.spmv(csr, x), csr.dtype, label="checked host arrays")
