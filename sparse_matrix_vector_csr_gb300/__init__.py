@@ -241,6 +241,7 @@ class SpmvMatrix:
 
         self._check_vec(v, "v")
         out = torch.empty_like(v) if out is None else out
+        self._check_vec(out, "out")
         spmv_permute_vector(self._h, v, out, 0, stream)
         return out
 
@@ -250,6 +251,7 @@ class SpmvMatrix:
 
         self._check_vec(v, "v")
         out = torch.empty_like(v) if out is None else out
+        self._check_vec(out, "out")
         spmv_permute_vector(self._h, v, out, 1, stream)
         return out
 
