@@ -285,7 +285,10 @@ SPMV_API int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const vo
  * Arithmetic: vectors in the value type; every dot product and the step lengths in
  * double, reduced in a fixed order (results are reproducible).  Workspace (4 vectors:
  * r, p, A p and the iterate) is taken from the stream-ordered pool of `stream` and
- * returned before the call ends.
+ * returned before the call ends.  While the solve runs, the calling thread keeps two
+ * iterations queued, pacing itself on a small page-locked progress record (allocated
+ * once per thread) that the kernels update; at most two iterations' products run
+ * after the stop.
  * Synchronises `stream`.  Returns SPMV_ERR_UNSUPPORTED (after filling the outputs) if
  * p.Ap <= 0 at some step, i.e. A is not positive definite; SPMV_ERR_INVALID_ARG for a
  * NULL handle or vector, overlapping b and x, max_iter < 0 or rtol < 0 / NaN.

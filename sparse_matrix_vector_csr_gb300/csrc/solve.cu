@@ -9,8 +9,10 @@
 // with a fixed grid; the last block to finish adds the per-block partials in block
 // order, so every sum is reproducible run to run.  The step lengths and the stopping
 // decision live in device memory: once the test has passed, the update kernels return
-// at once, so the host only needs to look at a flag every few iterations and the
-// iteration count is exact.
+// at once, so the iteration count is exact however far the host has enqueued.  The host
+// paces its launches on a progress record (iterations done, stop flag) that the kernels
+// write into page-locked host memory, keeping two iterations queued: no copy or
+// synchronisation sits in the stream between iterations.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -28,7 +30,7 @@ using namespace dev;
 constexpr int kRedBlocksPerSm = 4;  // 64 registers a thread for the unrolled loads
 constexpr int kRedBlocks = 152 * kRedBlocksPerSm;  // one wave on 152 SMs; fixed, so reductions are reproducible
 constexpr int kRedThreads = 256;
-constexpr int kCheckEvery = 8;    // iterations enqueued between two host looks at the flag
+constexpr int kAhead = 2;         // iterations enqueued beyond the last one whose update finished
 
 struct Control {
     int32_t stop;        // 0 running, 1 converged, 2 p.Ap <= 0 (not positive definite)
@@ -36,6 +38,21 @@ struct Control {
     uint32_t arrivals;   // blocks finished in the running reduction
     int32_t pad;
 };
+
+// The solve's progress as the host sees it: page-locked host memory that the kernels
+// write through its device mapping whenever they change the iteration count or the stop
+// flag, so the host paces its launches without any copy in the stream.
+struct Progress {
+    int32_t iterations;
+    int32_t stop;
+};
+
+__device__ __forceinline__ void publish(Progress *pg, const Control *ctl) {
+    volatile Progress *v = pg;
+    v->iterations = ctl->iterations;
+    v->stop = ctl->stop;
+    __threadfence_system();
+}
 
 // Scalars: rr[0], rr[1] the residual norms squared by iteration parity, pq = p.Ap, bb = b.b
 struct Scalars {
@@ -134,14 +151,17 @@ __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
 // r -= alpha q with alpha = rr_cur / pq, then rr_next = r.r and the stopping test
 template <typename T, int U>
 __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
-    k_cg_r(int64_t units, Scalars *sc, Control *ctl, int cur, double stop_rr, const Pack<T> *__restrict__ q,
-           Pack<T> *__restrict__ r, double *__restrict__ partial) {
+    k_cg_r(int64_t units, Scalars *sc, Control *ctl, Progress *pg, int cur, double stop_rr,
+           const Pack<T> *__restrict__ q, Pack<T> *__restrict__ r, double *__restrict__ partial) {
     allow_dependents();
     grid_wait();
     if (ctl->stop) return;
     const double pq = sc->pq;
     if (!(pq > 0.0)) {  // no positive curvature along p: CG is undefined here
-        if (blockIdx.x == 0 && threadIdx.x == 0) ctl->stop = 2;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            ctl->stop = 2;
+            publish(pg, ctl);
+        }
         return;
     }
     using A = typename Acc<T>::type;
@@ -171,6 +191,7 @@ __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
         sc->rr[cur ^ 1] = total;
         ctl->iterations += 1;
         if (!(total > stop_rr)) ctl->stop = 1;  // NaN stops too
+        publish(pg, ctl);
     }
 }
 
@@ -253,14 +274,17 @@ __device__ __forceinline__ bool finish_sum2(double a, double b, double *partial,
 // p = r + beta (p - omega v), beta = (rho_k / rho_{k-1}) (alpha / omega)
 template <typename T, int U>
 __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
-    k_bi_p(int64_t units, const BiScalars *sc, Control *ctl, int cur, const Pack<T> *__restrict__ r,
+    k_bi_p(int64_t units, const BiScalars *sc, Control *ctl, Progress *pg, int cur, const Pack<T> *__restrict__ r,
            const Pack<T> *__restrict__ v, Pack<T> *__restrict__ p) {
     allow_dependents();
     grid_wait();
     if (ctl->stop) return;
     const double rho = sc->rho[cur];
     if (!(rho != 0.0)) {  // (r_hat, r) = 0 (or NaN): breakdown
-        if (blockIdx.x == 0 && threadIdx.x == 0) ctl->stop = 2;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            ctl->stop = 2;
+            publish(pg, ctl);
+        }
         return;
     }
     const T beta = static_cast<T>((rho / sc->rho[cur ^ 1]) * (sc->alpha / sc->omega));
@@ -286,14 +310,17 @@ __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
 // alpha = rho_k / (r_hat, v); s = r - alpha v
 template <typename T, int U>
 __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
-    k_bi_s(int64_t units, BiScalars *sc, Control *ctl, int cur, const Pack<T> *__restrict__ r,
+    k_bi_s(int64_t units, BiScalars *sc, Control *ctl, Progress *pg, int cur, const Pack<T> *__restrict__ r,
            const Pack<T> *__restrict__ v, Pack<T> *__restrict__ s_out) {
     allow_dependents();
     grid_wait();
     if (ctl->stop) return;
     const double rv = sc->rv;
     if (!(rv != 0.0)) {  // (r_hat, A p) = 0: breakdown
-        if (blockIdx.x == 0 && threadIdx.x == 0) ctl->stop = 2;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            ctl->stop = 2;
+            publish(pg, ctl);
+        }
         return;
     }
     const double alpha_d = sc->rho[cur] / rv;
@@ -355,7 +382,8 @@ __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
 // rho = (r_hat, r) and the stopping test
 template <typename T, int U>
 __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
-    k_bi_xr(int64_t units, BiScalars *sc, Control *ctl, int cur, double stop_rr, const Pack<T> *__restrict__ p,
+    k_bi_xr(int64_t units, BiScalars *sc, Control *ctl, Progress *pg, int cur, double stop_rr,
+            const Pack<T> *__restrict__ p,
             const Pack<T> *__restrict__ s, const Pack<T> *__restrict__ t, const Pack<T> *__restrict__ r_hat,
             Pack<T> *__restrict__ x, Pack<T> *__restrict__ r, double *__restrict__ partial) {
     allow_dependents();
@@ -404,6 +432,7 @@ __global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
             ctl->stop = 1;             // converged (NaN stops too)
         else if (omega_d == 0.0)
             ctl->stop = 2;             // omega = 0 before convergence: breakdown
+        publish(pg, ctl);
     }
 }
 
@@ -426,6 +455,51 @@ struct StreamBuffer {
     cudaStream_t s = nullptr;
     ~StreamBuffer() {
         if (ptr) cudaFreeAsync(ptr, s);
+    }
+};
+
+// Paces the host's launches on the solve's Progress: before enqueuing an iteration the
+// host waits until at most kAhead - 1 enqueued iterations are still unfinished, so the
+// stream never drains between iterations and at most kAhead run after a stop (every
+// update kernel then returns at once; only the products run).  The wait looks at the
+// stream every 1024 reads and ends when the stream is idle or reports an error, so it
+// cannot outlast the work it waits for.
+// The record lives in page-locked memory allocated once per host thread (a solve call
+// is synchronous, so a thread runs one solve at a time) and kept for the thread's life:
+// allocating and freeing it per solve cost about a millisecond.
+struct Pacer {
+    Progress *host = nullptr;
+    Progress *dev = nullptr;
+    cudaStream_t s = nullptr;
+    ~Pacer() {
+        if (host) cudaStreamSynchronize(s);  // no kernel of this solve may still write the record
+    }
+    int init() {
+        thread_local Progress *record = nullptr;
+        if (!record)
+            SPMV_TRY_CUDA(cudaHostAlloc(reinterpret_cast<void **>(&record), sizeof(Progress),
+                                        cudaHostAllocMapped | cudaHostAllocPortable));
+        host = record;
+        host->iterations = 0;
+        host->stop = 0;
+        SPMV_TRY_CUDA(cudaHostGetDevicePointer(reinterpret_cast<void **>(&dev), host, 0));
+        return SPMV_OK;
+    }
+    // returns with *stop set when the solve has stopped
+    int wait(int32_t launched, bool *stop) {
+        const volatile Progress *v = host;
+        for (uint32_t reads = 1;; ++reads) {
+            if (v->stop) {
+                *stop = true;
+                return SPMV_OK;
+            }
+            if (launched - v->iterations < kAhead) return SPMV_OK;
+            if ((reads & 1023u) == 0) {
+                const cudaError_t e = cudaStreamQuery(s);
+                if (e == cudaSuccess) return SPMV_OK;  // everything enqueued has finished
+                if (e != cudaErrorNotReady) return set_cuda_error(e, "cudaStreamQuery");
+            }
+        }
     }
 };
 
@@ -471,22 +545,23 @@ int cg(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, cudaStr
     int32_t launched = 0;
     Control hc{};
     if (max_iter > 0 && hs.rr[0] > stop_rr) {
-        while (launched < max_iter) {
-            const int32_t block = std::min<int32_t>(kCheckEvery, max_iter - launched);
-            for (int32_t j = 0; j < block; ++j, ++launched) {
-                const int cur = launched & 1;
-                SPMV_TRY(spmv_apply(h, p, q, s));
-                SPMV_TRY_CUDA(launch(k_dot<T, kUnroll>, s, units, cp, cq, partial, ctl, &sc->pq));
-                SPMV_TRY_CUDA(launch(k_cg_r<T, kUnroll>, s, units, sc, ctl, cur, stop_rr, cq, r, partial));
-                SPMV_TRY_CUDA(launch(k_cg_xp<T, kUnrollXp>, s, units, static_cast<const Scalars *>(sc),
-                                     static_cast<const Control *>(ctl), launched, cr, p, xw));
-            }
-            SPMV_TRY_CUDA(cudaMemcpyAsync(&hc, ctl, sizeof(hc), cudaMemcpyDeviceToHost, s));
-            SPMV_TRY_CUDA(cudaStreamSynchronize(s));
-            if (hc.stop) break;
+        Pacer pace;
+        pace.s = s;
+        SPMV_TRY(pace.init());
+        for (; launched < max_iter; ++launched) {
+            bool stop = false;
+            SPMV_TRY(pace.wait(launched, &stop));
+            if (stop) break;
+            const int cur = launched & 1;
+            SPMV_TRY(spmv_apply(h, p, q, s));
+            SPMV_TRY_CUDA(launch(k_dot<T, kUnroll>, s, units, cp, cq, partial, ctl, &sc->pq));
+            SPMV_TRY_CUDA(launch(k_cg_r<T, kUnroll>, s, units, sc, ctl, pace.dev, cur, stop_rr, cq, r, partial));
+            SPMV_TRY_CUDA(launch(k_cg_xp<T, kUnrollXp>, s, units, static_cast<const Scalars *>(sc),
+                                 static_cast<const Control *>(ctl), launched, cr, p, xw));
         }
         SPMV_TRY_CUDA(cudaMemcpyAsync(x, xw, vec, cudaMemcpyDeviceToDevice, s));
         SPMV_TRY_CUDA(cudaMemcpyAsync(&hs, sc, sizeof(hs), cudaMemcpyDeviceToHost, s));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(&hc, ctl, sizeof(hc), cudaMemcpyDeviceToHost, s));
         SPMV_TRY_CUDA(cudaStreamSynchronize(s));
     }
     const double rr = hs.rr[hc.iterations & 1];
@@ -546,26 +621,27 @@ int bicgstab(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, c
     int32_t launched = 0;
     Control hc{};
     if (max_iter > 0 && hs.rr[0] > stop_rr) {
-        while (launched < max_iter) {
-            const int32_t block = std::min<int32_t>(kCheckEvery, max_iter - launched);
-            for (int32_t j = 0; j < block; ++j, ++launched) {
-                const int cur = launched & 1;
-                SPMV_TRY_CUDA(launch(k_bi_p<T, kUnroll>, s, units, static_cast<const BiScalars *>(sc), ctl, cur, cr,
-                                     cv, p));
-                SPMV_TRY(spmv_apply(h, p, v, s));
-                SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, crh, cv, partial, ctl, &sc->rv));
-                SPMV_TRY_CUDA(launch(k_bi_s<T, kUnroll>, s, units, sc, ctl, cur, cr, cv, sv));
-                SPMV_TRY(spmv_apply(h, sv, t, s));
-                SPMV_TRY_CUDA(launch(k_bi_tt<T, kUnroll>, s, units, sc, ctl, ct, csv, partial));
-                SPMV_TRY_CUDA(launch(k_bi_xr<T, kUnroll>, s, units, sc, ctl, cur, stop_rr, cp, csv, ct, crh, xw, r,
-                                     partial));
-            }
-            SPMV_TRY_CUDA(cudaMemcpyAsync(&hc, ctl, sizeof(hc), cudaMemcpyDeviceToHost, s));
-            SPMV_TRY_CUDA(cudaStreamSynchronize(s));
-            if (hc.stop) break;
+        Pacer pace;
+        pace.s = s;
+        SPMV_TRY(pace.init());
+        for (; launched < max_iter; ++launched) {
+            bool stop = false;
+            SPMV_TRY(pace.wait(launched, &stop));
+            if (stop) break;
+            const int cur = launched & 1;
+            SPMV_TRY_CUDA(launch(k_bi_p<T, kUnroll>, s, units, static_cast<const BiScalars *>(sc), ctl, pace.dev, cur,
+                                 cr, cv, p));
+            SPMV_TRY(spmv_apply(h, p, v, s));
+            SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, crh, cv, partial, ctl, &sc->rv));
+            SPMV_TRY_CUDA(launch(k_bi_s<T, kUnroll>, s, units, sc, ctl, pace.dev, cur, cr, cv, sv));
+            SPMV_TRY(spmv_apply(h, sv, t, s));
+            SPMV_TRY_CUDA(launch(k_bi_tt<T, kUnroll>, s, units, sc, ctl, ct, csv, partial));
+            SPMV_TRY_CUDA(launch(k_bi_xr<T, kUnroll>, s, units, sc, ctl, pace.dev, cur, stop_rr, cp, csv, ct, crh, xw,
+                                 r, partial));
         }
         SPMV_TRY_CUDA(cudaMemcpyAsync(x, xw, vec, cudaMemcpyDeviceToDevice, s));
         SPMV_TRY_CUDA(cudaMemcpyAsync(&hs, sc, sizeof(hs), cudaMemcpyDeviceToHost, s));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(&hc, ctl, sizeof(hc), cudaMemcpyDeviceToHost, s));
         SPMV_TRY_CUDA(cudaStreamSynchronize(s));
     }
     const double rr = hs.rr[hc.iterations & 1];
