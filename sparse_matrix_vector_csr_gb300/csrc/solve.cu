@@ -476,6 +476,13 @@ struct Pacer {
     }
     int init() {
         thread_local Progress *record = nullptr;
+        if (record) {  // still page-locked? (a device reset releases it)
+            cudaPointerAttributes attr;
+            if (cudaPointerGetAttributes(&attr, record) != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+                (void)cudaGetLastError();
+                record = nullptr;
+            }
+        }
         if (!record)
             SPMV_TRY_CUDA(cudaHostAlloc(reinterpret_cast<void **>(&record), sizeof(Progress),
                                         cudaHostAllocMapped | cudaHostAllocPortable));
