@@ -50,7 +50,9 @@ template <typename T, int CS, int NV>
 __device__ __forceinline__ void sellmm_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
                                            const T *__restrict__ X, int64_t ldx, T *__restrict__ Y, int64_t ldy,
                                            const Epi &ep) {
-    constexpr int U = NV >= 8 ? 1 : 2;
+    // entries of the row loaded ahead of their gathers: enough bytes in flight to stream
+    // the matrix, within the registers the NV accumulators and gathered values leave
+    constexpr int U = NV >= 8 ? 1 : sizeof(T) == 4 ? 4 : 2;
     const int w = __ldg(a.len + p);
     const uint64_t up = static_cast<uint64_t>(p);
     const int64_t slot = __ldg(a.slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS);
@@ -239,7 +241,9 @@ bool sell_multi_supported(const Sliced &sl) {
 cudaError_t launch_sell_multi(int dtype, int nv, const Sliced &sl, int64_t n, const Segmented *split, const void *X,
                               int64_t ldx, void *Y, int64_t ldy, cudaStream_t s, const Scale &scale) {
     if (!sl.present || sl.n_pos <= 0) return cudaSuccess;
-    const Epi ep{scale.alpha, scale.beta, 1};
+    // Y = A X (alpha 1, beta 0) stores the sums as they are: the scaling multiply would
+    // cost about a seventh of the FP64 work on short rows, and 1 * v is v
+    const Epi ep{scale.alpha, scale.beta, (scale.alpha == 1.0 && scale.beta == 0.0) ? 0 : 1};
     if (dtype == SPMV_F64)
         return mm_dispatch<double>(nv, sl, n, split, static_cast<const double *>(X), ldx, static_cast<double *>(Y),
                                    ldy, s, ep);
