@@ -161,3 +161,56 @@ def test_full_size_laplacian_3d_128():
     assert res <= 1e-6
     assert 0 < it <= cg_iteration_bound((128, 128, 128), 1e-6)
     assert true_residual(csr, x, b) <= 1.05e-6
+
+
+def test_stop_at_the_first_step_is_exact():
+    """A multiple of the identity converges in one step; the host has more iterations
+    queued by then, which must neither move x nor count."""
+    from workloads import CSR
+
+    n, c = 5000, 4.0
+    csr = CSR(n, np.arange(n + 1, dtype=np.int32), np.arange(n, dtype=np.int32), np.full(n, c))
+    b = uniform_x(n, seed=51)
+    with build(csr, "auto") as A:
+        x, it, res = device_cg(A, b, rtol=1e-12, max_iter=1000)
+    assert it == 1 and res <= 1e-15
+    assert np.max(np.abs(x - b / c)) <= 1e-15 * np.max(np.abs(b / c))
+
+
+def test_solves_from_two_threads():
+    """Two host threads solve on their own handles and streams at the same time: each has
+    its own progress record, and each result equals the one-thread result bit for bit."""
+    import threading
+
+    torch = torch_cuda()
+    csr = laplacian_2d(96, 80)
+    cases = [uniform_x(csr.n, seed=61), uniform_x(csr.n, seed=62)]
+    ref = []
+    for b in cases:
+        with build(csr, "auto") as A:
+            x, it, _ = device_cg(A, b, rtol=1e-9, max_iter=3000)
+            ref.append((x, it))
+    out = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            with build(csr, "auto") as A, torch.cuda.stream(s):
+                bd = torch.from_numpy(cases[i]).cuda()
+                xd = torch.zeros_like(bd)
+                s.synchronize()
+                x, it, _ = A.cg(bd, xd, rtol=1e-9, max_iter=3000, stream=s)
+                s.synchronize()
+                out[i] = (x.cpu().numpy(), it)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for (x, it), (xr, itr) in zip(out, ref):
+        assert it == itr and np.array_equal(x.view(np.uint64), xr.view(np.uint64))
