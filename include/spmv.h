@@ -100,7 +100,9 @@ typedef enum {
  *   spill_csr           HYB spill kind: 1 = CSR (HEC), 0 = COO (HYB).  Automatic = CSR.
  *   long_row_threshold  rows with more entries go to the merge-path pass.  0 = never.
  *   subwarp             CSR-vector lanes per row (2, 4, 8, 16 or 32) for every row;
- *                       automatic = per row-length bin.
+ *                       automatic = per row-length bin, about eight entries a lane: 2
+ *                       lanes up to 16 entries, 4 up to 32, 8 up to 64, 16 up to 128,
+ *                       32 above.
  *   row_threads         threads per row in the SELL / ELLPACK-R / HYB-ELL apply (1, 2, 4,
  *                       8, 16 or 32), the multi-thread-per-row ELL variants of the
  *                       load-balancing SpMV paper.  Automatic: 1, unless one thread per

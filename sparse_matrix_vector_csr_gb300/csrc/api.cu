@@ -523,7 +523,8 @@ int build_csr_vector(BuildCtx &c, int32_t forced_g) {
         SPMV_TRY_CUDA(cudaMemcpyAsync(h->csr_col, c.col, sizeof(int32_t) * h->nnz, cudaMemcpyDeviceToDevice, c.s));
         SPMV_TRY_CUDA(cudaMemcpyAsync(h->csr_val, c.val, vb * h->nnz, cudaMemcpyDeviceToDevice, c.s));
     }
-    // bin sizes from the histogram (bins: <=2, <=4, <=8, <=16, longer)
+    // bin sizes from the histogram (bins: <=16, <=32, <=64, <=128, longer: about eight
+    // entries a lane; the device partition applies the same rule, vector_bin in build.cu)
     const int gs[5] = {2, 4, 8, 16, 32};
     std::vector<int64_t> cnt(5, 0);
     const int64_t n_short = n - c.n_long;
@@ -535,7 +536,7 @@ int build_csr_vector(BuildCtx &c, int32_t forced_g) {
         const int32_t thr = c.threshold;
         for (int l = 0; l < kHistCap; ++l) {
             if (thr >= 0 && l > thr) continue;  // long row
-            const int b = l <= 2 ? 0 : l <= 4 ? 1 : l <= 8 ? 2 : l <= 16 ? 3 : 4;
+            const int b = l <= 16 ? 0 : l <= 32 ? 1 : l <= 64 ? 2 : l <= 128 ? 3 : 4;
             cnt[b] += c.hist[l];
         }
         // the top bucket holds every row of kHistCap or more entries

@@ -265,8 +265,9 @@ def test_csr_vector_bins():
         d = A.describe()
         thr = d["long_row_threshold"]
         short = lens[lens <= thr]
-        expect = {2: (short <= 2).sum(), 4: ((short > 2) & (short <= 4)).sum(), 8: ((short > 4) & (short <= 8)).sum(),
-                  16: ((short > 8) & (short <= 16)).sum(), 32: (short > 16).sum()}
+        # about eight entries a lane: 2 lanes up to 16 entries, then 4, 8, 16 up to 32, 64, 128, 32 above
+        expect = {2: (short <= 16).sum(), 4: ((short > 16) & (short <= 32)).sum(), 8: ((short > 32) & (short <= 64)).sum(),
+                  16: ((short > 64) & (short <= 128)).sum(), 32: (short > 128).sum()}
         got = {g: c for g, c in d["bins"]}
         assert got == {g: int(c) for g, c in expect.items() if c}
         assert d["n_long_rows"] == int((lens > thr).sum())
