@@ -76,10 +76,11 @@ typedef enum { SPMV_F64 = 0, SPMV_F32 = 1 } spmv_dtype;
  *      Trilinos issue attributes to the vendor library; the load-balanced CSR/COO
  *      kernels of the scite report's abstract).  Suited to irregular matrices.
  *  SPMV_FMT_AUTO        the builder picks one of the above from the row lengths.
- * In every format, rows longer than the long-row threshold are taken out and
- * handled by a load-balanced merge-path pass (the class of the longest rows in the
- * Trilinos issue; merge-path split as the Trilinos issue attributes to the vendor
- * library), so no single thread walks a very long row.
+ * In SELL, ELLPACK-R and CSR-vector, rows longer than the long-row threshold are
+ * taken out and handled by a row-split pass: each is cut into chunks of 2048 entries,
+ * one warp per chunk, and the chunk sums of a row combine in a tree (the class of the
+ * longest rows in the Trilinos issue, processed in pieces).  So no single thread walks
+ * a very long row.
  */
 typedef enum {
     SPMV_FMT_AUTO = 0,
@@ -98,7 +99,8 @@ typedef enum {
  *   K                   HYB ELL width.  Automatic: the smallest K with
  *                       (value_bytes + 8) * #{rows longer than K} <= ld * (value_bytes + 4).
  *   spill_csr           HYB spill kind: 1 = CSR (HEC), 0 = COO (HYB).  Automatic = CSR.
- *   long_row_threshold  rows with more entries go to the merge-path pass.  0 = never.
+ *   long_row_threshold  rows with more entries go to the row-split pass.  0 = never.
+ *                       Automatic: 128 for SELL / ELLPACK-R, 256 for CSR-vector.
  *   subwarp             CSR-vector lanes per row (2, 4, 8, 16 or 32) for every row;
  *                       automatic = per row-length bin, about eight entries a lane: 2
  *                       lanes up to 16 entries, 4 up to 32, 8 up to 64, 16 up to 128,
