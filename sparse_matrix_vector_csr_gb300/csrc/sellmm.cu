@@ -102,24 +102,42 @@ template <typename T, int NV>
 __device__ __forceinline__ void splitmm_chunk(int64_t c, int lane, const SplitArgs &a, const T *__restrict__ val,
                                               const T *__restrict__ X, int64_t ldx, T *__restrict__ Y, int64_t ldy,
                                               const Epi &ep) {
+    // U entries a lane loaded ahead of their gathers, as in the single-vector chunk loop;
+    // each lane still adds its entries in index order
+    constexpr int U = NV >= 8 ? 2 : 4;
     const int32_t b = __ldg(a.chunk_begin + c), e = __ldg(a.chunk_end + c);
     T acc[NV];
 #pragma unroll
     for (int q = 0; q < NV; ++q) acc[q] = T(0);
-    int32_t k = b + lane;
-    int32_t cc = k < e ? ld_stream(a.col + k) : 0;
-    T v = k < e ? ld_stream(val + k) : T(0);
-    grid_wait();
-    for (; k < e; k += 32) {
-        T xr[NV];
-        load_row<T, NV>(X + static_cast<int64_t>(cc) * ldx, xr);
+    bool first = true;
+    for (int32_t k = b + lane; k < e; k += 32 * U) {
+        int32_t cc[U];
+        T v[U];
 #pragma unroll
-        for (int q = 0; q < NV; ++q) acc[q] = fma(v, xr[q], acc[q]);
-        if (k + 32 < e) {
-            cc = ld_stream(a.col + k + 32);
-            v = ld_stream(val + k + 32);
+        for (int u = 0; u < U; ++u) {
+            const bool on = k + 32 * u < e;
+            cc[u] = on ? ld_stream(a.col + k + 32 * u) : 0;
+            v[u] = on ? ld_stream(val + k + 32 * u) : T(0);
         }
+        if (first) {
+            grid_wait();  // matrix data above, X and Y below
+            first = false;
+        }
+        T xr[U][NV];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (k + 32 * u < e)
+                load_row<T, NV>(X + static_cast<int64_t>(cc[u]) * ldx, xr[u]);
+            else
+#pragma unroll
+                for (int q = 0; q < NV; ++q) xr[u][q] = T(0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int q = 0; q < NV; ++q) acc[q] = fma(v[u], xr[u][q], acc[q]);  // past the end: +0 * +0
     }
+    if (first) grid_wait();  // a lane with no entry of its own still writes after the wait
     double s[NV];
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
