@@ -402,3 +402,35 @@ def test_apply_after_a_kernel_that_writes_x():
             ref = oracle.spmv(csr, xd.cpu().numpy())
             assert_parity(y.cpu().numpy(), ref, np.float64, label=f"round {k}")
             assert torch.equal(z, y * 2.0)
+
+
+def test_csr_vector_bin_boundaries():
+    """Rows whose lengths sit on every bin edge (16/17, 32/33, 64/65, 128/129) and on the
+    long-row threshold (256/257): each lands in its bin, the rows above 256 go to the
+    row-split pass, and the product matches the oracle (bit for bit on integers)."""
+    from workloads import CSR
+
+    torch = torch_cuda()
+    rng = np.random.default_rng(71)
+    lens = np.array([0, 1, 16, 17, 32, 33, 64, 65, 128, 129, 256, 257, 1000] * 40)
+    rng.shuffle(lens)
+    n = 4096
+    lens = np.concatenate([lens, rng.integers(0, 9, n - lens.size)])
+    row_ptr = np.zeros(n + 1, np.int64)
+    np.cumsum(lens, out=row_ptr[1:])
+    cols = np.concatenate([np.sort(rng.choice(n, size=l, replace=False)) for l in lens]).astype(np.int32)
+    vals = rng.integers(-4, 5, cols.size).astype(np.float64)
+    csr = CSR(n, row_ptr.astype(np.int32), cols, vals)
+    x = rng.integers(-8, 9, n).astype(np.float64)
+    with build(csr, "csr_vector") as A:
+        d = A.describe()
+        assert d["long_row_threshold"] == 256
+        short = lens[lens <= 256]
+        expect = {2: (short <= 16).sum(), 4: ((short > 16) & (short <= 32)).sum(),
+                  8: ((short > 32) & (short <= 64)).sum(), 16: ((short > 64) & (short <= 128)).sum(),
+                  32: (short > 128).sum()}
+        assert {g: c for g, c in d["bins"]} == {g: int(c) for g, c in expect.items() if c}
+        assert d["n_long_rows"] == int((lens > 256).sum())
+        y = A.apply(torch.from_numpy(x).cuda())
+        torch.cuda.synchronize()
+        assert_parity(y.cpu().numpy(), oracle.spmv(csr, x), np.float64, exact=True, label="bin edges")
