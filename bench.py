@@ -613,7 +613,11 @@ def run_cg(args):
         b = torch.from_numpy(b_np).to(dev)
         x = torch.zeros_like(b)
         A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=args.format)
-        solve = A.bicgstab if args.solver == "bicgstab" else A.cg
+        if args.solver == "gmres":
+            def solve(b_, x_, **kw):
+                return A.gmres(b_, x_, restart=args.restart, **kw)
+        else:
+            solve = A.bicgstab if args.solver == "bicgstab" else A.cg
         solve(b, x, rtol=0.0, max_iter=max(args.warmup, 3))
 
         def timed(iters):
@@ -640,10 +644,20 @@ def run_cg(args):
         if args.solver == "bicgstab":
             bytes_iter = 2 * effective_bytes(csr.n, csr.nnz, sv) + 18 * csr.n * sv
             launches = 7
+        elif args.solver == "gmres":
+            # Arnoldi step j: the product, two Gram-Schmidt passes that each read the j + 1
+            # basis vectors twice (dot, then axpy), seven passes over w (dots, axpys with w
+            # written, scale); mean j + 1 over a cycle is (m + 1) / 2.  Per cycle, spread over
+            # its m steps: x += V y (m vectors, x read and written) and r = b - A x with its norm
+            m = args.restart
+            beff = effective_bytes(csr.n, csr.nnz, sv)
+            bytes_iter = beff + (2 * (m + 1) + 7) * csr.n * sv + ((m + 4) * csr.n * sv + beff) / m
+            launches = 6
         else:
             bytes_iter = effective_bytes(csr.n, csr.nnz, sv) + 10 * csr.n * sv
             launches = 4
         print(json.dumps({"workload": args.workload, "dtype": "f64" if sv == 8 else "f32", "solver": args.solver,
+                          **({"restart": args.restart} if args.solver == "gmres" else {}),
                           "format": A.describe()["format"], "us_per_iteration": ms_iter * 1e3,
                           "launches_per_iteration": launches, "bytes_per_iteration": bytes_iter,
                           "effective_gbs": bytes_iter / ms_iter / 1e6, "frac": bytes_iter / ms_iter / 1e6 / peak,
@@ -827,7 +841,8 @@ def main(argv=None):
                     help="time the workload in its given numbering and in the row-length / RCM permuted bases")
     ap.add_argument("--cg", type=int, default=0, metavar="ITERS",
                     help="time the Krylov solver (ITERS fixed steps per run) instead of the bench line")
-    ap.add_argument("--solver", choices=["cg", "bicgstab"], default="cg", help="with --cg: which solver")
+    ap.add_argument("--solver", choices=["cg", "bicgstab", "gmres"], default="cg", help="with --cg: which solver")
+    ap.add_argument("--restart", type=int, default=30, help="with --solver gmres: the restart length m")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -312,6 +312,25 @@ SPMV_API int spmv_bicgstab(spmv_handle_t h, const void *b, void *x, double rtol,
                            int32_t *iterations, double *relative_residual);
 
 /*
+ * Solve A x = b by restarted GMRES(m) (Saad and Schultz), unpreconditioned: the third
+ * Krylov solver the Krylov/AMG paper lists beside CG and BiCGSTAB.  Each Arnoldi step
+ * is one product on this handle, Gram-Schmidt orthogonalisation applied twice (fused
+ * multi-dot and multi-axpy kernels over the basis), and a Givens rotation of the
+ * Hessenberg column; a cycle ends after `restart` steps or when the rotated residual
+ * estimate meets the test, and then x is updated and the true residual b - A x is
+ * recomputed.
+ *   restart  m, the Krylov dimension of a cycle: 1 .. 64.
+ * Other arguments, arithmetic and pacing as spmv_cg.  The solve stops when the true
+ * residual at the end of a cycle meets ||b - A x|| <= rtol ||b|| (||b|| -> 1 when
+ * b = 0) or after max_iter Arnoldi steps over all cycles; iterations counts those steps
+ * and relative_residual is the true residual.  Workspace: m + 2 vectors and the small
+ * Hessenberg state.  Returns SPMV_ERR_UNSUPPORTED (after filling the outputs) on a zero
+ * pivot of the rotated Hessenberg matrix (A singular on the Krylov space).
+ */
+SPMV_API int spmv_gmres(spmv_handle_t h, const void *b, void *x, int32_t restart, double rtol, int32_t max_iter,
+                        void *stream, int32_t *iterations, double *relative_residual);
+
+/*
  * Orderings of the permuted basis (spmv_build_permuted).  perm maps a position of the
  * basis to an original index (new -> old).
  *   NATURAL     the identity.

@@ -33,6 +33,7 @@ from ._abi import (  # noqa: F401
     spmv_get_permutation,
     spmv_build_permuted,
     spmv_bicgstab,
+    spmv_gmres,
     spmv_permute_vector,
     spmv_get_slots,
     spmv_last_error,
@@ -168,6 +169,19 @@ class SpmvMatrix:
             x = torch.zeros_like(b)
         self._check_vec(x, "x")
         it, res = spmv_bicgstab(self._h, b, x, rtol, max_iter, stream)
+        return x, it, res
+
+    def gmres(self, b, x=None, restart=30, rtol=1e-8, max_iter=1000, stream=None):
+        """Solve A x = b by restarted GMRES(restart) on the device (any nonsingular A).
+        ``x`` is the initial guess (zeros when not given) and is updated in place.
+        Returns (x, Arnoldi steps, true relative residual)."""
+        import torch
+
+        self._check_vec(b, "b")
+        if x is None:
+            x = torch.zeros_like(b)
+        self._check_vec(x, "x")
+        it, res = spmv_gmres(self._h, b, x, restart, rtol, max_iter, stream)
         return x, it, res
 
     __matmul__ = apply

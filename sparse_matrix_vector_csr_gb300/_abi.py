@@ -28,6 +28,7 @@ EXPORTS = (
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
     "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
     "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector", "spmv_apply_mapped", "spmv_bicgstab",
+    "spmv_gmres",
 )
 
 #: spmv_ordering codes
@@ -104,6 +105,8 @@ def _load():
     lib.spmv_cg.restype = c_int
     lib.spmv_bicgstab.argtypes = lib.spmv_cg.argtypes
     lib.spmv_bicgstab.restype = c_int
+    lib.spmv_gmres.argtypes = [vp, vp, vp, i32, f64, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(f64)]
+    lib.spmv_gmres.restype = c_int
     lib.spmv_build_permuted.argtypes = [i64, i64, vp, vp, vp, c_int, c_int, ctypes.POINTER(FormatParams), c_int, vp,
                                         vp]
     lib.spmv_build_permuted.restype = vp
@@ -314,4 +317,14 @@ def spmv_bicgstab(h, b, x, rtol, max_iter, stream=None):
     res = ctypes.c_double(0.0)
     _check(lib.spmv_bicgstab(h, _ptr(b), _ptr(x), float(rtol), int(max_iter), _stream(stream), ctypes.byref(it),
                              ctypes.byref(res)))
+    return int(it.value), float(res.value)
+
+
+def spmv_gmres(h, b, x, restart, rtol, max_iter, stream=None):
+    """Restarted GMRES(restart) for A x = b (x holds the initial guess and receives the
+    iterate).  Returns (Arnoldi steps, true relative residual)."""
+    it = ctypes.c_int32(0)
+    res = ctypes.c_double(0.0)
+    _check(lib.spmv_gmres(h, _ptr(b), _ptr(x), int(restart), float(rtol), int(max_iter), _stream(stream),
+                          ctypes.byref(it), ctypes.byref(res)))
     return int(it.value), float(res.value)

@@ -658,6 +658,339 @@ int bicgstab(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, c
     return SPMV_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// GMRES(m) (Saad and Schultz), unpreconditioned, restarted
+// ---------------------------------------------------------------------------
+constexpr int kGmMax = 64;  // longest restart (Krylov dimension of a cycle)
+constexpr int kGmTile = 8;  // dot products a thread accumulates at once
+
+// Small state of a GMRES solve, in device memory.  H holds the rotated Hessenberg
+// matrix column by column: entry (i, j) at H[j * (kGmMax + 1) + i].
+struct GmScalars {
+    double tol;   // rtol * ||b|| (||b|| -> 1 when b = 0)
+    double beta;  // ||b - A x|| at the last restart
+    double inv;   // 1 / ||w|| (or 1 / beta) for the scale kernel
+    double d1[kGmMax + 1];  // V^T w, first Gram-Schmidt pass
+    double d2[kGmMax + 1];  // second pass
+    double H[(kGmMax + 1) * kGmMax];
+    double cs[kGmMax], sn[kGmMax];
+    double g[kGmMax + 1];
+    double y[kGmMax];
+    int32_t steps;       // Arnoldi steps of the running cycle
+    int32_t cycle_done;  // the running cycle has ended
+    int32_t max_iter;
+    int32_t m;
+};
+
+__device__ __forceinline__ void gm_publish(Progress *pg, const Control *ctl, const GmScalars *gs) {
+    volatile Progress *v = pg;
+    v->iterations = ctl->iterations;
+    v->stop = ctl->stop || gs->cycle_done;
+    __threadfence_system();
+}
+
+// True in every thread of the last block to finish; resets the arrival count.
+__device__ __forceinline__ bool last_block(Control *ctl) {
+    __shared__ bool is_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        is_last = atomicAdd(&ctl->arrivals, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (is_last) {
+        __threadfence();
+        if (threadIdx.x == 0) ctl->arrivals = 0;
+    }
+    return is_last;
+}
+
+// out[k] = V_k . w for k < nk (V_k at V + k * units), kGmTile dot products at a time;
+// per-block partials, then each sum over blocks in block order by one warp of the last
+// block.  which = 1 writes d1, 2 writes d2.
+template <typename T>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_gm_dot(int64_t units, const Pack<T> *__restrict__ V, int nk, const Pack<T> *__restrict__ w,
+             double *__restrict__ partial, Control *ctl, GmScalars *gs, int which) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop || gs->cycle_done) return;
+    using A = typename Acc<T>::type;
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int k0 = 0; k0 < nk; k0 += kGmTile) {
+        A acc[kGmTile];
+#pragma unroll
+        for (int t = 0; t < kGmTile; ++t) acc[t] = 0;
+        for (int64_t u = gtid(); u < units; u += st) {
+            const Pack<T> pw = w[u];
+#pragma unroll
+            for (int t = 0; t < kGmTile; ++t) {
+                if (k0 + t < nk) {
+                    const Pack<T> pv = V[static_cast<int64_t>(k0 + t) * units + u];
+#pragma unroll
+                    for (int l = 0; l < Pack<T>::L; ++l)
+                        acc[t] = fma(static_cast<A>(pv.v[l]), static_cast<A>(pw.v[l]), acc[t]);
+                }
+            }
+        }
+        for (int t = 0; t < kGmTile && k0 + t < nk; ++t) {
+            const double bs = block_sum(static_cast<double>(acc[t]));
+            if (threadIdx.x == 0) partial[static_cast<int64_t>(k0 + t) * gridDim.x + blockIdx.x] = bs;
+            __syncthreads();  // warp_sum is reused
+        }
+    }
+    if (!last_block(ctl)) return;
+    double *out = which == 1 ? gs->d1 : gs->d2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int k = warp; k < nk; k += kRedThreads / 32) {
+        double s = 0.0;
+        for (int i = lane; i < static_cast<int>(gridDim.x); i += 32) s += __ldcg(partial + static_cast<int64_t>(k) * gridDim.x + i);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) out[k] = s;
+    }
+}
+
+// Arnoldi column j, by one thread once ||w||^2 is summed: H(:, j) = d1 + d2 with
+// h_{j+1} = ||w||; the earlier rotations, the new one, the rotated right-hand side g
+// and the end-of-cycle test.
+__device__ void gm_column(Control *ctl, GmScalars *gs, Progress *pg, int j, double ww) {
+    const double hn = sqrt(ww);
+    double *col = gs->H + static_cast<int64_t>(j) * (kGmMax + 1);
+    for (int i = 0; i <= j; ++i) col[i] = gs->d1[i] + gs->d2[i];
+    col[j + 1] = hn;
+    for (int i = 0; i < j; ++i) {
+        const double a = col[i], b = col[i + 1];
+        col[i] = gs->cs[i] * a + gs->sn[i] * b;
+        col[i + 1] = -gs->sn[i] * a + gs->cs[i] * b;
+    }
+    const double rho = hypot(col[j], col[j + 1]);
+    const double c = rho > 0.0 ? col[j] / rho : 1.0;
+    const double s = rho > 0.0 ? col[j + 1] / rho : 0.0;
+    gs->cs[j] = c;
+    gs->sn[j] = s;
+    col[j] = c * col[j] + s * col[j + 1];
+    col[j + 1] = 0.0;
+    const double gj = gs->g[j];
+    gs->g[j + 1] = -s * gj;
+    gs->g[j] = c * gj;
+    gs->steps = j + 1;
+    ctl->iterations += 1;
+    const bool met = !(fabs(gs->g[j + 1]) > gs->tol);  // NaN ends the cycle too
+    if (met || hn == 0.0 || ctl->iterations >= gs->max_iter || j + 1 == gs->m) gs->cycle_done = 1;
+    gs->inv = hn > 0.0 ? 1.0 / hn : 0.0;
+    gm_publish(pg, ctl, gs);
+}
+
+// w += sign * sum_{k < nk} coef_k V_k, coef = d1 (which 1), d2 (2) or y (3); nk < 0 takes
+// the cycle's step count.  column >= 0: also ||w||^2, and the last block finishes
+// Arnoldi column `column`.  During a cycle (which 1, 2) the kernel does nothing once
+// the cycle has ended; the update of x (which 3) only once the solve has stopped.
+template <typename T>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_gm_axpy(int64_t units, const Pack<T> *__restrict__ V, int nk, int which, double sign, Pack<T> *__restrict__ w,
+              double *__restrict__ partial, Control *ctl, GmScalars *gs, Progress *pg, int column) {
+    __shared__ double s_coef[kGmMax + 1];
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop || (which != 3 && gs->cycle_done)) return;
+    if (nk < 0) nk = gs->steps;
+    const double *coef = which == 1 ? gs->d1 : which == 2 ? gs->d2 : gs->y;
+    for (int i = threadIdx.x; i < nk; i += blockDim.x) s_coef[i] = sign * coef[i];
+    __syncthreads();
+    using A = typename Acc<T>::type;
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    A ss = 0;
+    for (int64_t u = gtid(); u < units; u += st) {
+        Pack<T> pw = w[u];
+#pragma unroll 4
+        for (int k = 0; k < nk; ++k) {
+            const Pack<T> pv = V[static_cast<int64_t>(k) * units + u];
+            const T c = static_cast<T>(s_coef[k]);
+#pragma unroll
+            for (int l = 0; l < Pack<T>::L; ++l) pw.v[l] = fma(c, pv.v[l], pw.v[l]);
+        }
+        w[u] = pw;
+        if (column >= 0)
+#pragma unroll
+            for (int l = 0; l < Pack<T>::L; ++l) ss = fma(static_cast<A>(pw.v[l]), static_cast<A>(pw.v[l]), ss);
+    }
+    if (column < 0) return;
+    const double bs = block_sum(static_cast<double>(ss));
+    if (threadIdx.x == 0) partial[blockIdx.x] = bs;
+    if (!last_block(ctl)) return;
+    double s = 0.0;
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) s += __ldcg(partial + i);
+    const double total = block_sum(s);
+    if (threadIdx.x == 0) gm_column(ctl, gs, pg, column, total);
+}
+
+// v *= inv (the new basis vector, or r / beta at a restart)
+template <typename T>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_gm_scale(int64_t units, Pack<T> *__restrict__ v, Control *ctl, const GmScalars *gs) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop || gs->cycle_done) return;
+    const T inv = static_cast<T>(gs->inv);
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t u = gtid(); u < units; u += st) {
+        Pack<T> p = v[u];
+#pragma unroll
+        for (int l = 0; l < Pack<T>::L; ++l) p.v[l] *= inv;
+        v[u] = p;
+    }
+}
+
+// y = R^-1 g by back-substitution over the cycle's steps (one thread); a zero pivot
+// is a breakdown (stop = 2).
+__global__ void k_gm_solve(Control *ctl, GmScalars *gs, Progress *pg) {
+    if (threadIdx.x != 0 || ctl->stop) return;
+    const int n = gs->steps;
+    for (int i = n - 1; i >= 0; --i) {
+        const double piv = gs->H[static_cast<int64_t>(i) * (kGmMax + 1) + i];
+        if (piv == 0.0) {
+            ctl->stop = 2;
+            gm_publish(pg, ctl, gs);
+            return;
+        }
+        double t = gs->g[i];
+        for (int l = i + 1; l < n; ++l) t -= gs->H[static_cast<int64_t>(l) * (kGmMax + 1) + i] * gs->y[l];
+        gs->y[i] = t / piv;
+    }
+}
+
+// ||r|| at a restart (r = b - A x in v_0): the convergence test on the true residual,
+// then g = beta e_1 and a fresh cycle.
+template <typename T>
+__global__ void __launch_bounds__(kRedThreads, kRedBlocksPerSm)
+    k_gm_restart(int64_t units, const Pack<T> *__restrict__ r, double *__restrict__ partial, Control *ctl,
+                 GmScalars *gs, Progress *pg) {
+    allow_dependents();
+    grid_wait();
+    if (ctl->stop) return;
+    using A = typename Acc<T>::type;
+    const int64_t st = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    A ss = 0;
+    for (int64_t u = gtid(); u < units; u += st) {
+        const Pack<T> p = r[u];
+#pragma unroll
+        for (int l = 0; l < Pack<T>::L; ++l) ss = fma(static_cast<A>(p.v[l]), static_cast<A>(p.v[l]), ss);
+    }
+    const double bs = block_sum(static_cast<double>(ss));
+    if (threadIdx.x == 0) partial[blockIdx.x] = bs;
+    if (!last_block(ctl)) return;
+    double s = 0.0;
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) s += __ldcg(partial + i);
+    const double total = block_sum(s);
+    if (threadIdx.x == 0) {
+        const double beta = sqrt(total);
+        gs->beta = beta;
+        if (!(beta > gs->tol)) ctl->stop = 1;  // converged (NaN stops too)
+        gs->g[0] = beta;
+        for (int i = 1; i <= kGmMax; ++i) gs->g[i] = 0.0;
+        gs->steps = 0;
+        gs->cycle_done = 0;
+        gs->inv = beta > 0.0 ? 1.0 / beta : 0.0;
+        gm_publish(pg, ctl, gs);
+    }
+}
+
+
+template <typename T>
+int gmres(spmv_handle_t h, const T *b, T *x, int32_t m, double rtol, int32_t max_iter, cudaStream_t s,
+          int32_t *iterations, double *relative_residual) {
+    using P = Pack<T>;
+    const int64_t n = h->n;
+    const size_t vec = static_cast<size_t>(n) * sizeof(T);
+    const size_t vec_pad = (vec + 255) / 256 * 256;
+    const int64_t units = static_cast<int64_t>(vec_pad / sizeof(P));
+    // workspace: V (m + 1 vectors) | x (zero-padded) | partial sums ((kGmMax + 1) arrays) |
+    // GMRES scalars | control
+    StreamBuffer ws;
+    ws.s = s;
+    const size_t bytes = static_cast<size_t>(m + 2) * vec_pad + static_cast<size_t>(kGmMax + 1) * kRedBlocks * sizeof(double) +
+                         sizeof(GmScalars) + sizeof(Control);
+    SPMV_TRY_CUDA(cudaMallocAsync(&ws.ptr, bytes, s));
+    SPMV_TRY_CUDA(cudaMemsetAsync(ws.ptr, 0, bytes, s));
+    char *base = static_cast<char *>(ws.ptr);
+    P *V = reinterpret_cast<P *>(base);
+    P *xw = reinterpret_cast<P *>(base + static_cast<size_t>(m + 1) * vec_pad);
+    double *partial = reinterpret_cast<double *>(base + static_cast<size_t>(m + 2) * vec_pad);
+    GmScalars *gs = reinterpret_cast<GmScalars *>(partial + static_cast<size_t>(kGmMax + 1) * kRedBlocks);
+    Control *ctl = reinterpret_cast<Control *>(gs + 1);
+
+    // ||b|| for the tolerance (v_0 holds b meanwhile)
+    SPMV_TRY_CUDA(cudaMemcpyAsync(V, b, vec, cudaMemcpyDeviceToDevice, s));
+    SPMV_TRY_CUDA(launch(k_dot<T, 4>, s, units, static_cast<const P *>(V), static_cast<const P *>(V), partial, ctl,
+                         &gs->beta));
+    double bb = 0.0;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&bb, &gs->beta, sizeof(bb), cudaMemcpyDeviceToHost, s));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    const double denom = bb > 0.0 ? std::sqrt(bb) : 1.0;  // b = 0: absolute residual
+    const double tol = rtol * denom;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&gs->tol, &tol, sizeof(tol), cudaMemcpyHostToDevice, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&gs->max_iter, &max_iter, sizeof(max_iter), cudaMemcpyHostToDevice, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&gs->m, &m, sizeof(m), cudaMemcpyHostToDevice, s));
+
+    Pacer pace;
+    pace.s = s;
+    SPMV_TRY(pace.init());
+    // r = b - A x into v_0, its norm (the first convergence test) and v_0 = r / beta
+    SPMV_TRY_CUDA(cudaMemcpyAsync(xw, x, vec, cudaMemcpyDeviceToDevice, s));
+    SPMV_TRY(spmv_apply_ex(h, -1.0, xw, 1.0, V, s));
+    SPMV_TRY_CUDA(launch(k_gm_restart<T>, s, units, static_cast<const P *>(V), partial, ctl, gs, pace.dev));
+    SPMV_TRY_CUDA(launch(k_gm_scale<T>, s, units, V, ctl, static_cast<const GmScalars *>(gs)));
+
+    Control hc{};
+    for (;;) {
+        SPMV_TRY_CUDA(cudaMemcpyAsync(&hc, ctl, sizeof(hc), cudaMemcpyDeviceToHost, s));
+        SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+        if (hc.stop || hc.iterations >= max_iter) break;
+        // one cycle: Arnoldi steps paced on the progress record, which the step that ends
+        // the cycle marks stopped
+        pace.host->iterations = hc.iterations;
+        pace.host->stop = 0;
+        int32_t launched = hc.iterations;
+        for (int j = 0; j < m && launched < max_iter; ++j, ++launched) {
+            bool stop = false;
+            SPMV_TRY(pace.wait(launched, &stop));
+            if (stop) break;
+            P *vj = V + static_cast<int64_t>(j) * units;
+            P *w = V + static_cast<int64_t>(j + 1) * units;
+            SPMV_TRY(spmv_apply(h, vj, w, s));
+            SPMV_TRY_CUDA(launch(k_gm_dot<T>, s, units, static_cast<const P *>(V), j + 1, static_cast<const P *>(w),
+                                 partial, ctl, gs, 1));
+            SPMV_TRY_CUDA(launch(k_gm_axpy<T>, s, units, static_cast<const P *>(V), j + 1, 1, -1.0, w, partial, ctl,
+                                 gs, pace.dev, -1));
+            SPMV_TRY_CUDA(launch(k_gm_dot<T>, s, units, static_cast<const P *>(V), j + 1, static_cast<const P *>(w),
+                                 partial, ctl, gs, 2));
+            SPMV_TRY_CUDA(launch(k_gm_axpy<T>, s, units, static_cast<const P *>(V), j + 1, 2, -1.0, w, partial, ctl,
+                                 gs, pace.dev, j));
+            SPMV_TRY_CUDA(launch(k_gm_scale<T>, s, units, w, ctl, static_cast<const GmScalars *>(gs)));
+        }
+        // end of the cycle: y = R^-1 g, x += V y, then r = b - A x and the restart test
+        k_gm_solve<<<1, 32, 0, s>>>(ctl, gs, pace.dev);
+        SPMV_TRY_CUDA(cudaGetLastError());
+        SPMV_TRY_CUDA(launch(k_gm_axpy<T>, s, units, static_cast<const P *>(V), -1, 3, 1.0, xw, partial, ctl, gs,
+                             pace.dev, -1));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(V, b, vec, cudaMemcpyDeviceToDevice, s));
+        SPMV_TRY(spmv_apply_ex(h, -1.0, xw, 1.0, V, s));
+        SPMV_TRY_CUDA(launch(k_gm_restart<T>, s, units, static_cast<const P *>(V), partial, ctl, gs, pace.dev));
+        SPMV_TRY_CUDA(launch(k_gm_scale<T>, s, units, V, ctl, static_cast<const GmScalars *>(gs)));
+    }
+    double beta = 0.0;
+    SPMV_TRY_CUDA(cudaMemcpyAsync(x, xw, vec, cudaMemcpyDeviceToDevice, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(&beta, &gs->beta, sizeof(beta), cudaMemcpyDeviceToHost, s));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    if (iterations) *iterations = hc.iterations;
+    if (relative_residual) *relative_residual = beta / denom;
+    if (hc.stop == 2)
+        return set_error(SPMV_ERR_UNSUPPORTED, "GMRES broke down: zero pivot (A singular on the Krylov space)");
+    return SPMV_OK;
+}
+
 }  // namespace
 }  // namespace spmv
 
@@ -704,4 +1037,23 @@ extern "C" SPMV_API int spmv_bicgstab(spmv_handle_t h, const void *b, void *x, d
                                 iterations, relative_residual);
     return bicgstab<float>(h, static_cast<const float *>(b), static_cast<float *>(x), rtol, max_iter, s, iterations,
                            relative_residual);
+}
+
+extern "C" SPMV_API int spmv_gmres(spmv_handle_t h, const void *b, void *x, int32_t restart, double rtol,
+                                   int32_t max_iter, void *stream, int32_t *iterations, double *relative_residual) {
+    if (iterations) *iterations = 0;
+    if (relative_residual) *relative_residual = 0.0;
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    if (max_iter < 0 || !(rtol >= 0.0)) return set_error(SPMV_ERR_INVALID_ARG, "need max_iter >= 0 and rtol >= 0");
+    if (restart < 1 || restart > kGmMax)
+        return set_error(SPMV_ERR_INVALID_ARG, "restart must lie in [1, " + std::to_string(kGmMax) + "]");
+    if (h->n == 0) return SPMV_OK;
+    if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
+    if (overlapping(h, b, x)) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not overlap");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->dtype == SPMV_F64)
+        return gmres<double>(h, static_cast<const double *>(b), static_cast<double *>(x), restart, rtol, max_iter, s,
+                             iterations, relative_residual);
+    return gmres<float>(h, static_cast<const float *>(b), static_cast<float *>(x), restart, rtol, max_iter, s,
+                        iterations, relative_residual);
 }
