@@ -197,7 +197,8 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * x and y are device arrays of n elements of the handle's value type, in the
  * caller's original row order (any row permutation of the format is internal);
  * overlapping x and y are refused with SPMV_ERR_INVALID_ARG.
- * Asynchronous on `stream`: returns after enqueueing 1 to 4 kernel launches.
+ * Asynchronous on `stream`: returns after enqueueing 1 to 6 kernel launches (one for the
+ * SELL / ELLPACK-R plans AUTO picks; CSR-vector: one per row-length bin and the row-split).
  * The handle holds a small scratch array for the merge-path pass, so two applies
  * of the SAME handle must not run concurrently (on different streams); applies of
  * different handles may.  Empty rows give +0.
