@@ -97,7 +97,10 @@ typedef enum {
  *                       warps; 32 and 64 have compiled-in addressing).  Automatic = 32.
  *   sigma               SELL sort window in rows: 1 = no sort, >= n = global sort (pJDS).
  *   K                   HYB ELL width.  Automatic: the smallest K with
- *                       (value_bytes + 8) * #{rows longer than K} <= ld * (value_bytes + 4).
+ *                       4 * (value_bytes + 8) * #{rows longer than K} <= ld * (value_bytes + 4):
+ *                       each spilled entry's bytes count four times, since the spill pass
+ *                       costs about four times its bytes in time against the streamed ELL
+ *                       slots.
  *   spill_csr           HYB spill kind: 1 = CSR (HEC), 0 = COO (HYB).  Automatic = CSR.
  *   long_row_threshold  rows with more entries go to the row-split pass.  0 = never.
  *                       Automatic: 128 for SELL / ELLPACK-R, 256 for CSR-vector.

@@ -618,14 +618,20 @@ int probe_sigma1_slots(BuildCtx &c, int64_t *slots) {
     return sync(c.s);
 }
 
+// Byte weight of a spill entry against a streamed ELL slot in the HYB width rule: a spill
+// entry walked by the merge-path pass costs about four times its bytes in time (HYB on
+// the HMEp-shaped matrix: 322 us at the unweighted rule's K = 13, 232 at K = 17 from
+// weight 4; power-law: 369 us at K = 1, 342 at K = 3).
+constexpr int64_t kSpillWeight = 4;
+
 int32_t hyb_auto_width(const BuildCtx &c, int dtype, int64_t n, int32_t cap) {
-    // smallest K with (vb + 8) * #{len > K} <= ld * (vb + 4)
+    // smallest K with kSpillWeight * (vb + 8) * #{len > K} <= ld * (vb + 4)
     const int64_t vb = static_cast<int64_t>(value_bytes(dtype));
     const int64_t ld = ceil_div(std::max<int64_t>(n, 1), 256) * 256;
     int64_t longer = n;  // #{len > K} for K = -1
     int32_t K = 0;
     longer -= c.hist[0];
-    while (K < cap && K < kHistCap && (vb + 8) * longer > ld * (vb + 4)) {
+    while (K < cap && K < kHistCap && kSpillWeight * (vb + 8) * longer > ld * (vb + 4)) {
         ++K;
         longer -= c.hist[K];
     }

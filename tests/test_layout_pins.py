@@ -99,15 +99,16 @@ def test_excluded_rows_count_as_empty():
     assert lay["perm"].tolist() == [5, 0, 2, 3, 4, 1]
 
 
+@pytest.mark.parametrize("c", [1.0, 4.0])
 @pytest.mark.parametrize("seed", range(8))
 @pytest.mark.parametrize("value_bytes", [4, 8])
-def test_hyb_width_minimises_byte_model(seed, value_bytes):
+def test_hyb_width_minimises_byte_model(seed, value_bytes, c):
     rng = np.random.default_rng(seed)
     n = int(rng.integers(1, 3000))
     lens = np.minimum(rng.zipf(1.5 + seed * 0.2, size=n), 400)
     ld = layout.ell_leading_dim(n)
-    K = layout.hyb_width(lens, value_bytes, ld)
-    costs = [layout.hyb_modeled_bytes(lens, k, value_bytes, ld) for k in range(int(lens.max()) + 1)]
+    K = layout.hyb_width(lens, value_bytes, ld, c=c)
+    costs = [layout.hyb_modeled_bytes(lens, k, value_bytes, ld, c=c) for k in range(int(lens.max()) + 1)]
     best = min(costs)
     assert costs[K] == best
     assert all(c > best for c in costs[:K])  # smallest minimiser
