@@ -543,7 +543,7 @@ SWEEP_FORMATS = [
     ("auto", {}), ("csr_vector", {}), ("ell_r", {}),
     ("sell", {"C": 32, "sigma": 1}), ("sell", {"C": 64, "sigma": 1}), ("sell", {"C": 32, "sigma": 256}),
     ("sell", {"C": 64, "sigma": 256}), ("sell", {"C": 32, "sigma": 1 << 30}), ("sell", {"C": 64, "sigma": 1 << 30}),
-    ("hyb", {}), ("hyb", {"spill_csr": 0}), ("hyb", {"K": 20}), ("merge", {}),
+    ("hyb", {}), ("hyb", {"spill_csr": 1}), ("hyb", {"K": 20}), ("merge", {}),
     ("sell", {"row_threads": 1}), ("sell", {"row_threads": 2}), ("sell", {"row_threads": 4}), ("sell", {"row_threads": 8}),
     ("sell", {"row_threads": 16}), ("sell", {"row_threads": 32}), ("sell", {"row_threads": 4, "row_group_mode": 0}),
     ("sell", {"row_threads": 8, "row_group_mode": 0}), ("sell", {"row_threads": 2, "row_group_mode": 2}),

@@ -101,7 +101,8 @@ typedef enum {
  *                       each spilled entry's bytes count four times, since the spill pass
  *                       costs about four times its bytes in time against the streamed ELL
  *                       slots.
- *   spill_csr           HYB spill kind: 1 = CSR (HEC), 0 = COO (HYB).  Automatic = CSR.
+ *   spill_csr           HYB spill kind: 1 = CSR (HEC), 0 = COO (HYB).  Automatic = COO
+ *                       (faster on the irregular matrices measured).
  *   long_row_threshold  rows with more entries go to the row-split pass.  0 = never.
  *                       Automatic: 128 for SELL / ELLPACK-R, 256 for CSR-vector.
  *   subwarp             CSR-vector lanes per row (2, 4, 8, 16 or 32) for every row;
