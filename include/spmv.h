@@ -203,9 +203,10 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * overlapping x and y are refused with SPMV_ERR_INVALID_ARG.
  * Asynchronous on `stream`: returns after enqueueing 1 to 6 kernel launches (one for the
  * SELL / ELLPACK-R plans AUTO picks; CSR-vector: one per row-length bin and the row-split).
- * The handle holds a small scratch array for the merge-path pass, so two applies
- * of the SAME handle must not run concurrently (on different streams); applies of
- * different handles may.  Empty rows give +0.
+ * The handle holds small scratch arrays (the carries of the merge-path and COO passes,
+ * the chunk partials and counters of the row-split pass), so two applies of the SAME
+ * handle must not run concurrently (on different streams); applies of different
+ * handles may.  Empty rows give +0.
  */
 SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
 
@@ -443,8 +444,8 @@ SPMV_API int spmv_get_slots(spmv_handle_t h, int32_t *col, void *val, void *stre
  * allocations, or a time-critical loop that cannot afford the implicit device
  * synchronisation of cudaMalloc / cudaFree -- and therefore cannot build a handle.
  *
- * The computation is the load-balanced merge-path pass used for long rows,
- * applied to every row; y is overwritten.  Its only scratch (one partial sum per
+ * The computation is the load-balanced merge-path pass of the `merge` format (and of
+ * HYB's CSR spill), applied to every row; y is overwritten.  Its only scratch (one partial sum per
  * 2048-item share of the work) sits in a fixed 768 KiB array inside this
  * library's device image, which every GPU that loads the library keeps until the
  * process exits.  Hence:
