@@ -1,6 +1,6 @@
-// Load-balanced passes: merge-path over a compact CSR (long rows, HEC spill, or
-// every row), load-balanced COO (HYB spill), and the carry fix-up for rows that
-// cross CTA boundaries.  Equal work shares per CTA regardless of row lengths
+// Load-balanced passes: merge-path over a compact CSR (the HEC spill of HYB, or every
+// row of the merge format and of the allocation-free entry point), load-balanced COO
+// (the HYB spill), and the carry fix-up for rows that cross CTA boundaries.  Equal work shares per CTA regardless of row lengths
 // (merge-path split named in the Trilinos issue on unpackAndCombine; load-balanced
 // COO of the scite report's abstract).  No atomics.
 #include <cuda_runtime.h>
@@ -82,7 +82,7 @@ __device__ __forceinline__ T seg_scan_exclusive(int f, T v, SegScan<T, THREADS> 
 }
 
 // ---------------------------------------------------------------------------
-// merge-path over a compact CSR (long rows, or the HEC spill)
+// merge-path over a compact CSR (the HEC spill, or every row)
 // ---------------------------------------------------------------------------
 // Shared-memory slot of path item i.  Thread t walks items t*kMergeIpt .. +kMergeIpt-1,
 // so a plain layout puts the 32 lanes of a warp kMergeIpt words apart (an 8- or
