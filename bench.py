@@ -1,16 +1,23 @@
 #!/usr/bin/env python
-"""Benchmark of the GB300 SpMV library on the 3D 7-point Laplacian 128^3.
+"""Benchmark of the GB300 SpMV library on every configuration of the metric.
 
-One step = one y = A x (every kernel of the handle's apply plan) over the matrix
-already resident in HBM; the format is built once before timing (build time is
-reported separately).  Headline: float64; float32 is measured in the same run.
+One step = one y = A x (every kernel of the handle's apply plan) over a matrix already
+resident in HBM; the format is AUTO, built once before timing (build time is reported
+separately).  The five workloads are timed in one run: the 2D Laplacian 256^2 (fp64,
+also under a CUDA graph: it fits in L2), the 3D Laplacian 128^3 (fp64 and fp32), the
+HMEp-shaped matrix (fp64), the power-law matrix (fp64) and the random uniform matrix
+(fp32).  The headline is the largest, the random uniform matrix (16.8 M rows, 268 M
+entries); the others are sub-records of the same JSON line, each with its roofline,
+its L2-flushed figure and its format.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload all|NAME]
 
-Prints ONE JSON line (rank 0).  GFLOP/s = 2 nnz / t; effective GB/s uses the
-algorithmic bytes nnz (value + int32 index) + (n + 1) int32 row pointers + n
-values of x + n values of y.  Multi-GPU runs are independent replicas (one
-process per GPU, no collective on the data path); ``value`` is the aggregate.
+Each configuration: W warm-up applies, then 11 timed regions of K back-to-back applies
+(barrier + synchronize around each); value and ms_per_step come from the median region,
+with p10/p90 beside them.  GFLOP/s = 2 nnz / t; effective GB/s uses the algorithmic
+bytes nnz (value + int32 index) + (n + 1) int32 row pointers + n values of x + n values
+of y.  Multi-GPU runs are independent replicas (one process per GPU, no collective on
+the data path); ``value`` is the aggregate.
 """
 from __future__ import annotations
 
@@ -124,10 +131,6 @@ def kernel_source(kernel: str) -> str:
 
 
 #: headers every kernel source includes; a change there changes the kernels too
-# row blocks of the pipelined host path timed beside the default e2e (best of 2-16 blocks
-# on the 3D Laplacian and the HMEp-shaped matrix in float64)
-E2E_HOST_BLOCKS = 8
-
 KERNEL_HEADERS = ("spmv_internal.cuh", "device_util.cuh", "sell_common.cuh")
 
 
@@ -238,89 +241,258 @@ def _gpu_id(torch):
         return None
 
 
-def measure_device(torch, spmv, csr, x_np, steps, warmup, sampler=None, fmt="auto"):
-    """Build once, then time `steps` back-to-back applies with CUDA events on the stream."""
-    dev = torch.device("cuda", torch.cuda.current_device())
-    rp = torch.from_numpy(csr.row_ptr).to(dev)
-    ci = torch.from_numpy(csr.col_idx).to(dev)
-    vv = torch.from_numpy(csr.vals).to(dev)
+#: every configuration the metric is quoted on, in run order: (workload, value type)
+BENCH_CONFIGS = [
+    ("lap2d_256", "f64"),
+    ("lap3d_128", "f64"),
+    ("lap3d_128", "f32"),
+    ("hmep_6p2m", "f64"),
+    ("powerlaw_4m", "f64"),
+    ("uniform16_16m", "f32"),
+]
+#: the headline: the largest configuration (16.8 M rows, 268 M entries)
+HEADLINE = ("uniform16_16m", "f32")
+#: timed regions of K applies each; the line reports their median and spread
+REPEATS = 11
+#: matrices small enough to sit in L2: timed under a CUDA graph, flagged "not HBM-bound"
+GRAPH_TIMED = ("lap2d_256",)
+#: applies captured per CUDA graph for the launch-bound configurations
+APPLIES_PER_GRAPH = 100
+#: gathers of the random-gather probe (about 1 ms on a GB300)
+PROBE_GATHERS = 1 << 28
+
+
+def np_dtype(tag: str):
+    import numpy as np
+
+    return np.float64 if tag == "f64" else np.float32
+
+
+def percentile(values, q):
+    v = sorted(values)
+    if not v:
+        return None
+    k = (len(v) - 1) * q
+    lo, hi = int(k), min(int(k) + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (k - lo)
+
+
+def random_gather_sectors(csr, threshold: int = 128) -> dict:
+    """x sectors (32 bytes) a warp instruction of the AUTO plan touches, summed over one apply.
+    Rows of at most `threshold` entries sit in the sliced layout, where a warp instruction
+    covers one entry of 32 different rows: with random columns every such gather is a
+    sector of its own.  Longer rows go to the row-split pass, whose warp instruction covers
+    32 consecutive entries of one row: their distinct sectors are counted exactly (columns
+    sorted within a row, so a new sector starts where col // (32 / value bytes) changes)."""
+    import numpy as np
+
+    lens = np.diff(csr.row_ptr.astype(np.int64))
+    per_sector = 32 // csr.vals.dtype.itemsize
+    short = int(lens[lens <= threshold].sum())
+    long_sectors = 0
+    for r in np.nonzero(lens > threshold)[0]:
+        a, b = int(csr.row_ptr[r]), int(csr.row_ptr[r + 1])
+        sec = csr.col_idx[a:b].astype(np.int64) // per_sector
+        new = np.ones(sec.size, dtype=bool)
+        new[1:] = sec[1:] != sec[:-1]
+        new[::32] = True  # each warp instruction starts afresh (chunks are multiples of 32)
+        long_sectors += int(new.sum())
+    return {"short_row_gathers": short, "long_row_sectors": long_sectors, "sectors": short + long_sectors,
+            "model": "sliced rows: one sector per entry; row-split chunks: distinct sectors per 32 consecutive "
+                     "entries"}
+
+
+def probe_gather_rate(torch, spmv, x) -> float:
+    """Random gathers per second from x (spmv_probe_gather), best of 5 launches."""
+    dev = x.device
+    out = torch.zeros(1, dtype=torch.float64, device=dev)
+    code = 0 if x.dtype == torch.float64 else 1
+    stream = torch.cuda.current_stream()
+    spmv.spmv_probe_gather(x, x.numel(), code, PROBE_GATHERS, out, stream)  # warm-up
+    rates = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        done = spmv.spmv_probe_gather(x, x.numel(), code, PROBE_GATHERS, out, stream)
+        e1.record(stream)
+        e1.synchronize()
+        rates.append(done / (e0.elapsed_time(e1) / 1e3))
+    return max(rates)
+
+
+def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, sampler, peak, peak_kind, keep=False):
+    """Build one workload with AUTO, then time REPEATS regions of `steps` back-to-back
+    applies (barrier + synchronize on both sides of each), an L2-flushed apply, the
+    per-kernel split and, for L2-resident matrices, applies captured in a CUDA graph."""
+    import numpy as np
+
+    from workloads import WORKLOADS, make_workload
+
+    t_gen = time.perf_counter()
+    csr, x_np = make_workload(name, dtype=np_dtype(tag))
+    gen_s = time.perf_counter() - t_gen
+    n, nnz, sv = csr.n, csr.nnz, csr.vals.dtype.itemsize
+    dev = torch.device("cuda", dev_index)
+    rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
     x = torch.from_numpy(x_np).to(dev)
     y = torch.empty_like(x)
     torch.cuda.synchronize()
     t_b = time.perf_counter()
-    A = spmv.SpmvMatrix.from_csr(rp, ci, vv, format=fmt)
+    A = spmv.SpmvMatrix.from_csr(rp, ci, vv)
     build_ms = (time.perf_counter() - t_b) * 1e3
     desc = A.describe()
     stream = torch.cuda.current_stream()
-    # the C entry point itself, with its arguments marshalled once
-    apply_c = spmv._abi.lib.spmv_apply
+    apply_c = spmv._abi.lib.spmv_apply  # the C entry point, arguments marshalled once
     args = (A._h, x.data_ptr(), y.data_ptr(), stream.cuda_stream or None)
     rc = 0
     for _ in range(warmup):
         rc |= apply_c(*args)
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if sampler:
-        sampler.mark()
-    t0 = time.time()
-    e0.record(stream)
-    for _ in range(steps):
-        rc |= apply_c(*args)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    regions, t0, t1 = [], None, None
+    for _ in range(REPEATS):
+        barrier(world, dev_index)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if t0 is None:
+            t0 = time.time()
+        e0.record(stream)
+        for _ in range(steps):
+            rc |= apply_c(*args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world, dev_index)
+        regions.append(e0.elapsed_time(e1))
     t1 = time.time()
     if rc:
-        raise RuntimeError(f"spmv_apply failed: {spmv.spmv_last_error_message()}")
-    region_ms = e0.elapsed_time(e1)
+        raise RuntimeError(f"spmv_apply failed on {name}: {spmv.spmv_last_error_message()}")
+    median_ms = statistics.median(regions)
+    region_ms = reduce_max(median_ms, world, device=dev)
     # per-kernel split of one apply (separate, event-bracketed launches)
-    splits = [A.apply_profiled(x, y) for _ in range(20)]
+    splits = [A.apply_profiled(x, y) for _ in range(10)]
     per_kernel = [statistics.median(s[i] for s in splits) for i in range(len(splits[0]))]
-    # cold: L2 flushed before every apply (flush outside the events)
+    # cold: L2 flushed (a write of twice its size) before every apply, outside the events
     flush = torch.empty(int(2 * device_l2_bytes(torch)) // 4, dtype=torch.float32, device=dev)
     cold = []
-    for _ in range(30):
+    for _ in range(15):
         flush.fill_(1.0)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        A.apply(x, y)
+        apply_c(*args)
         b.record(stream)
         b.synchronize()
         cold.append(a.elapsed_time(b))
     del flush
+    graph_ms = None
+    if name in GRAPH_TIMED:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                apply_c(A._h, x.data_ptr(), y.data_ptr(), s.cuda_stream)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream().cuda_stream
+            for _ in range(APPLIES_PER_GRAPH):
+                apply_c(A._h, x.data_ptr(), y.data_ptr(), cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(REPEATS):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            reps.append(e0.elapsed_time(e1) / APPLIES_PER_GRAPH)
+        graph_ms = statistics.median(reps)
+        del g
+    gather = None
+    if name.startswith(("powerlaw", "uniform")):
+        sectors = random_gather_sectors(csr)
+        rate = probe_gather_rate(torch, spmv, x)
+        bound_ms = sectors["sectors"] / rate * 1e3
+        gather = {"probe_gathers_per_s": rate, **sectors, "bound_ms": bound_ms,
+                  "frac_of_gather_bound": bound_ms / (region_ms / steps),
+                  "hbm_frac_at_gather_bound": effective_bytes(n, nnz, sv) / (bound_ms / 1e3) / 1e9 / peak,
+                  "probe": "spmv_probe_gather on this x: random indices, 8 gathers in flight per thread, a full "
+                           "wave of threads, best of 5 launches of 2^28 gathers"}
     A.close()
-    return {"region_ms": region_ms, "t0": t0, "t1": t1, "build_ms": build_ms, "desc": desc,
-            "per_kernel_ms": per_kernel, "cold_ms": statistics.median(cold)}
+    del rp, ci, vv, x, y
+    torch.cuda.empty_cache()
+
+    beff = effective_bytes(n, nnz, sv)
+    kernels = desc["kernels"]
+    ms = region_ms / steps
+    if len(kernels) == 1:
+        kernel_ms = ms
+        note = ("single-kernel plan: launch duration = median timed region / steps (consecutive launches "
+                "overlap through programmatic dependent launch, so this is the launch-to-launch interval)")
+    else:
+        dom = max(range(len(per_kernel)), key=lambda i: per_kernel[i])
+        kernel_ms = ms * per_kernel[dom] / sum(per_kernel)
+        note = f"{kernels[dom]} share {per_kernel[dom] / sum(per_kernel):.3f} of the event-timed apply"
+    dom_kernel = kernels[0] if len(kernels) == 1 else kernels[max(range(len(per_kernel)), key=lambda i: per_kernel[i])]
+    cold_ms = statistics.median(cold)
+    l2 = device_l2_bytes(torch)
+    rec = {
+        "workload": name, "dtype": tag, "desc": WORKLOADS[name]["desc"], "n": n, "nnz": nnz,
+        "value": 2.0 * nnz * world / (ms / 1e3) / 1e9, "unit": UNIT,
+        "ms_per_step": ms, "ms_per_step_p10": percentile(regions, 0.1) / steps,
+        "ms_per_step_p90": percentile(regions, 0.9) / steps, "regions": REPEATS, "steps_per_region": steps,
+        "effective_gbs": beff / (ms / 1e3) / 1e9,
+        "cold_ms_per_step": cold_ms, "cold_effective_gbs": beff / (cold_ms / 1e3) / 1e9,
+        "build_ms": build_ms, "generate_s": gen_s,
+        "format": {k: desc[k] for k in ("format", "C", "sigma", "K", "slots", "padded_entries", "n_long_rows",
+                                        "segment", "kernels")},
+        "per_kernel_ms": per_kernel,
+        "l2": ("stream larger than L2: back-to-back applies" if beff > l2 else
+               "stream fits in L2: back-to-back figures include L2 reuse; the cold (L2-flushed) figure is the "
+               "HBM one"),
+        "roofline": {"bound": "hbm", "achieved": beff / (kernel_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": beff / (kernel_ms / 1e3) / 1e9 / peak,
+                     "frac_cold": beff / (cold_ms / 1e3) / 1e9 / peak,
+                     "traffic": committed_traffic(name, tag, dom_kernel), "kernel": dom_kernel,
+                     "algorithmic_bytes_per_launch": beff, "peak_source": f"{peak_kind} (hbm_gbs)", "note": note},
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+    }
+    if graph_ms is not None:
+        rec["graph"] = {"ms_per_step": graph_ms, "applies_per_graph": APPLIES_PER_GRAPH,
+                        "value": 2.0 * nnz / (graph_ms / 1e3) / 1e9, "effective_gbs": beff / (graph_ms / 1e3) / 1e9,
+                        "frac": beff / (graph_ms / 1e3) / 1e9 / peak,
+                        "note": "not HBM-bound: the matrix fits in L2; launch and latency figures"}
+    if gather:
+        rec["gather_roofline"] = gather
+    if keep:
+        rec["_csr"], rec["_x"] = csr, x_np
+    return rec
 
 
-def measure_e2e(torch, spmv, csr, x_np, steps, mapped=False, host_blocks=-1):
-    """Public API with host buffers, wall clock over `steps` calls.  Copy path
-    (spmv_apply_host): H2D of x, apply, D2H of y every step (pipelined by row blocks
-    when the handle's plan allows it).  Mapped path (spmv_apply_mapped): the kernels
-    read x from and write y to the page-locked host arrays directly.  Returns the time
-    and the row blocks of the last host call (0 = unpipelined)."""
+def measure_e2e(torch, spmv, csr, x_np, steps):
+    """The public host-buffer call (spmv_apply_host) timed by wall clock over `steps`
+    calls: every call copies x from page-locked host memory to the device, applies, moves
+    y back to page-locked host memory and waits for the stream."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    rp = torch.from_numpy(csr.row_ptr).to(dev)
-    ci = torch.from_numpy(csr.col_idx).to(dev)
-    vv = torch.from_numpy(csr.vals).to(dev)
-    with spmv.SpmvMatrix.from_csr(rp, ci, vv, host_blocks=host_blocks) as A:
+    rp, ci, vv = (torch.from_numpy(a).to(dev) for a in (csr.row_ptr, csr.col_idx, csr.vals))
+    with spmv.SpmvMatrix.from_csr(rp, ci, vv) as A:
         xt = torch.from_numpy(x_np).pin_memory()
         yt = torch.empty(csr.n, dtype=xt.dtype).pin_memory()
         xh, yh = xt.numpy(), yt.numpy()
-        call = (lambda: spmv.spmv_apply_mapped(A._h, xt, yt)) if mapped else (lambda: A.apply_host(xh, yh))
         for _ in range(3):
-            call()
+            A.apply_host(xh, yh)
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(steps):
-            call()
-        t = time.perf_counter() - t0
-        blocks = A.describe().get("host_pipeline_blocks", 0)
-    return t, blocks
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                A.apply_host(xh, yh)
+            times.append(time.perf_counter() - t0)
+    return statistics.median(times)
 
 
-def cpu_baseline(csr, x_np, budget_s=8.0):
+def cpu_baseline(csr, x_np, budget_s=10.0):
     """The oracle as it stands (single thread, long double) on a row prefix sized to the budget."""
     import numpy as np
 
@@ -371,126 +543,86 @@ def cpu_openmp_baseline(csr, x_np, schedule):
             "sample": "the full workload, median of 11 applies, value-type sums"}
 
 
+def selected_configs(workload: str):
+    """(configs to time, headline) for --workload: all five, or one workload's value types."""
+    from workloads import WORKLOADS
+
+    if workload == "all":
+        return list(BENCH_CONFIGS), HEADLINE
+    picked = [c for c in BENCH_CONFIGS if c[0] == workload]
+    if not picked:
+        dt = WORKLOADS[workload]["dtype"]
+        picked = [(workload, "f64" if dt == __import__("numpy").float64 else "f32")]
+    return picked, picked[0]
+
+
 def run_ours(args):
-    import numpy as np
     import torch
 
     import sparse_matrix_vector_csr_gb300 as spmv
-    from workloads import WORKLOADS, make_workload
+    from workloads import WORKLOADS
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     init_dist(world, "nccl")
     dev_index = torch.cuda.current_device()
-
-    csr64, x64 = make_workload(args.workload, dtype=np.float64)
-    csr32, x32 = csr64.astype(np.float32), x64.astype(np.float32)
-    n, nnz = csr64.n, csr64.nnz
-
+    peak, peak_kind = load_peaks()
+    configs, headline = selected_configs(args.workload)
     sampler = ClockSampler(_gpu_id(torch)) if rank == 0 else None
-    results = {}
-    for tag, csr, x in (("f64", csr64, x64), ("f32", csr32, x32)):
-        barrier(world, dev_index)
-        r = measure_device(torch, spmv, csr, x, args.steps, args.warmup, sampler if tag == "f64" else None,
-                           fmt=args.format)
-        barrier(world, dev_index)
-        r["region_ms_max"] = reduce_max(r["region_ms"], world, device=torch.device("cuda", dev_index))
-        results[tag] = r
-    if sampler:
-        sampler.stop()
-    clocks = sampler.summary(results["f64"]["t0"], results["f64"]["t1"]) if sampler else None
-
-    e2e_steps = min(args.steps, 500)
-    e2e_t, e2e_blocks = measure_e2e(torch, spmv, csr64, x64, e2e_steps)
-    e2e_t = reduce_max(e2e_t, world, device=torch.device("cuda", dev_index))
-    e2e_mapped_t, _ = measure_e2e(torch, spmv, csr64, x64, e2e_steps, mapped=True)
-    e2e_mapped_t = reduce_max(e2e_mapped_t, world, device=torch.device("cuda", dev_index))
-    e2e_pipe_t, e2e_pipe_blocks = measure_e2e(torch, spmv, csr64, x64, e2e_steps, host_blocks=E2E_HOST_BLOCKS)
-    e2e_pipe_t = reduce_max(e2e_pipe_t, world, device=torch.device("cuda", dev_index))
-
+    records = {}
+    try:
+        for name, tag in configs:
+            records[(name, tag)] = measure_config(torch, spmv, name, tag, args.steps, args.warmup, world, dev_index,
+                                                  sampler, peak, peak_kind, keep=(name, tag) == headline)
+    finally:
+        if sampler:
+            sampler.stop()
+    head = records[headline]
+    csr, x_np = head.pop("_csr"), head.pop("_x")
+    e2e_steps = max(args.steps, 3)
+    e2e_t = reduce_max(measure_e2e(torch, spmv, csr, x_np, e2e_steps), world,
+                       device=torch.device("cuda", dev_index))
     if rank != 0:
         return
+    sv = csr.vals.dtype.itemsize
     l2_bytes = device_l2_bytes(torch)
-    peak, peak_kind = load_peaks()
-
-    def summarize(tag, sv):
-        r = results[tag]
-        sec = r["region_ms_max"] / 1e3
-        steps = args.steps
-        gflops = aggregate_rate(2.0 * nnz * steps, world, sec) / 1e9
-        beff = effective_bytes(n, nnz, sv)
-        eff_gbs = aggregate_rate(beff * steps, world, sec) / 1e9
-        kernels = r["desc"]["kernels"]
-        pk = r["per_kernel_ms"]
-        dom = max(range(len(pk)), key=lambda i: pk[i]) if pk else 0
-        if len(kernels) == 1:
-            kernel_ms = r["region_ms"] / steps
-            note = ("single-kernel plan: launch duration = timed region / steps (consecutive launches overlap "
-                    "through programmatic dependent launch, so this is the launch-to-launch interval)")
-        else:
-            share = pk[dom] / sum(pk)
-            kernel_ms = r["region_ms"] / steps * share
-            note = f"{kernels[dom]} share {share:.3f} of the event-timed apply"
-        achieved = beff / (kernel_ms / 1e3) / 1e9
-        traffic = committed_traffic(args.workload, tag, kernels[dom] if kernels else "")
-        return {
-            "value": gflops, "effective_gbs": eff_gbs, "ms_per_step": r["region_ms_max"] / steps,
-            "cold_ms_per_step": r["cold_ms"], "cold_effective_gbs": beff / (r["cold_ms"] / 1e3) / 1e9,
-            "build_ms": r["build_ms"],
-            "format": {k: r["desc"][k] for k in ("format", "C", "sigma", "K", "slots", "padded_entries",
-                                                 "n_long_rows", "segment", "kernels")},
-            "per_kernel_ms": pk,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "kernel": kernels[dom] if kernels else None,
-                         "algorithmic_bytes_per_launch": beff, "peak_source": f"{peak_kind} (hbm_gbs)",
-                         "note": note},
-        }
-
-    s64 = summarize("f64", 8)
-    s32 = summarize("f32", 4)
-    e2e_value = aggregate_rate(2.0 * nnz * e2e_steps, world, e2e_t) / 1e9
-    e2e_mapped_value = aggregate_rate(2.0 * nnz * e2e_steps, world, e2e_mapped_t) / 1e9
-    e2e_pipe_value = aggregate_rate(2.0 * nnz * e2e_steps, world, e2e_pipe_t) / 1e9
+    beff = effective_bytes(csr.n, csr.nnz, sv)
     line = {
-        "metric": METRIC, "value": s64["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": s64["ms_per_step"], "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": headline[1], "data": "synthetic",
         "config": {
-            "workload": WORKLOADS[args.workload]["desc"] + f" (nnz={nnz}), float64 headline, float32 beside it",
-            "n": n, "nnz": nnz, "format": s64["format"]["format"], "parallelism": "replicas" if world > 1 else "single",
-            "l2": (f"inputs larger than L2: one apply streams {effective_bytes(n, nnz, 8) / 1e6:.0f} MB (f64) / "
-                   f"{effective_bytes(n, nnz, 4) / 1e6:.0f} MB (f32) > {l2_bytes / 1e6:.0f} MB L2, applies back to "
-                   "back; cold_* fields flush L2 before every apply"),
+            "workload": f"{WORKLOADS[headline[0]]['desc']} (nnz={csr.nnz}), {'float64' if sv == 8 else 'float32'}",
+            "n": csr.n, "nnz": csr.nnz, "format": head["format"]["format"],
+            "parallelism": "replicas" if world > 1 else "single",
+            "timing": (f"{REPEATS} timed regions of {args.steps} back-to-back applies after {args.warmup} warm-up "
+                       "applies, barrier + synchronize around each region; value and ms_per_step from the median "
+                       "region (max over ranks), p10/p90 beside it"),
+            "l2": (f"inputs larger than L2: one apply streams {beff / 1e6:.0f} MB > {l2_bytes / 1e6:.0f} MB L2"
+                   if beff > l2_bytes else f"stream of {beff / 1e6:.0f} MB fits in the {l2_bytes / 1e6:.0f} MB L2; "
+                                           "cold_* fields flush L2 before every apply"),
             "l2_bytes": int(l2_bytes),
+            "configs": [f"{n_}:{t_}" for n_, t_ in configs],
         },
-        "effective_gbs": s64["effective_gbs"],
-        "roofline": s64["roofline"],
-        "gpu_launches": args.steps * len(s64["format"]["kernels"]),
-        "e2e": {"value": e2e_value, "unit": UNIT, "steps": e2e_steps,
-                "h2d_bytes_per_step": n * 8, "d2h_bytes_per_step": n * 8,
-                "host_pipeline_blocks": e2e_blocks,
-                "note": ("spmv_apply_host: pinned x -> device, apply, y -> pinned host, stream sync each step; "
-                         + (f"pipelined in {e2e_blocks} row blocks (pieces of x in, blocks multiplied as their "
-                            "columns arrive, rows of y back on a second copy stream)" if e2e_blocks > 0
-                            else "unpipelined"))},
-        "e2e_mapped": {"value": e2e_mapped_value, "unit": UNIT, "steps": e2e_steps,
-                       "h2d_bytes_per_step": n * 8, "d2h_bytes_per_step": n * 8,
-                       "note": "spmv_apply_mapped: the kernels gather x from and store y to the page-locked "
-                               "host arrays over the CPU-GPU link (no staging copies), stream sync each step"},
-        "e2e_pipelined": {"value": e2e_pipe_value, "unit": UNIT, "steps": e2e_steps,
-                          "h2d_bytes_per_step": n * 8, "d2h_bytes_per_step": n * 8,
-                          "host_blocks": E2E_HOST_BLOCKS, "host_pipeline_blocks": e2e_pipe_blocks,
-                          "note": "spmv_apply_host with the opt-in copy/compute pipeline: x in by pieces, row "
-                                  "blocks multiplied as their columns arrive, rows of y back on a second copy "
-                                  "stream, stream sync each step"},
-        "clocks": clocks,
-        "detail_f64": {k: v for k, v in s64.items() if k not in ("roofline",)},
-        "fp32": s32,
+        "ms_per_step_p10": head["ms_per_step_p10"], "ms_per_step_p90": head["ms_per_step_p90"],
+        "effective_gbs": head["effective_gbs"],
+        "roofline": head["roofline"],
+        "gpu_launches": args.steps * len(head["format"]["kernels"]),
+        "gpu_launches_note": "kernels of this library launched in one timed region (steps x launches per apply)",
+        "e2e": {"value": 2.0 * csr.nnz * e2e_steps * world / e2e_t / 1e9, "unit": UNIT, "steps": e2e_steps,
+                "h2d_bytes_per_step": csr.n * sv, "d2h_bytes_per_step": csr.n * sv,
+                "note": ("spmv_apply_host on the headline workload: page-locked x -> device, apply, y -> "
+                         "page-locked host, stream synchronised every call; median of 3 runs of `steps` calls")},
+        "clocks": head["clocks"],
+        "headline": {k: v for k, v in head.items() if k not in ("roofline", "clocks")},
+        "configs": [{k: v for k, v in records[c].items()} for c in configs if c != headline],
     }
+    if "gather_roofline" in head:
+        line["gather_roofline"] = head["gather_roofline"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(csr64, x64)
-        line["cpu_openmp"] = cpu_openmp_baseline(csr64, x64,
-                                                 "dynamic" if args.workload.startswith("powerlaw") else "static")
+        line["cpu_baseline"] = cpu_baseline(csr, x_np)
+        line["cpu_openmp"] = cpu_openmp_baseline(csr, x_np,
+                                                 "dynamic" if headline[0].startswith("powerlaw") else "static")
     print(json.dumps(line), flush=True)
 
 
@@ -508,7 +640,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    csr, x = make_workload(args.workload, dtype=np.float64)
+    _, headline = selected_configs(args.workload)
+    csr, x = make_workload(headline[0], dtype=np_dtype(headline[1]))
     total_steps = args.steps + args.warmup
     budget = 90.0
     probe = min(csr.n, 20000)
@@ -530,9 +663,10 @@ def run_reference(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOADS[args.workload]["desc"] + f" (nnz={csr.nnz}), float64", "n": csr.n,
-                   "nnz": csr.nnz},
+        "scaling": "weak", "vs_baseline": None, "dtype": headline[1], "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{WORKLOADS[headline[0]]['desc']} (nnz={csr.nnz}), "
+                               f"{'float64' if headline[1] == 'f64' else 'float32'}",
+                   "n": csr.n, "nnz": csr.nnz},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -829,7 +963,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="lap3d_128")
+    ap.add_argument("--workload", default="all",
+                    help="all = every configuration (headline: uniform16_16m); or one workload name")
     ap.add_argument("--format", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
@@ -845,6 +980,8 @@ def main(argv=None):
     ap.add_argument("--restart", type=int, default=30, help="with --solver gmres: the restart length m")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.workload == "all" and (args.sweep or args.graph or args.orderings or args.cg > 0):
+        args.workload = "lap3d_128"  # the single-workload modes
     if args.impl == "reference":
         run_reference(args)
     elif args.cg > 0:

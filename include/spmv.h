@@ -203,10 +203,16 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * overlapping x and y are refused with SPMV_ERR_INVALID_ARG.
  * Asynchronous on `stream`: returns after enqueueing 1 to 6 kernel launches (one for the
  * SELL / ELLPACK-R plans AUTO picks; CSR-vector: one per row-length bin and the row-split).
- * The handle holds small scratch arrays (the carries of the merge-path and COO passes,
- * the chunk partials and counters of the row-split pass), so two applies of the SAME
- * handle must not run concurrently (on different streams); applies of different
- * handles may.  Empty rows give +0.
+ * The apply only reads the handle's matrix data.  What it writes besides y (the carries
+ * of the merge-path and COO passes, the chunk partials and counters of the row-split
+ * pass) the handle keeps once per stream: the first apply of a handle on a stream
+ * allocates that stream's set (a few bytes per long row or per 2048 entries of the
+ * segmented part; the build's own stream gets its set during the build), and later
+ * applies on the stream reuse it in stream order.  So applies of one handle on
+ * different streams may run concurrently, and so may applies of different handles.
+ * The sets are keyed by the stream handle and live until spmv_destroy; a graph
+ * captured on a stream keeps using that stream's set, so replaying it concurrently
+ * with other work on the same stream races.  Empty rows give +0.
  */
 SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
 
@@ -225,8 +231,11 @@ SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
  *  - staged: x copied in, product, y copied out.
  * The result is the same in every way (the same kernel sums each row in the same
  * order).  x_host and y_host may be the same array (in place); such a call runs
- * unpipelined, with all of x on the device before any of y moves.  The device staging buffers, streams and events are created by the first
- * call on a handle and kept until spmv_destroy.
+ * unpipelined, with all of x on the device before any of y moves.  The device staging
+ * columns belong to the stream's scratch set (allocated on the first call on each
+ * stream); the pipeline's copy streams and events are created by the first call on a
+ * handle, kept until spmv_destroy, and shared, so pipelined calls of one handle run
+ * one at a time.
  */
 SPMV_API int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *stream);
 
@@ -256,9 +265,10 @@ SPMV_API int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *
  * form for residuals r = b - A x (alpha = -1, beta = 1 with y holding b), as the
  * Krylov iterations of the Krylov/AMG paper (BiCGSTAB algorithm) combine SpMV with
  * vector updates.  SELL and ELLPACK-R handles fold alpha and beta into the kernel's
- * single write of each row; the other formats compute A x into a scratch column of
- * the handle first.  x and y must not overlap.  Asynchronous; same stream rules as
- * spmv_apply.
+ * single write of each row; the other formats compute A x into a scratch column first
+ * (n values, allocated on the first such call on each stream and kept with the
+ * stream's scratch set).  x and y must not overlap.  Asynchronous; same stream rules
+ * as spmv_apply.
  */
 SPMV_API int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double beta, void *y, void *stream);
 
@@ -269,7 +279,8 @@ SPMV_API int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double 
  * of up to 8 vectors and each gather of a row of X fetches that row's values with
  * one or two wide loads (SELL handles, slice height 32 or 64; X aligned to
  * min(16, 8 * value size) bytes with ldx a multiple of that); other formats and
- * left-over columns go one column at a time through scratch columns of the handle.
+ * left-over columns go one column at a time through two scratch columns of the
+ * stream's scratch set (allocated on first need).
  * beta == 0: Y is not read.  k = 0 is a no-op.  X and Y must not overlap (their spans
  * of (n - 1) * ld + k elements; SPMV_ERR_INVALID_ARG otherwise).  Asynchronous.
  */
@@ -436,6 +447,26 @@ SPMV_API int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr,
 SPMV_API int spmv_get_slots(spmv_handle_t h, int32_t *col, void *val, void *stream);
 
 /*
+ * Measurement aid: the device's rate of gathers from x at random positions, the ceiling
+ * of the matrices whose column indices have no locality.  The GPGPU spMVM paper's
+ * code-balance model (performance-model section) charges x by its reuse factor; with
+ * random columns nothing is reused and every x access of a warp touches a sector of its
+ * own, so the time of the product cannot fall below (random gathers) / (this rate),
+ * however much HBM bandwidth the streamed matrix leaves unused.
+ *   x        device array of n values of `dtype` (n < 2^31), only read.
+ *   gathers  gathers to perform, rounded up to whole rounds of 8 per thread of a full
+ *            wave (2048 threads per SM); the count done is written to *gathers_done
+ *            (host pointer, may be NULL).
+ *   out_sum  device double: the sum of the gathered values is ADDED to it (so no load
+ *            can be dropped); its value has no other meaning.
+ * Column indices come from a per-thread linear congruential sequence mapped onto
+ * [0, n), so no index array is read.  One kernel launch on `stream`; time it with
+ * events around the call.  Returns an spmv_status.
+ */
+SPMV_API int spmv_probe_gather(const void *x, int64_t n, int dtype, int64_t gathers, void *out_sum, void *stream,
+                               int64_t *gathers_done);
+
+/*
  * y = A x computed directly from a CSR matrix in the caller's device memory, with
  * no device allocation at all (no handle, no cudaMalloc / cudaFree, no allocating
  * library call).  None of the pages has a counterpart to this entry point: it is
@@ -453,13 +484,16 @@ SPMV_API int spmv_get_slots(spmv_handle_t h, int32_t *col, void *val, void *stre
  *     before anything runs;
  *   - all calls share that array: calls that overlap on the GPU (different streams,
  *     or different host threads) race on it and give wrong results; serialise them;
- *   - the first call on a device looks up the array's device address (and, with
- *     lazy module loading, makes the driver load the library's device code); make
- *     that first call before any stream capture;
+ *   - the first call on a device (and the first after a cudaDeviceReset) looks up the
+ *     array's device address (and, with lazy module loading, makes the driver load the
+ *     library's device code); make that first call before any stream capture;
  *   - the CSR is NOT validated (validation would need a device-to-host round trip):
  *     pass a matrix that spmv_build_from_csr would accept.
  * Arguments are as in spmv_build_from_csr plus x, y (device arrays of n values of
- * `dtype`) and `stream`.  Asynchronous; returns an spmv_status.
+ * `dtype`) and `stream`.  Every array must be memory of the current device.  y is
+ * written while other parts of the work still read x and the matrix, so a y that
+ * overlaps x, row_ptr, col_idx or vals is refused with SPMV_ERR_INVALID_ARG (no
+ * in-place product).  Asynchronous; returns an spmv_status.
  */
 SPMV_API int spmv_csr_apply_noalloc(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx,
                                     const void *vals, int dtype, const void *x, void *y, void *stream);

@@ -35,6 +35,7 @@ from ._abi import (  # noqa: F401
     spmv_bicgstab,
     spmv_gmres,
     spmv_permute_vector,
+    spmv_probe_gather,
     spmv_get_slots,
     spmv_last_error,
     spmv_last_error_message,
@@ -186,15 +187,16 @@ class SpmvMatrix:
 
     __matmul__ = apply
 
-    def apply_host(self, x_host, y_host=None):
-        """y = A x for numpy host arrays (pinned memory recommended)."""
+    def apply_host(self, x_host, y_host=None, stream=None):
+        """y = A x for numpy host arrays (pinned memory recommended), on the current (or
+        given) stream; returns once y_host holds the result."""
         import numpy as np
 
         self._check_host(x_host, "x_host")
         if y_host is None:
             y_host = np.empty_like(x_host)
         self._check_host(y_host, "y_host", writable=True)
-        spmv_apply_host(self._h, x_host, y_host)
+        spmv_apply_host(self._h, x_host, y_host, stream)
         return y_host
 
     def apply_mapped(self, x_host, y_host=None):

@@ -28,7 +28,7 @@ EXPORTS = (
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
     "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
     "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector", "spmv_apply_mapped", "spmv_bicgstab",
-    "spmv_gmres",
+    "spmv_gmres", "spmv_probe_gather",
 )
 
 #: spmv_ordering codes
@@ -96,6 +96,8 @@ def _load():
     lib.spmv_get_slots.restype = c_int
     lib.spmv_csr_apply_noalloc.argtypes = [i64, i64, vp, vp, vp, c_int, vp, vp, vp]
     lib.spmv_csr_apply_noalloc.restype = c_int
+    lib.spmv_probe_gather.argtypes = [vp, i64, c_int, i64, vp, vp, ctypes.POINTER(i64)]
+    lib.spmv_probe_gather.restype = c_int
     f64 = ctypes.c_double
     lib.spmv_apply_ex.argtypes = [vp, f64, vp, f64, vp, vp]
     lib.spmv_apply_ex.restype = c_int
@@ -287,6 +289,14 @@ def spmv_csr_apply_noalloc(n, nnz, row_ptr, col_idx, vals, dtype, x, y, stream=N
     """y = A x from a device CSR without any device allocation (see spmv.h)."""
     _check(lib.spmv_csr_apply_noalloc(int(n), int(nnz), _ptr(row_ptr), _ptr(col_idx), _ptr(vals), int(dtype),
                                       _ptr(x), _ptr(y), _stream(stream)))
+
+
+def spmv_probe_gather(x, n, dtype, gathers, out_sum, stream=None) -> int:
+    """Random gathers from x (measurement aid, see spmv.h); returns the gathers launched."""
+    done = ctypes.c_int64(0)
+    _check(lib.spmv_probe_gather(_ptr(x), int(n), int(dtype), int(gathers), _ptr(out_sum), _stream(stream),
+                                 ctypes.byref(done)))
+    return int(done.value)
 
 
 def spmv_apply_ex(h, alpha, x, beta, y, stream=None) -> None:

@@ -32,6 +32,22 @@ int set_cuda_error(cudaError_t err, const char *what) {
     return set_error(st, std::string(what) + ": " + cudaGetErrorString(err));
 }
 
+bool device_memory_here(const void *p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (attr.type == cudaMemoryTypeManaged) return true;
+    if (attr.type != cudaMemoryTypeDevice) return false;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return attr.device == dev;
+}
+
 namespace {
 
 void clear_error() {
@@ -83,14 +99,8 @@ struct Temp {
 };
 
 int check_device_pointer(const void *p, const char *name) {
-    cudaPointerAttributes attr;
-    cudaError_t e = cudaPointerGetAttributes(&attr, p);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return set_error(SPMV_ERR_INVALID_ARG, std::string(name) + " is not a CUDA pointer");
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-        return set_error(SPMV_ERR_INVALID_ARG, std::string(name) + " is not device memory");
+    if (!device_memory_here(p))
+        return set_error(SPMV_ERR_INVALID_ARG, std::string(name) + " is not device memory of the current device");
     return SPMV_OK;
 }
 
@@ -114,6 +124,64 @@ int check_fits(double bytes, const char *what) {
                                                  std::to_string(static_cast<long long>(bytes)) +
                                                  " bytes, more than the free device memory allows");
     return SPMV_OK;
+}
+
+// Allocations made after the build can fall inside a stream capture of the calling
+// thread (the first apply on a capturing stream).  cudaMalloc does not enqueue work, but
+// a capture in the default (global) mode forbids it as potentially unsafe; this guard
+// switches the thread to the relaxed mode around such an allocation and back.
+struct RelaxedCapture {
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    RelaxedCapture() { (void)cudaThreadExchangeStreamCaptureMode(&mode); }
+    ~RelaxedCapture() { (void)cudaThreadExchangeStreamCaptureMode(&mode); }
+};
+
+// The apply scratch of stream s: found, or allocated on the first apply of the handle
+// on s.  The row-split counters start at zero: cleared on s itself, so the clearing is
+// ordered before the apply's kernels (and, under stream capture, becomes part of the
+// graph).  The column and staging buffers are allocated later, on first need.
+int acquire_scratch(spmv_handle_t h, cudaStream_t s, ApplyScratch **out) {
+    std::lock_guard<std::mutex> lock(h->scratch_mutex);
+    for (auto &p : h->scratch)
+        if (p->stream == s) {
+            *out = p.get();
+            return SPMV_OK;
+        }
+    auto sc = std::make_unique<ApplyScratch>();
+    sc->stream = s;
+    const Segmented &sg = h->seg;
+    RelaxedCapture relaxed;
+    if ((sg.kind == 1 || sg.kind == 2) && sg.n_cta > 0) {
+        SPMV_TRY(dev_alloc_n(h, &sc->carry_row, sg.n_cta));
+        SPMV_TRY(dev_alloc_n(h, &sc->carry_val, sg.n_cta));
+    }
+    if (sg.kind == 3 && sg.n_rows > 0) {
+        SPMV_TRY(dev_alloc_n(h, &sc->partial, std::max<int64_t>(sg.n_chunks, 1) * 8));  // up to 8 right-hand sides
+        SPMV_TRY(dev_alloc_n(h, &sc->done, sg.n_rows));
+        SPMV_TRY_CUDA(cudaMemsetAsync(sc->done, 0, sizeof(int32_t) * sg.n_rows, s));
+    }
+    *out = sc.get();
+    h->scratch.push_back(std::move(sc));
+    return SPMV_OK;
+}
+
+// An n-value column of the scratch set (tmp_x, tmp_y, x_stage, y_stage), allocated on
+// its first use.
+int scratch_column(spmv_handle_t h, void **slot) {
+    std::lock_guard<std::mutex> lock(h->scratch_mutex);
+    if (*slot) return SPMV_OK;
+    RelaxedCapture relaxed;
+    return dev_alloc(h, slot, static_cast<size_t>(h->n) * value_bytes(h->dtype));
+}
+
+// The segmented part with the scratch pointers of one stream's set filled in.
+Segmented with_scratch(const Segmented &sg, const ApplyScratch &sc) {
+    Segmented v = sg;
+    v.carry_row = sc.carry_row;
+    v.carry_val = sc.carry_val;
+    v.partial = sc.partial;
+    v.done = sc.done;
+    return v;
 }
 
 const char *ordering_name(int o) {
@@ -209,13 +277,11 @@ int partition_rows(BuildCtx &c, int mode, int32_t a, int32_t forced_g, int32_t *
     return SPMV_OK;
 }
 
-// Carry slots of the segmented pass and, for merge-path, the precomputed split of
-// every CTA boundary (so the apply kernel does no search).
+// For merge-path, the precomputed split of every CTA boundary (so the apply kernel
+// does no search).  The carries the pass writes are per-stream apply scratch.
 int alloc_carries(BuildCtx &c, Segmented &sg) {
     spmv_handle_t h = c.h;
     if (sg.n_cta <= 0) return SPMV_OK;
-    SPMV_TRY(dev_alloc_n(h, &sg.carry_row, sg.n_cta));
-    SPMV_TRY(dev_alloc_n(h, &sg.carry_val, sg.n_cta));
     if (sg.kind == 1) {
         SPMV_TRY(dev_alloc_n(h, &sg.part, sg.n_cta + 1));
         SPMV_TRY_CUDA(launch_merge_partition(sg.n_rows, sg.nnz, sg.ptr, sg.n_cta, sg.part, c.s));
@@ -223,8 +289,8 @@ int alloc_carries(BuildCtx &c, Segmented &sg) {
     return SPMV_OK;
 }
 
-// Row chunks of the row-split pass (kind 3) over the compact CSR in sg, plus the
-// partial-sum scratch it writes.
+// Row chunks of the row-split pass (kind 3) over the compact CSR in sg (the partial
+// sums and completion counters it writes are per-stream apply scratch).
 int build_row_chunks(BuildCtx &c, Segmented &sg) {
     spmv_handle_t h = c.h;
     const int64_t m = sg.n_rows;
@@ -242,13 +308,8 @@ int build_row_chunks(BuildCtx &c, Segmented &sg) {
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_begin, total));
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_end, total));
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_row, total));
-    SPMV_TRY(dev_alloc_n(h, &sg.partial, total * 8));  // up to 8 right-hand sides per pass
     SPMV_TRY_CUDA(launch_chunk_fill(m, sg.ptr, cptr, sg.row_chunk_ptr, sg.chunk_begin, sg.chunk_end, sg.chunk_row,
                                     c.s));
-    // completion counters of the rows cut into several chunks (start at zero; the
-    // warp that finishes a row resets its counter)
-    SPMV_TRY(dev_alloc_n(h, &sg.done, m));
-    SPMV_TRY_CUDA(cudaMemsetAsync(sg.done, 0, sizeof(int32_t) * m, c.s));
     std::vector<int64_t> counts_host(static_cast<size_t>(m));
     SPMV_TRY_CUDA(cudaMemcpyAsync(counts_host.data(), count, sizeof(int64_t) * m, cudaMemcpyDeviceToHost, c.s));
     SPMV_TRY(sync(c.s));
@@ -800,10 +861,9 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
     if ((h->seg.kind == 1 || h->seg.kind == 2) && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
     if (h->seg.kind == 3 && !h->sliced.present) h->kernels.push_back("rowsplit_chunks");
-    // one column of x and of y for the scaled and multi-vector applies of formats
-    // without a fused epilogue
-    SPMV_TRY(dev_alloc(h, &h->tmp_x, static_cast<size_t>(n) * value_bytes(h->dtype)));
-    SPMV_TRY(dev_alloc(h, &h->tmp_y, static_cast<size_t>(n) * value_bytes(h->dtype)));
+    // the apply scratch of the build's stream, so applies there allocate nothing
+    ApplyScratch *first = nullptr;
+    SPMV_TRY(acquire_scratch(h, c.s, &first));
     return sync(c.s);
 }
 
@@ -840,15 +900,19 @@ bool fused_epilogue(spmv_handle_t h) {
 }
 
 int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *rec, const Scale *scale = nullptr) {
+    ApplyScratch *sc = nullptr;
+    SPMV_TRY(acquire_scratch(h, s, &sc));
     if (scale && !fused_epilogue(h)) {
-        // y = alpha * t + beta * y with t = A x computed into the handle's scratch column
-        SPMV_TRY(enqueue(h, x, h->tmp_y, s, rec, nullptr));
-        SPMV_TRY_CUDA(launch_axpby_col(h->dtype, h->n, scale->alpha, h->tmp_y, scale->beta, y, 1, s));
+        // y = alpha * t + beta * y with t = A x computed into a scratch column of this stream
+        SPMV_TRY(scratch_column(h, &sc->tmp_y));
+        SPMV_TRY(enqueue(h, x, sc->tmp_y, s, rec, nullptr));
+        SPMV_TRY_CUDA(launch_axpby_col(h->dtype, h->n, scale->alpha, sc->tmp_y, scale->beta, y, 1, s));
         if (rec) SPMV_TRY(rec->mark(s));
         return SPMV_OK;
     }
     if (rec) SPMV_TRY(rec->mark(s));
-    const bool split = h->seg.kind == 3;
+    const Segmented seg = with_scratch(h->seg, *sc);
+    const bool split = seg.kind == 3;
     if (h->format == SPMV_FMT_CSR_VECTOR) {
         for (const Bin &b : h->bins) {
             SPMV_TRY_CUDA(launch_csr_vector(h->dtype, b.g, b.count, h->bin_rows ? h->bin_rows + b.offset : nullptr,
@@ -856,7 +920,7 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
             if (rec) SPMV_TRY(rec->mark(s));
         }
         if (split) {
-            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, seg, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
     } else if (h->sliced.present && (h->sliced.group > 1 || h->sliced.vec)) {
@@ -867,19 +931,19 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
             SPMV_TRY_CUDA(launch_sellg_apply(h->dtype, h->sliced, h->n, x, y, s, scale));
         if (rec) SPMV_TRY(rec->mark(s));
         if (split) {
-            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, h->seg, x, y, s));
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, seg, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
     } else if (h->sliced.present) {
         // sliced rows (and, in the same launch, the chunks of the long rows)
-        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &h->seg : nullptr, x, y, s, scale));
+        SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &seg : nullptr, x, y, s, scale));
         if (rec) SPMV_TRY(rec->mark(s));
     }
-    if (!split && h->seg.kind != 0) {
-        SPMV_TRY_CUDA(launch_segmented(h->dtype, h->seg, x, y, s));
+    if (!split && seg.kind != 0) {
+        SPMV_TRY_CUDA(launch_segmented(h->dtype, seg, x, y, s));
         if (rec) SPMV_TRY(rec->mark(s));
-        if (h->seg.n_cta > 1) {
-            SPMV_TRY_CUDA(launch_carry_fixup(h->dtype, h->seg, y, s));
+        if (seg.n_cta > 1) {
+            SPMV_TRY_CUDA(launch_carry_fixup(h->dtype, seg, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
     }
@@ -976,12 +1040,6 @@ int64_t gcd64(int64_t a, int64_t b) {
     return a;
 }
 
-// [a, a + abytes) and [b, b + bbytes) share a byte
-bool spans_overlap(const void *a, size_t abytes, const void *b, size_t bbytes) {
-    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
-    return pa < pb + bbytes && pb < pa + abytes;
-}
-
 bool vectors_alias(spmv_handle_t h, const void *x, const void *y) {
     const size_t bytes = static_cast<size_t>(h->n) * value_bytes(h->dtype);
     return spans_overlap(x, bytes, y, bytes);
@@ -1041,7 +1099,10 @@ int host_pipe_setup(spmv_handle_t h, cudaStream_t s) {
     if (nb < 2) return SPMV_OK;
 
     void *d_max = nullptr;
-    SPMV_TRY(dev_alloc(h, &d_max, static_cast<size_t>(nb) * sizeof(int32_t)));
+    {
+        std::lock_guard<std::mutex> lock(h->scratch_mutex);  // guards h->allocations
+        SPMV_TRY(dev_alloc(h, &d_max, static_cast<size_t>(nb) * sizeof(int32_t)));
+    }
     SPMV_TRY_CUDA(cudaMemsetAsync(d_max, 0xff, static_cast<size_t>(nb) * sizeof(int32_t), s));
     SPMV_TRY_CUDA(launch_block_max_col(sl, block, static_cast<int32_t *>(d_max), s));
     std::vector<int32_t> reach(static_cast<size_t>(nb));
@@ -1070,7 +1131,7 @@ int host_pipe_setup(spmv_handle_t h, cudaStream_t s) {
 // blocks done, 2 nb start, 2 nb + 1 all of x in, 2 nb + 2 all of y out.  (Blocks that
 // store y straight into the page-locked y_host instead measured slower: those stores
 // overlap the incoming copies less than a second copy engine does.)
-int apply_host_pipelined(spmv_handle_t h, const void *x_host, void *y_host, cudaStream_t s) {
+int apply_host_pipelined(spmv_handle_t h, const ApplyScratch &sc, const void *x_host, void *y_host, cudaStream_t s) {
     const Sliced &sl = h->sliced;
     const int64_t vb = static_cast<int64_t>(value_bytes(h->dtype));
     const int64_t n = h->n, block = h->host_block;
@@ -1078,8 +1139,8 @@ int apply_host_pipelined(spmv_handle_t h, const void *x_host, void *y_host, cuda
     cudaEvent_t *ev = h->host_events.data();
     const char *xh = static_cast<const char *>(x_host);
     char *yh = static_cast<char *>(y_host);
-    char *xs = static_cast<char *>(h->x_stage);
-    char *ys = static_cast<char *>(h->y_stage);
+    char *xs = static_cast<char *>(sc.x_stage);
+    char *ys = static_cast<char *>(sc.y_stage);
     SPMV_TRY_CUDA(cudaEventRecord(ev[2 * nb], s));
     SPMV_TRY_CUDA(cudaStreamWaitEvent(h->host_in, ev[2 * nb], 0));
     SPMV_TRY_CUDA(cudaStreamWaitEvent(h->host_out, ev[2 * nb], 0));
@@ -1253,17 +1314,23 @@ int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *str
     if (!x_host || !y_host) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
     SPMV_TRY(check_current_device(h));
     const size_t bytes = static_cast<size_t>(h->n) * value_bytes(h->dtype);
-    if (!h->x_stage) SPMV_TRY(dev_alloc(h, &h->x_stage, bytes));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (h->host_pipe == 0) SPMV_TRY(host_pipe_setup(h, s));
-    // in place (x_host and y_host overlapping): unpipelined, where all of x is in before y moves
-    if (h->host_pipe == 1 && page_locked(x_host) && page_locked(y_host) && !vectors_alias(h, x_host, y_host)) {
-        if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
-        h->host_last_blocks = static_cast<int>(h->host_need.size());
-        return apply_host_pipelined(h, x_host, y_host, s);
+    ApplyScratch *sc = nullptr;
+    SPMV_TRY(acquire_scratch(h, s, &sc));
+    SPMV_TRY(scratch_column(h, &sc->x_stage));
+    {
+        // the pipeline's copy streams and events belong to the handle: one call at a time
+        std::unique_lock<std::mutex> pipe(h->host_mutex);
+        if (h->host_pipe == 0) SPMV_TRY(host_pipe_setup(h, s));
+        // in place (x_host and y_host overlapping): unpipelined, where all of x is in before y moves
+        if (h->host_pipe == 1 && page_locked(x_host) && page_locked(y_host) && !vectors_alias(h, x_host, y_host)) {
+            SPMV_TRY(scratch_column(h, &sc->y_stage));
+            h->host_last_blocks = static_cast<int>(h->host_need.size());
+            return apply_host_pipelined(h, *sc, x_host, y_host, s);
+        }
     }
     h->host_last_blocks = 0;
-    SPMV_TRY_CUDA(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
+    SPMV_TRY_CUDA(cudaMemcpyAsync(sc->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
     // A plan that writes every row of y exactly once (one sliced launch, no accumulating
     // pass) stores y straight into page-locked host memory: the transfer back then runs
     // inside the product instead of after it.
@@ -1275,11 +1342,11 @@ int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *str
         (void)cudaGetLastError();
     }
     if (y_direct) {
-        SPMV_TRY(enqueue(h, h->x_stage, y_direct, s, nullptr));
+        SPMV_TRY(enqueue(h, sc->x_stage, y_direct, s, nullptr));
     } else {
-        if (!h->y_stage) SPMV_TRY(dev_alloc(h, &h->y_stage, bytes));
-        SPMV_TRY(enqueue(h, h->x_stage, h->y_stage, s, nullptr));
-        SPMV_TRY_CUDA(cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s));
+        SPMV_TRY(scratch_column(h, &sc->y_stage));
+        SPMV_TRY(enqueue(h, sc->x_stage, sc->y_stage, s, nullptr));
+        SPMV_TRY_CUDA(cudaMemcpyAsync(y_host, sc->y_stage, bytes, cudaMemcpyDeviceToHost, s));
     }
     SPMV_TRY_CUDA(cudaStreamSynchronize(s));
     return SPMV_OK;
@@ -1361,7 +1428,10 @@ int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, in
     const size_t vb = value_bytes(h->dtype);
     const Scale scale{alpha, beta};
     const bool fused = fused_epilogue(h) && sell_multi_supported(h->sliced);
-    const Segmented *split = h->seg.kind == 3 ? &h->seg : nullptr;
+    ApplyScratch *sc = nullptr;
+    SPMV_TRY(acquire_scratch(h, s, &sc));
+    const Segmented seg = with_scratch(h->seg, *sc);
+    const Segmented *split = seg.kind == 3 ? &seg : nullptr;
     int64_t c = 0;
     while (c < k) {
         const char *xc = static_cast<const char *>(X) + c * vb;
@@ -1381,9 +1451,11 @@ int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, in
             c += nv;
         } else {
             // one column through the single-vector path
-            SPMV_TRY_CUDA(launch_gather_col(h->dtype, h->n, xc, ldx, h->tmp_x, s));
-            SPMV_TRY(enqueue(h, h->tmp_x, h->tmp_y, s, nullptr));
-            SPMV_TRY_CUDA(launch_axpby_col(h->dtype, h->n, alpha, h->tmp_y, beta, yc, ldy, s));
+            SPMV_TRY(scratch_column(h, &sc->tmp_x));
+            SPMV_TRY(scratch_column(h, &sc->tmp_y));
+            SPMV_TRY_CUDA(launch_gather_col(h->dtype, h->n, xc, ldx, sc->tmp_x, s));
+            SPMV_TRY(enqueue(h, sc->tmp_x, sc->tmp_y, s, nullptr));
+            SPMV_TRY_CUDA(launch_axpby_col(h->dtype, h->n, alpha, sc->tmp_y, beta, yc, ldy, s));
             c += 1;
         }
     }
@@ -1499,7 +1571,7 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     append(o, "\"x_evict_last\":%s,", sl.keep_x ? "true" : "false");
     // host_blocks: the parameter (0 = off); host_pipeline_blocks: blocks of the last
     // spmv_apply_host call (0 = unpipelined, -1 = no call yet)
-    append(o, "\"host_blocks\":%d,\"host_pipeline_blocks\":%d,", h->params.host_blocks, h->host_last_blocks);
+    append(o, "\"host_blocks\":%d,\"host_pipeline_blocks\":%d,", h->params.host_blocks, h->host_last_blocks.load());
     // once pipelined: rows per block, and for each block the last piece of x it waits for
     if (h->host_pipe == 1) {
         append(o, "\"host_pipeline_block_rows\":%lld,\"host_pipeline_reach\":[", (long long)h->host_block);

@@ -26,15 +26,28 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void *g_scratch_address[kMaxDevices] = {};
 
+// The cached address is still this device's array: a cudaDeviceReset ends the context
+// that held it, and the reloaded module may place the array elsewhere.
+bool still_valid(void *p, int dev) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return attr.type == cudaMemoryTypeDevice && attr.device == dev;
+}
+
 // Device address of the scratch array on the current device.  In host code the
 // name g_noalloc_scratch is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// with the device current, on the first call on each device, and cached; every call
+// checks the cached address before use and looks it up again if the device was reset.
 int scratch_address(void **out) {
     int dev = -1;
     SPMV_TRY_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices)
         return set_error(SPMV_ERR_UNSUPPORTED, "device ordinal beyond the scratch table");
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_address[dev] && !still_valid(g_scratch_address[dev], dev)) g_scratch_address[dev] = nullptr;
     if (!g_scratch_address[dev]) {
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
@@ -43,15 +56,6 @@ int scratch_address(void **out) {
     }
     *out = g_scratch_address[dev];
     return SPMV_OK;
-}
-
-int is_device_memory(const void *p) {
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
 }
 
 }  // namespace
@@ -74,9 +78,16 @@ extern "C" SPMV_API int spmv_csr_apply_noalloc(int64_t n, int64_t nnz, const int
     if (n == 0) return SPMV_OK;
     if (!row_ptr || !x || !y || (nnz > 0 && (!col_idx || !vals)))
         return set_error(SPMV_ERR_INVALID_ARG, "NULL array");
-    if (!is_device_memory(row_ptr) || !is_device_memory(x) || !is_device_memory(y) ||
-        (nnz > 0 && (!is_device_memory(col_idx) || !is_device_memory(vals))))
-        return set_error(SPMV_ERR_INVALID_ARG, "every array must be device memory");
+    if (!device_memory_here(row_ptr) || !device_memory_here(x) || !device_memory_here(y) ||
+        (nnz > 0 && (!device_memory_here(col_idx) || !device_memory_here(vals))))
+        return set_error(SPMV_ERR_INVALID_ARG, "every array must be device memory of the current device");
+    // y is written while other CTAs still read x and the matrix
+    const size_t vb = value_bytes(dtype), ybytes = static_cast<size_t>(n) * vb;
+    if (spans_overlap(y, ybytes, x, ybytes)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
+    if (spans_overlap(y, ybytes, row_ptr, static_cast<size_t>(n + 1) * sizeof(int32_t)) ||
+        (nnz > 0 && (spans_overlap(y, ybytes, col_idx, static_cast<size_t>(nnz) * sizeof(int32_t)) ||
+                     spans_overlap(y, ybytes, vals, static_cast<size_t>(nnz) * vb))))
+        return set_error(SPMV_ERR_INVALID_ARG, "y overlaps the matrix arrays");
     void *scratch = nullptr;
     SPMV_TRY(scratch_address(&scratch));
     Segmented sg;

@@ -1,0 +1,90 @@
+// spmv_probe_gather: the random-gather rate of the device, the ceiling of the matrices
+// whose x accesses have no locality (uniformly random columns; the short rows of a
+// power-law matrix).  On such a matrix every x access of a warp touches its own
+// 32-byte sector, and the sliced kernels can go no faster than the device serves
+// scattered sectors, whatever the bandwidth left to the streamed matrix entries.
+//
+// The probe does only that part: each thread draws column indices from a 32-bit linear
+// congruential sequence mapped onto [0, n) by a multiply-high, so there is no index
+// stream, and gathers x there eight at a time (eight independent loads in flight, as
+// the sliced kernels keep), through the same read-only load path.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_util.cuh"
+#include "spmv_internal.cuh"
+
+namespace spmv {
+namespace {
+
+constexpr int kProbeThreads = 256;
+constexpr int kProbeInFlight = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kProbeThreads) k_probe_gather(const T *__restrict__ x, uint32_t n, int64_t rounds,
+                                                              uint32_t seed, double *__restrict__ out) {
+    const uint32_t tid = blockIdx.x * kProbeThreads + threadIdx.x;
+    // distinct starting states per thread (a multiplicative hash of the thread index)
+    uint32_t state = (tid + 1u) * 2654435761u ^ seed;
+    T acc = T(0);
+    for (int64_t r = 0; r < rounds; ++r) {
+        uint32_t idx[kProbeInFlight];
+#pragma unroll
+        for (int u = 0; u < kProbeInFlight; ++u) {
+            state = state * 1664525u + 1013904223u;
+            idx[u] = __umulhi(state, n);  // in [0, n)
+        }
+        T v[kProbeInFlight];
+#pragma unroll
+        for (int u = 0; u < kProbeInFlight; ++u) v[u] = __ldg(x + idx[u]);
+#pragma unroll
+        for (int u = 0; u < kProbeInFlight; ++u) acc += v[u];
+    }
+    // keep the loads: one sum per block into *out
+    double s = static_cast<double>(acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    __shared__ double warp_sum[kProbeThreads / 32];
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kProbeThreads / 32; ++w) t += warp_sum[w];
+        atomicAdd(out, t);
+    }
+}
+
+}  // namespace
+}  // namespace spmv
+
+using namespace spmv;
+
+extern "C" SPMV_API int spmv_probe_gather(const void *x, int64_t n, int dtype, int64_t gathers, void *out_sum,
+                                          void *stream, int64_t *gathers_done) {
+    if (!x || !out_sum || n <= 0 || n >= (int64_t(1) << 31) || gathers < 0)
+        return set_error(SPMV_ERR_INVALID_ARG, "need x, out_sum, 0 < n < 2^31 and gathers >= 0");
+    if (dtype != SPMV_F64 && dtype != SPMV_F32)
+        return set_error(SPMV_ERR_INVALID_ARG, "dtype must be SPMV_F64 or SPMV_F32");
+    if (!device_memory_here(x) || !device_memory_here(out_sum))
+        return set_error(SPMV_ERR_INVALID_ARG, "x and out_sum must be device memory of the current device");
+    int dev = 0, sms = 0;
+    SPMV_TRY_CUDA(cudaGetDevice(&dev));
+    SPMV_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    // a full wave: 2048 resident threads on every SM
+    const int64_t blocks = static_cast<int64_t>(sms) * (2048 / kProbeThreads);
+    const int64_t per_round = blocks * kProbeThreads * kProbeInFlight;
+    const int64_t rounds = (gathers + per_round - 1) / per_round;
+    if (gathers_done) *gathers_done = rounds * per_round;
+    if (rounds == 0) return SPMV_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint32_t nn = static_cast<uint32_t>(n);
+    if (dtype == SPMV_F64)
+        k_probe_gather<double><<<static_cast<unsigned>(blocks), kProbeThreads, 0, s>>>(
+            static_cast<const double *>(x), nn, rounds, 0x9e3779b9u, static_cast<double *>(out_sum));
+    else
+        k_probe_gather<float><<<static_cast<unsigned>(blocks), kProbeThreads, 0, s>>>(
+            static_cast<const float *>(x), nn, rounds, 0x9e3779b9u, static_cast<double *>(out_sum));
+    SPMV_TRY_CUDA(cudaGetLastError());
+    return SPMV_OK;
+}

@@ -62,11 +62,19 @@ __device__ __forceinline__ void load_slots(const int32_t *__restrict__ cp, const
 // row length, so padding is never touched), then the U gathers, then U FMAs.
 // UW > 0 replaces U (the short-row variant below loads a whole row of up to UW entries
 // before the dependency wait).
+// Positions come in whole warps (n_pos is a multiple of the slice height or of the ELL
+// leading dimension, both multiples of 32), so every lane of a warp runs this function.
+// The loop runs in step over the warp's longest row, wmax: a multiply-add past wmax is
+// not issued at all (on this GPU a warp's float64 multiply-add occupies the FP64 pipe
+// for many cycles, so the U-rounding of a 5- or 7-entry row would cost 3/8 or 1/8 of
+// the pipe), and a lane past its own row adds +0 * +0, which leaves its sum unchanged
+// (a sum started at +0 is never -0).
 template <typename T, int CS, bool K, int UW = 0>
 __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
                                          const T *__restrict__ x, T *__restrict__ y, const Epi &ep) {
     constexpr int U = UW > 0 ? UW : SellChunk<T, CS>::U;
     const int w = __ldg(a.len + p);
+    const int wmax = __reduce_max_sync(0xffffffffu, w);
     const uint64_t up = static_cast<uint64_t>(p);
     const int64_t slot = CS > 0 ? __ldg(a.slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
                                 : __ldg(a.slice_ptr + (p >> a.log2C)) + static_cast<int64_t>(p & a.cmask);
@@ -80,14 +88,15 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
     load_slots<T, U, CS>(cp, vp, ld, 0, w, c, v);  // first entries before the dependency wait
     grid_wait();
     T acc = T(0);
-    for (int j = 0; j < w;) {
+    for (int j = 0; j < wmax;) {
         T xv[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
 #pragma unroll
-        for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);  // inactive slots add +0 * +0
+        for (int u = 0; u < U; ++u)
+            if (j + u < wmax) acc = fma(v[u], xv[u], acc);  // slots past w add +0 * +0
         j += U;
-        if (j >= w) break;
+        if (j >= wmax) break;
         cp += U * ld;
         vp += U * ld;
         load_slots<T, U, CS>(cp, vp, ld, j, w, c, v);
@@ -176,9 +185,11 @@ __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
 // Short rows on a small matrix (fewer row positions than one wave of threads, every row
 // at most kShortRow entries): each thread loads its whole row before grid_wait(), so
 // between back-to-back applies the matrix read overlaps the previous apply entirely.
-// With less than a wave there is no occupancy to protect, hence 64 registers.
+// With less than a wave there is no occupancy to protect, hence 64 registers; CTAs of
+// kShortBlock threads spread the few positions over every SM (256-thread CTAs left a
+// 65,536-row matrix on 256 CTAs: two on most SMs, one on the rest).
 template <typename T, int CS, bool K>
-__global__ void __launch_bounds__(kSellBlock, 4)
+__global__ void __launch_bounds__(kShortBlock, 16)
     k_sell_short(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     allow_dependents();
     const int64_t p = gtid();
@@ -232,8 +243,11 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
                                   static_cast<const T *>(sg->val), split_ctas, x, y, ep);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
-    if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax)
+    if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax) {
+        cfg.blockDim = dim3(kShortBlock);
+        cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(sl.n_pos, kShortBlock)));
         return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K>, sell_args(sl, n), val, x, y, ep);
+    }
     return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y, ep);
 }
 

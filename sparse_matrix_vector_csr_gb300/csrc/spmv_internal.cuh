@@ -4,7 +4,10 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
+#include <memory>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -23,6 +26,7 @@ constexpr int kMergeItems = kMergeThreads * kMergeIpt;
 constexpr int kHistCap = 4096;              // row-length histogram: buckets 0..kHistCap-1, last = ">= kHistCap"
 constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows are sorted in one CTA
 constexpr int kShortRow = 8;                 // rows this short on a small matrix: whole-row loads
+constexpr int kShortBlock = 64;              // threads per CTA of that short-row kernel
 constexpr int64_t kShortRowsMax = 152 * 2048;  // "small": fewer row positions than one wave of threads
 constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows
 constexpr int kMaxHostBlocks = 1024;         // row blocks of the spmv_apply_host pipeline, at most
@@ -104,9 +108,26 @@ struct Segmented {
     int32_t *chunk_row = nullptr;      // [n_chunks] compact row of the chunk; ~row if it is the row's only chunk
     int64_t n_multi = 0;               // compact rows cut into more than one chunk
     int32_t *done = nullptr;           // [n_rows] chunks of the row finished in the running apply
-    double *partial = nullptr;         // [n_chunks] partial sums (scratch of the pass)
+    double *partial = nullptr;         // [n_chunks * 8] partial sums, up to 8 right-hand sides
+    // carry_row, carry_val, done and partial are written by the apply: the handle keeps
+    // them per stream (ApplyScratch) and each apply fills in its own stream's set
     int accumulate = 1;            // 1: add into y (y written before), 0: write y
     int32_t dst_offset = 0;        // in-row position of the first held entry (K for the spill)
+};
+
+// The arrays an apply writes besides y, one set per stream a handle is applied on:
+// applies of one handle on different streams may overlap on the GPU, and each works
+// in its own set, while applies on one stream run in stream order and share it.
+struct ApplyScratch {
+    cudaStream_t stream = nullptr;
+    int32_t *carry_row = nullptr;  // [seg.n_cta]   merge-path / COO carries
+    double *carry_val = nullptr;   // [seg.n_cta]
+    double *partial = nullptr;     // [seg.n_chunks * 8] row-split chunk partials
+    int32_t *done = nullptr;       // [seg.n_rows]  row-split counters, zero between applies
+    void *tmp_x = nullptr;         // [n] columns of scaled / multi-vector applies without a
+    void *tmp_y = nullptr;         // [n] fused path (allocated on first need)
+    void *x_stage = nullptr;       // [n] spmv_apply_host staging (allocated on first need)
+    void *y_stage = nullptr;       // [n]
 };
 
 // One CSR-vector launch: g lanes per row over rows bin_rows[offset, offset + count),
@@ -144,22 +165,23 @@ struct spmv_handle_s {
     int64_t long_nnz = 0;
     int32_t K = 0;
 
-    // spmv_apply_host staging
-    void *x_stage = nullptr;
-    void *y_stage = nullptr;
+    // per-stream apply scratch; scratch_mutex guards the list and `allocations`
+    // after the build
+    std::mutex scratch_mutex;
+    std::vector<std::unique_ptr<spmv::ApplyScratch>> scratch;
     // spmv_apply_host pipeline: decided by the first call (0 = not yet, 1 = pipelined,
     // -1 = not pipelined); row positions per block; for every block, the last piece of x
-    // its columns reach (-1 = the block has no entries); copy streams and events
+    // its columns reach (-1 = the block has no entries); copy streams and events.
+    // host_mutex serialises the pipeline's set-up and its calls (they share the copy
+    // streams and events).
+    std::mutex host_mutex;
     int host_pipe = 0;
     int64_t host_block = 0;
     std::vector<int32_t> host_need;
-    int host_last_blocks = -1;  // blocks of the last spmv_apply_host call (0 = unpipelined)
+    std::atomic<int> host_last_blocks{-1};  // blocks of the last spmv_apply_host call (0 = unpipelined)
     cudaStream_t host_in = nullptr;
     cudaStream_t host_out = nullptr;
     std::vector<cudaEvent_t> host_events;
-    // one column of x and of y, for scaled / multi-vector applies without a fused path
-    void *tmp_x = nullptr;
-    void *tmp_y = nullptr;
 
     // permuted basis (spmv_build_permuted): position -> original index; nullptr = identity
     int32_t *basis_perm = nullptr;
@@ -190,6 +212,14 @@ int set_cuda_error(cudaError_t err, const char *what);
     } while (0)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// [a, a + abytes) and [b, b + bbytes) share a byte
+inline bool spans_overlap(const void *a, size_t abytes, const void *b, size_t bbytes) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + bbytes && pb < pa + abytes;
+}
+// p is device memory of the current device (or managed memory, reachable from every
+// device); memory of another GPU, host memory and unknown addresses are not -- api.cu
+bool device_memory_here(const void *p);
 inline size_t value_bytes(int dtype) { return dtype == SPMV_F64 ? 8 : 4; }
 
 // ----------------------------------------------------------------------------

@@ -21,6 +21,31 @@ def test_effective_bytes_formula():
     assert bench.effective_bytes(0, 0, 4) == 4
 
 
+def test_percentile_and_config_selection():
+    assert bench.percentile([5.0, 1.0, 3.0], 0.5) == 3.0
+    assert bench.percentile([1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0, 9.0, 10.0, 11.0], 0.1) == pytest.approx(2.0)
+    configs, head = bench.selected_configs("all")
+    assert head == ("uniform16_16m", "f32") and head in configs and len(configs) == 6
+    assert {c[0] for c in configs} == {"lap2d_256", "lap3d_128", "hmep_6p2m", "powerlaw_4m", "uniform16_16m"}
+    assert bench.selected_configs("lap3d_128") == ([("lap3d_128", "f64"), ("lap3d_128", "f32")], ("lap3d_128", "f64"))
+
+
+def test_random_gather_sector_model():
+    """Short rows: one sector per entry.  A long row of sorted columns 0..199 in float64
+    (4 values per 32-byte sector): six warp instructions of 32 entries touch 8 sectors
+    each, the seventh (8 entries) 2."""
+    import numpy as np
+
+    from workloads import CSR
+
+    cols = np.concatenate([[5, 900, 4000], np.arange(200)]).astype(np.int32)
+    csr = CSR(5000, np.array([0, 3] + [203] * 4999, dtype=np.int32), cols, np.ones(203))
+    m = bench.random_gather_sectors(csr)
+    assert m["short_row_gathers"] == 3 and m["long_row_sectors"] == 6 * 8 + 2 and m["sectors"] == 53
+    m32 = bench.random_gather_sectors(csr.astype(np.float32))  # 8 values per sector
+    assert m32["long_row_sectors"] == 6 * 4 + 1
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))

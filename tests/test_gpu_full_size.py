@@ -55,7 +55,12 @@ def test_full_size_sampled_rows(name, dtype, record_property):
     extra = []
     if name.startswith("powerlaw"):
         lens = np.diff(csr.row_ptr.astype(np.int64))
-        extra = np.nonzero(lens > 128)[0][:2000]  # long rows: row-split chunks
+        # long rows go to the row-split chunks: a spread of 2000 of them over the whole
+        # matrix, and every one of the 32 dense rows (200k - 1M entries, hundreds of chunks)
+        long_rows = np.nonzero(lens > 128)[0]
+        dense = np.argsort(-lens, kind="stable")[:32]
+        assert lens[dense].min() >= 200_000
+        extra = np.concatenate([long_rows[np.linspace(0, long_rows.size - 1, 2000).astype(np.int64)], dense])
     rows = sample_rows(csr, extra=extra)
     ref = oracle.spmv(csr, x, rows=rows)
     with build(csr, "auto") as A:

@@ -248,7 +248,7 @@ def test_hyb_split_matches_rule(name, dtype):
     vb = np.dtype(dtype).itemsize
     ld = layout.ell_leading_dim(csr.n)
     cap = 4096 if dtype == np.float64 else 128
-    K = layout.hyb_width(lens, vb, ld, c=4.0, k_cap=cap)  # spill bytes weighted 4 (reading 6)
+    K = layout.hyb_width(lens, vb, ld, c=4.0, k_cap=cap)  # each spilled entry's bytes weighted 4 against a streamed ELL slot's
     split = layout.hyb_split(lens, K)
     with build(csr, "hyb") as A:
         d = A.describe()
