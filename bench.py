@@ -684,6 +684,7 @@ SWEEP_FORMATS = [
     ("sell", {"row_threads": 4, "row_group_mode": 2}), ("sell", {"row_threads": 8, "row_group_mode": 2}),
     ("ell_r", {"row_threads": 4}), ("sell", {"vector_loads": 1}), ("sell", {"C": 64, "vector_loads": 1}),
     ("sell", {"sigma": 1 << 30, "vector_loads": 1}),
+    ("sell", {"staged": 1}), ("sell", {"sigma": 1 << 30, "staged": 1}),
 ]
 
 

@@ -77,8 +77,9 @@ typedef enum { SPMV_F64 = 0, SPMV_F32 = 1 } spmv_dtype;
  *      kernels of the scite report's abstract).  Suited to irregular matrices.
  *  SPMV_FMT_AUTO        the builder picks one of the above from the row lengths.
  * In SELL, ELLPACK-R and CSR-vector, rows longer than the long-row threshold are
- * taken out and handled by a row-split pass: each is cut into chunks of 2048 entries,
- * one warp per chunk, and the chunk sums of a row combine in a tree (the class of the
+ * taken out and handled by a row-split pass: each is cut into chunks of 4096 entries
+ * (float64) or 2048 (float32), one warp per chunk, and the chunk sums of a row combine
+ * in a tree (the class of the
  * longest rows in the Trilinos issue, processed in pieces).  So no single thread walks
  * a very long row.
  */
@@ -145,6 +146,13 @@ typedef enum {
  *                       latency and each direction slows to about 154 GB/s while the other
  *                       is busy: -10 % per call on the HMEp-shaped matrix with 8 blocks,
  *                       -3 % on the 3D Laplacian in float64 with 4, +9 % in float32.
+ *   staged              SELL-32 with one thread per row: 1 = the slots of each group of 8
+ *                       slices reach shared memory by bulk copies (the copy engine streams
+ *                       the matrix; the load units serve only the gathers of x), and long
+ *                       rows' chunks run in a launch of their own; 0 = every thread loads its
+ *                       own slots.  Automatic = 0.  Takes one thread per row (an automatic
+ *                       row_threads becomes 1); SPMV_ERR_UNSUPPORTED when asked for on another
+ *                       layout.
  */
 typedef struct {
     int32_t C;
@@ -158,6 +166,7 @@ typedef struct {
     int32_t x_policy;
     int32_t vector_loads;
     int32_t host_blocks;
+    int32_t staged;
 } spmv_format_params;
 
 typedef enum {
@@ -206,7 +215,7 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * The apply only reads the handle's matrix data.  What it writes besides y (the carries
  * of the merge-path and COO passes, the chunk partials and counters of the row-split
  * pass) the handle keeps once per stream: the first apply of a handle on a stream
- * allocates that stream's set (a few bytes per long row or per 2048 entries of the
+ * allocates that stream's set (a few bytes per long row or per chunk of the
  * segmented part; the build's own stream gets its set during the build), and later
  * applies on the stream reuse it in stream order.  So applies of one handle on
  * different streams may run concurrently, and so may applies of different handles.
@@ -397,6 +406,16 @@ SPMV_API int spmv_get_permutation(spmv_handle_t h, int32_t *perm, void *stream);
  * are device arrays of n values of the handle's type and must not overlap.  Asynchronous.
  */
 SPMV_API int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int direction, void *stream);
+
+/*
+ * Synchronise `stream` and report whether an apply kernel of this handle gave up a
+ * bounded wait on the device since the last report: SPMV_ERR_TIMEOUT (results of the
+ * applies since then are invalid; the flag is cleared) or SPMV_OK.  Only the
+ * bulk-staged apply (parameter `staged`) waits on the device, for its own bulk copies,
+ * each wait bounded by about a second.  spmv_apply_host, spmv_apply_mapped and
+ * spmv_apply_profiled make this check themselves.
+ */
+SPMV_API int spmv_device_status(spmv_handle_t h, void *stream);
 
 /* Release every device buffer of the handle.  NULL is accepted and ignored. */
 SPMV_API void spmv_destroy(spmv_handle_t h);

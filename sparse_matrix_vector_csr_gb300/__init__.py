@@ -36,6 +36,7 @@ from ._abi import (  # noqa: F401
     spmv_gmres,
     spmv_permute_vector,
     spmv_probe_gather,
+    spmv_device_status,
     spmv_get_slots,
     spmv_last_error,
     spmv_last_error_message,
@@ -60,7 +61,7 @@ class SpmvMatrix:
         """Build from device CSR tensors (int32 row_ptr/col_idx, float64/float32 vals).
 
         ``params``: C, sigma, K, spill_csr, long_row_threshold, subwarp, row_threads,
-        row_group_mode, x_policy, vector_loads, host_blocks (see spmv.h).  ``ordering`` ("natural", "row_length", "rcm", or an
+        row_group_mode, x_policy, vector_loads, host_blocks, staged (see spmv.h).  ``ordering`` ("natural", "row_length", "rcm", or an
         int32 CUDA tensor holding a permutation): build B = P A P^T and work in that
         permuted basis (see ``to_basis`` / ``from_basis``).
         """

@@ -28,7 +28,7 @@ EXPORTS = (
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
     "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
     "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector", "spmv_apply_mapped", "spmv_bicgstab",
-    "spmv_gmres", "spmv_probe_gather",
+    "spmv_gmres", "spmv_probe_gather", "spmv_device_status",
 )
 
 #: spmv_ordering codes
@@ -54,6 +54,7 @@ class FormatParams(ctypes.Structure):
         ("x_policy", ctypes.c_int32),
         ("vector_loads", ctypes.c_int32),
         ("host_blocks", ctypes.c_int32),
+        ("staged", ctypes.c_int32),
     ]
 
 
@@ -98,6 +99,8 @@ def _load():
     lib.spmv_csr_apply_noalloc.restype = c_int
     lib.spmv_probe_gather.argtypes = [vp, i64, c_int, i64, vp, vp, ctypes.POINTER(i64)]
     lib.spmv_probe_gather.restype = c_int
+    lib.spmv_device_status.argtypes = [vp, vp]
+    lib.spmv_device_status.restype = c_int
     f64 = ctypes.c_double
     lib.spmv_apply_ex.argtypes = [vp, f64, vp, f64, vp, vp]
     lib.spmv_apply_ex.restype = c_int
@@ -171,7 +174,7 @@ def dtype_code(dtype) -> int:
 
 
 def make_params(C=-1, sigma=-1, K=-1, spill_csr=-1, long_row_threshold=-1, subwarp=-1, row_threads=-1,
-                row_group_mode=-1, x_policy=-1, vector_loads=-1, host_blocks=-1) -> FormatParams:
+                row_group_mode=-1, x_policy=-1, vector_loads=-1, host_blocks=-1, staged=-1) -> FormatParams:
     p = FormatParams()
     lib.spmv_default_params(ctypes.byref(p))
     p.C, p.sigma, p.K = int(C), int(sigma), int(K)
@@ -179,6 +182,7 @@ def make_params(C=-1, sigma=-1, K=-1, spill_csr=-1, long_row_threshold=-1, subwa
     p.row_threads, p.row_group_mode, p.x_policy = int(row_threads), int(row_group_mode), int(x_policy)
     p.vector_loads = int(vector_loads)
     p.host_blocks = int(host_blocks)
+    p.staged = int(staged)
     return p
 
 
@@ -289,6 +293,11 @@ def spmv_csr_apply_noalloc(n, nnz, row_ptr, col_idx, vals, dtype, x, y, stream=N
     """y = A x from a device CSR without any device allocation (see spmv.h)."""
     _check(lib.spmv_csr_apply_noalloc(int(n), int(nnz), _ptr(row_ptr), _ptr(col_idx), _ptr(vals), int(dtype),
                                       _ptr(x), _ptr(y), _stream(stream)))
+
+
+def spmv_device_status(h, stream=None) -> None:
+    """Synchronise the stream; raise SPMV_ERR_TIMEOUT if an apply kernel gave up a wait."""
+    _check(lib.spmv_device_status(h, _stream(stream)))
 
 
 def spmv_probe_gather(x, n, dtype, gathers, out_sum, stream=None) -> int:

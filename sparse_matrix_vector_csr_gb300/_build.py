@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspmv_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["api.cu", "build.cu", "sell.cu", "sellmm.cu", "vector.cu", "merge.cu", "vecops.cu", "noalloc.cu", "solve.cu", "sellg.cu", "order.cu", "sellv.cu", "probe.cu"]
+SOURCES = ["api.cu", "build.cu", "sell.cu", "sellmm.cu", "vector.cu", "merge.cu", "vecops.cu", "noalloc.cu", "solve.cu", "sellg.cu", "order.cu", "sellv.cu", "probe.cu", "sellb.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -298,7 +298,11 @@ int build_row_chunks(BuildCtx &c, Segmented &sg) {
     SPMV_TRY(c.temp.get(&count, m));
     SPMV_TRY(c.temp.get(&cptr, m + 1));
     SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(m)));
-    SPMV_TRY_CUDA(launch_chunk_counts(m, sg.ptr, count, c.s));
+    // chunk length: no lane sums more than chunk / 32 terms of a row in sequence (64 in
+    // float32, whose rounding bound is the tighter; 128 in float64, where longer chunks
+    // halve the per-chunk overhead on rows of up to a million entries)
+    sg.chunk = h->dtype == SPMV_F64 ? kSplitChunk64 : kSplitChunk;
+    SPMV_TRY_CUDA(launch_chunk_counts(m, sg.ptr, sg.chunk, count, c.s));
     SPMV_TRY_CUDA(launch_exclusive_scan(count, m, cptr, scan_tmp, c.s));
     int64_t total = 0;
     SPMV_TRY_CUDA(cudaMemcpyAsync(&total, cptr + m, sizeof(int64_t), cudaMemcpyDeviceToHost, c.s));
@@ -308,8 +312,8 @@ int build_row_chunks(BuildCtx &c, Segmented &sg) {
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_begin, total));
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_end, total));
     SPMV_TRY(dev_alloc_n(h, &sg.chunk_row, total));
-    SPMV_TRY_CUDA(launch_chunk_fill(m, sg.ptr, cptr, sg.row_chunk_ptr, sg.chunk_begin, sg.chunk_end, sg.chunk_row,
-                                    c.s));
+    SPMV_TRY_CUDA(launch_chunk_fill(m, sg.ptr, sg.chunk, cptr, sg.row_chunk_ptr, sg.chunk_begin, sg.chunk_end,
+                                    sg.chunk_row, c.s));
     std::vector<int64_t> counts_host(static_cast<size_t>(m));
     SPMV_TRY_CUDA(cudaMemcpyAsync(counts_host.data(), count, sizeof(int64_t) * m, cudaMemcpyDeviceToHost, c.s));
     SPMV_TRY(sync(c.s));
@@ -501,6 +505,20 @@ int plan_sliced(BuildCtx &c, const int32_t *lens, int32_t C, int64_t sigma, int6
         sl.slots = slots;
         sl.padded_entries = padded;
         sl.max_width = mw;
+        // the narrow tail of a global sort (widths never increase along the slices)
+        if (sl.perm && sl.sigma >= n && sl.C == 32 && round_to == 1 && c.group == 1 && !c.vec) {
+            bool monotone = true;
+            for (int64_t s = 1; s < sl.n_slices && monotone; ++s) monotone = widths[s] <= widths[s - 1];
+            if (monotone) {
+                sl.has_tail = true;
+                int64_t s = 0, slot = 0;
+                for (int w = kTailMaxW; w >= 0; --w) {  // first slice of width <= w, and its slot
+                    while (s < sl.n_slices && widths[s] > w) slot += static_cast<int64_t>(widths[s++]) * sl.C;
+                    sl.tail_slice[w] = s;
+                    sl.tail_slot[w] = slot;
+                }
+            }
+        }
     }
     return SPMV_OK;
 }
@@ -772,7 +790,7 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
         int32_t g = prm.row_threads;
         if (g > 0 && (g > 32 || (g & (g - 1))))
             return set_error(SPMV_ERR_INVALID_ARG, "row_threads must be 1, 2, 4, 8, 16 or 32");
-        if (g <= 0 && prm.vector_loads == 1) g = 1;  // vector loads: one thread per row
+        if (g <= 0 && (prm.vector_loads == 1 || prm.staged == 1)) g = 1;  // vector loads, staged: one thread per row
         if (g <= 0) {
             int sms = 0;
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -857,6 +875,17 @@ int build_all(BuildCtx &c, int format, const spmv_format_params &prm) {
                                                    stream_bytes > static_cast<double>(l2);
         h->params.x_policy = h->sliced.keep_x ? 1 : 0;
     }
+    if (prm.staged > 1) return set_error(SPMV_ERR_INVALID_ARG, "staged must be 0 or 1");
+    if (prm.staged == 1) {
+        if (format != SPMV_FMT_SELL || !sell_staged_supported(h->sliced))
+            return set_error(SPMV_ERR_UNSUPPORTED, "the bulk-staged apply takes SELL-32 with one thread per row");
+        h->sliced.staged = true;
+        h->kernels.assign(1, "sell_staged");  // long rows: the row-split chunks in a launch of their own
+        if (h->seg.kind == 3) h->kernels.push_back("rowsplit_chunks");
+    }
+    h->params.staged = h->sliced.staged ? 1 : 0;
+    SPMV_TRY(dev_alloc_n(h, &h->dev_err, 1));
+    SPMV_TRY_CUDA(cudaMemsetAsync(h->dev_err, 0, sizeof(int), c.s));
     if (h->seg.kind == 1) h->kernels.push_back("merge_path");
     if (h->seg.kind == 2) h->kernels.push_back("coo_segmented");
     if ((h->seg.kind == 1 || h->seg.kind == 2) && h->seg.n_cta > 1) h->kernels.push_back("carry_fixup");
@@ -895,7 +924,7 @@ struct Recorder {
 
 // Formats whose kernels write y exactly once per row (so alpha/beta fold into that write).
 bool fused_epilogue(spmv_handle_t h) {
-    if (h->sliced.group > 1 || h->sliced.vec) return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
+    if (h->sliced.group > 1 || h->sliced.vec || h->sliced.staged) return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
     return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && (h->seg.kind == 0 || h->seg.kind == 3);
 }
 
@@ -934,6 +963,13 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
             SPMV_TRY_CUDA(launch_rowsplit(h->dtype, seg, x, y, s));
             if (rec) SPMV_TRY(rec->mark(s));
         }
+    } else if (h->sliced.present && h->sliced.staged) {
+        SPMV_TRY_CUDA(launch_sell_staged(h->dtype, h->sliced, h->n, x, y, h->dev_err, s, scale));
+        if (rec) SPMV_TRY(rec->mark(s));
+        if (split) {
+            SPMV_TRY_CUDA(launch_rowsplit(h->dtype, seg, x, y, s));
+            if (rec) SPMV_TRY(rec->mark(s));
+        }
     } else if (h->sliced.present) {
         // sliced rows (and, in the same launch, the chunks of the long rows)
         SPMV_TRY_CUDA(launch_sell_apply(h->dtype, h->sliced, h->n, split ? &seg : nullptr, x, y, s, scale));
@@ -948,6 +984,17 @@ int enqueue(spmv_handle_t h, const void *x, void *y, cudaStream_t s, Recorder *r
         }
     }
     return SPMV_OK;
+}
+
+// After the stream has been synchronised: report (and clear) a bounded device wait of an
+// apply kernel that ran out.  Only the bulk-staged kernel waits on the device.
+int check_device_flag(spmv_handle_t h) {
+    if (!h->sliced.staged || !h->dev_err) return SPMV_OK;
+    int v = 0;
+    SPMV_TRY_CUDA(cudaMemcpy(&v, h->dev_err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (!v) return SPMV_OK;
+    SPMV_TRY_CUDA(cudaMemset(h->dev_err, 0, sizeof(int)));
+    return set_error(SPMV_ERR_TIMEOUT, "an apply kernel gave up waiting for its bulk copies (results invalid)");
 }
 
 int check_current_device(spmv_handle_t h) {
@@ -1069,6 +1116,7 @@ Sliced sliced_view(const Sliced &sl, int dtype, int64_t p0, int64_t p1) {
         v.val = static_cast<char *>(sl.val) + p0 * static_cast<int64_t>(value_bytes(dtype));
     }
     v.pdl = false;
+    v.has_tail = false;  // the tail table counts slices of the whole layout
     return v;
 }
 
@@ -1196,6 +1244,7 @@ int spmv_default_params(spmv_format_params *p) {
     p->x_policy = -1;
     p->vector_loads = -1;
     p->host_blocks = -1;
+    p->staged = -1;
     return SPMV_OK;
 }
 
@@ -1349,7 +1398,7 @@ int spmv_apply_host(spmv_handle_t h, const void *x_host, void *y_host, void *str
         SPMV_TRY_CUDA(cudaMemcpyAsync(y_host, sc->y_stage, bytes, cudaMemcpyDeviceToHost, s));
     }
     SPMV_TRY_CUDA(cudaStreamSynchronize(s));
-    return SPMV_OK;
+    return check_device_flag(h);
 }
 
 // Device address of page-locked host memory (cudaHostAlloc / cudaHostRegister), or an error.
@@ -1376,7 +1425,7 @@ int spmv_apply_mapped(spmv_handle_t h, const void *x_host, void *y_host, void *s
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     SPMV_TRY(enqueue(h, xd, yd, s, nullptr));
     SPMV_TRY_CUDA(cudaStreamSynchronize(s));
-    return SPMV_OK;
+    return check_device_flag(h);
 }
 
 int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, float *kernel_ms, int cap) {
@@ -1389,6 +1438,7 @@ int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, f
     Recorder rec;
     SPMV_TRY(enqueue(h, x, y, s, &rec));
     SPMV_TRY_CUDA(cudaStreamSynchronize(s));
+    SPMV_TRY(check_device_flag(h));
     const int k = static_cast<int>(rec.ev.size()) - 1;
     for (int i = 0; i < k && i < cap; ++i) {
         float ms = 0.f;
@@ -1460,6 +1510,13 @@ int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, in
         }
     }
     return SPMV_OK;
+}
+
+int spmv_device_status(spmv_handle_t h, void *stream) {
+    if (!h) return set_error(SPMV_ERR_INVALID_ARG, "NULL handle");
+    SPMV_TRY(check_current_device(h));
+    SPMV_TRY_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    return check_device_flag(h);
 }
 
 void spmv_destroy(spmv_handle_t h) { free_handle(h); }
@@ -1568,7 +1625,9 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
               "\"ld\":%lld,\"max_width\":%d,\"permuted\":%s,",
            sl.present ? "true" : "false", (long long)sl.n_slices, (long long)sl.slots, (long long)sl.padded_entries,
            (long long)sl.stored_entries, (long long)sl.ld, sl.max_width, sl.perm ? "true" : "false");
-    append(o, "\"x_evict_last\":%s,", sl.keep_x ? "true" : "false");
+    append(o, "\"x_evict_last\":%s,\"staged\":%s,", sl.keep_x ? "true" : "false", sl.staged ? "true" : "false");
+    // positions of the narrow tail of a globally sorted layout, several rows per thread
+    append(o, "\"tail_positions\":%lld,", (long long)sell_tail_positions(sl));
     // host_blocks: the parameter (0 = off); host_pipeline_blocks: blocks of the last
     // spmv_apply_host call (0 = unpipelined, -1 = no call yet)
     append(o, "\"host_blocks\":%d,\"host_pipeline_blocks\":%d,", h->params.host_blocks, h->host_last_blocks.load());

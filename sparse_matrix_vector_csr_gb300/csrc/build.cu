@@ -484,14 +484,14 @@ __global__ void k_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *__
     }
 }
 
-__global__ void k_chunk_counts(int64_t m, const int32_t *__restrict__ ptr, int64_t *__restrict__ count) {
+__global__ void k_chunk_counts(int64_t m, const int32_t *__restrict__ ptr, int32_t chunk, int64_t *__restrict__ count) {
     for (int64_t i = gtid(); i < m; i += gstride()) {
         const int64_t len = static_cast<int64_t>(ptr[i + 1]) - ptr[i];
-        count[i] = len > 0 ? ceil_div_dev(len, kSplitChunk) : 1;
+        count[i] = len > 0 ? ceil_div_dev(len, chunk) : 1;
     }
 }
 
-__global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, const int64_t *__restrict__ cptr,
+__global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, int32_t chunk, const int64_t *__restrict__ cptr,
                              int32_t *__restrict__ row_chunk_ptr, int32_t *__restrict__ chunk_begin,
                              int32_t *__restrict__ chunk_end, int32_t *__restrict__ chunk_row) {
     for (int64_t i = gtid(); i < m; i += gstride()) {
@@ -502,7 +502,7 @@ __global__ void k_chunk_fill(int64_t m, const int32_t *__restrict__ ptr, const i
         if (i == m - 1) row_chunk_ptr[m] = static_cast<int32_t>(cptr[m]);
         int32_t k = a;
         do {
-            const int32_t e = (b - k > kSplitChunk) ? k + kSplitChunk : b;
+            const int32_t e = (b - k > chunk) ? k + chunk : b;
             chunk_begin[c] = k;
             chunk_end[c] = e;
             chunk_row[c] = single ? ~static_cast<int32_t>(i) : static_cast<int32_t>(i);
@@ -729,16 +729,17 @@ cudaError_t launch_merge_partition(int64_t n_rows, int64_t nnz, const int32_t *p
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int64_t *count, cudaStream_t s) {
-    if (m > 0) k_chunk_counts<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, count);
+cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int32_t chunk, int64_t *count, cudaStream_t s) {
+    if (m > 0) k_chunk_counts<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, chunk, count);
     return cudaGetLastError();
 }
 
-cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, const int64_t *cptr, int32_t *row_chunk_ptr,
-                              int32_t *chunk_begin, int32_t *chunk_end, int32_t *chunk_row, cudaStream_t s) {
+cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, int32_t chunk, const int64_t *cptr,
+                              int32_t *row_chunk_ptr, int32_t *chunk_begin, int32_t *chunk_end, int32_t *chunk_row,
+                              cudaStream_t s) {
     if (m > 0)
-        k_chunk_fill<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, cptr, row_chunk_ptr, chunk_begin, chunk_end,
-                                                                  chunk_row);
+        k_chunk_fill<<<grid_for(m, kBlock, 65536), kBlock, 0, s>>>(m, ptr, chunk, cptr, row_chunk_ptr, chunk_begin,
+                                                                  chunk_end, chunk_row);
     return cudaGetLastError();
 }
 

@@ -7,8 +7,8 @@
 // Long rows leave the sliced layout for the row-split pass (the Trilinos issue on
 // unpackAndCombine treats its longest class of rows with three levels of parallelism:
 // rows, pieces of a row, and the entries of a piece): every long row is cut into
-// chunks of at most kSplitChunk entries and one warp reduces one chunk.  A row
-// with a single chunk is written at once; for longer rows the warp that completes
+// chunks of at most 4096 (float64) or 2048 (float32) entries and one warp reduces one
+// chunk.  A row with a single chunk is written at once; for longer rows the warp that completes
 // the last chunk sums the row's partials (in double, in chunk order) -- it learns it
 // is last from a per-row integer counter.  Work per warp is bounded whatever the
 // row lengths; values are never accumulated atomically, and the summation order is
@@ -62,19 +62,11 @@ __device__ __forceinline__ void load_slots(const int32_t *__restrict__ cp, const
 // row length, so padding is never touched), then the U gathers, then U FMAs.
 // UW > 0 replaces U (the short-row variant below loads a whole row of up to UW entries
 // before the dependency wait).
-// Positions come in whole warps (n_pos is a multiple of the slice height or of the ELL
-// leading dimension, both multiples of 32), so every lane of a warp runs this function.
-// The loop runs in step over the warp's longest row, wmax: a multiply-add past wmax is
-// not issued at all (on this GPU a warp's float64 multiply-add occupies the FP64 pipe
-// for many cycles, so the U-rounding of a 5- or 7-entry row would cost 3/8 or 1/8 of
-// the pipe), and a lane past its own row adds +0 * +0, which leaves its sum unchanged
-// (a sum started at +0 is never -0).
 template <typename T, int CS, bool K, int UW = 0>
 __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *__restrict__ val,
                                          const T *__restrict__ x, T *__restrict__ y, const Epi &ep) {
     constexpr int U = UW > 0 ? UW : SellChunk<T, CS>::U;
     const int w = __ldg(a.len + p);
-    const int wmax = __reduce_max_sync(0xffffffffu, w);
     const uint64_t up = static_cast<uint64_t>(p);
     const int64_t slot = CS > 0 ? __ldg(a.slice_ptr + (up / CS)) + static_cast<int64_t>(up % CS)
                                 : __ldg(a.slice_ptr + (p >> a.log2C)) + static_cast<int64_t>(p & a.cmask);
@@ -88,15 +80,14 @@ __device__ __forceinline__ void sell_row(int64_t p, const SellArgs &a, const T *
     load_slots<T, U, CS>(cp, vp, ld, 0, w, c, v);  // first entries before the dependency wait
     grid_wait();
     T acc = T(0);
-    for (int j = 0; j < wmax;) {
+    for (int j = 0; j < w;) {
         T xv[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) xv[u] = (j + u < w) ? gather_x<K>(x + c[u]) : T(0);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (j + u < wmax) acc = fma(v[u], xv[u], acc);  // slots past w add +0 * +0
+        for (int u = 0; u < U; ++u) acc = fma(v[u], xv[u], acc);  // inactive slots add +0 * +0
         j += U;
-        if (j >= wmax) break;
+        if (j >= w) break;
         cp += U * ld;
         vp += U * ld;
         load_slots<T, U, CS>(cp, vp, ld, j, w, c, v);
@@ -185,11 +176,9 @@ __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
 // Short rows on a small matrix (fewer row positions than one wave of threads, every row
 // at most kShortRow entries): each thread loads its whole row before grid_wait(), so
 // between back-to-back applies the matrix read overlaps the previous apply entirely.
-// With less than a wave there is no occupancy to protect, hence 64 registers; CTAs of
-// kShortBlock threads spread the few positions over every SM (256-thread CTAs left a
-// 65,536-row matrix on 256 CTAs: two on most SMs, one on the rest).
+// With less than a wave there is no occupancy to protect, hence 64 registers.
 template <typename T, int CS, bool K>
-__global__ void __launch_bounds__(kShortBlock, 16)
+__global__ void __launch_bounds__(kSellBlock, 4)
     k_sell_short(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     allow_dependents();
     const int64_t p = gtid();
@@ -214,6 +203,107 @@ __global__ void __launch_bounds__(kSellBlock, (CS > 0 && sizeof(T) == 4) ? 8 : 6
     if (p < a.n_pos) sell_row<T, CS, K>(p, a, val, x, y, ep);
 }
 
+// ---------------------------------------------------------------------------
+// narrow tail of a globally sorted layout
+// ---------------------------------------------------------------------------
+// With all rows sorted by length (sigma >= n) the slice widths never increase, and the
+// last slices hold the rows of at most kTailW entries: on the power-law matrix three
+// rows in four.  There a thread's whole row is an entry or two, and sell_row spends it
+// on a chain of three dependent loads (slice offset and length, then the row's slots,
+// then x) with a single gather in flight.  The tail path takes each slot address from
+// the table of width regions (no slice-offset load), and gives every thread kTailR rows
+// (row q of kTailR consecutive slices, one warp per kTailR slices) with all their loads
+// issued before the first gather: two dependent steps, and kTailR times the gathers in
+// flight.  The slots are loaded up to the slice width (padding slots hold column 0 and
+// value 0), and x is gathered only below the row's own length, so padding never
+// touches x.
+constexpr int kTailW = 2;  // slice widths the tail path takes
+constexpr int kTailR = 2;  // rows per thread there
+static_assert(kTailW <= kTailMaxW, "tail table too small");
+
+struct TailArgs {
+    int64_t n_slices;
+    int64_t slice[kTailW + 1];  // first slice of width <= w
+    int64_t slot[kTailW + 1];   // its first slot
+};
+
+template <typename T, bool K>
+__device__ __forceinline__ void sell_tail(int64_t warp, int lane, const SellArgs &a, const TailArgs &t,
+                                          const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y,
+                                          const Epi &ep) {
+    int32_t c[kTailR][kTailW];
+    T v[kTailR][kTailW];
+    int len[kTailR];
+    int32_t row[kTailR];
+#pragma unroll
+    for (int r = 0; r < kTailR; ++r) {
+        const int64_t s = t.slice[kTailW] + warp * kTailR + r;
+        len[r] = -1;
+        row[r] = -1;
+        int w = 0;
+        int64_t slot = 0;
+        if (s < t.n_slices) {
+            // width of slice s: the smallest w whose region (slices t.slice[w] on) holds s
+            int64_t s0 = t.slice[kTailW], b0 = t.slot[kTailW];
+            w = kTailW;
+#pragma unroll
+            for (int q = kTailW - 1; q >= 0; --q)
+                if (s >= t.slice[q]) {
+                    w = q;
+                    s0 = t.slice[q];
+                    b0 = t.slot[q];
+                }
+            slot = b0 + (s - s0) * (32 * w) + lane;
+            const int64_t p = s * 32 + lane;
+            len[r] = __ldg(a.len + p);
+            row[r] = __ldg(a.perm + p);
+        }
+#pragma unroll
+        for (int j = 0; j < kTailW; ++j) {
+            const bool on = j < w;
+            c[r][j] = on ? ld_stream(a.col + slot + 32 * j) : 0;
+            v[r][j] = on ? ld_stream(val + slot + 32 * j) : T(0);
+        }
+    }
+    grid_wait();  // see sell_row
+    T xv[kTailR][kTailW];
+#pragma unroll
+    for (int r = 0; r < kTailR; ++r)
+#pragma unroll
+        for (int j = 0; j < kTailW; ++j) xv[r][j] = j < len[r] ? gather_x<K>(x + c[r][j]) : T(0);
+#pragma unroll
+    for (int r = 0; r < kTailR; ++r) {
+        T acc = T(0);
+#pragma unroll
+        for (int j = 0; j < kTailW; ++j) acc = fma(v[r][j], xv[r][j], acc);  // past the row: +0 * +0
+        if (len[r] >= 0 && row[r] >= 0 && row[r] < a.n) store_y(y, row[r], acc, ep);
+    }
+}
+
+// A globally sorted layout with a narrow tail: the first split_ctas CTAs take the long
+// rows' chunks (one per warp, as in k_sell_split; none without long rows), the next
+// head_ctas the positions before the tail (one per thread), the rest the tail.
+template <typename T, bool K, bool SPLIT>
+__global__ void __launch_bounds__(kSellBlock, SPLIT ? 6 : 8)
+    k_sell_tail(SellArgs a, const T *__restrict__ val, SplitArgs b, const T *__restrict__ split_val,
+                int64_t split_ctas, int64_t head_ctas, TailArgs t, const T *__restrict__ x, T *__restrict__ y,
+                Epi ep) {
+    allow_dependents();
+    if (SPLIT && blockIdx.x < split_ctas) {
+        const int64_t c = (static_cast<int64_t>(blockIdx.x) * kSellBlock + threadIdx.x) >> 5;
+        if (c < b.n_chunks) split_chunk<T, K>(c, threadIdx.x & 31, b, split_val, x, y, ep);
+        return;
+    }
+    const int64_t hb = static_cast<int64_t>(blockIdx.x) - (SPLIT ? split_ctas : 0);
+    if (hb < head_ctas) {
+        const int64_t p = hb * kSellBlock + threadIdx.x;
+        if (p < t.slice[kTailW] * 32) sell_row<T, 32, K>(p, a, val, x, y, ep);
+        return;
+    }
+    const int64_t warp = (hb - head_ctas) * (kSellBlock / 32) + (threadIdx.x >> 5);
+    sell_tail<T, K>(warp, threadIdx.x & 31, a, t, val, x, y, ep);
+}
+
 // Row-split chunks alone (long rows next to the CSR-vector bins).
 template <typename T>
 __global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__restrict__ val, const T *__restrict__ x,
@@ -236,18 +326,35 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (sg && sg->kind == 3 && sg->n_chunks > 0) {
+    const bool split = sg && sg->kind == 3 && sg->n_chunks > 0;
+    if (CS == 32 && sl.has_tail && sl.tail_slice[kTailW] < sl.n_slices) {
+        TailArgs t;
+        t.n_slices = sl.n_slices;
+        for (int w = 0; w <= kTailW; ++w) {
+            t.slice[w] = sl.tail_slice[w];
+            t.slot[w] = sl.tail_slot[w];
+        }
+        const int64_t split_ctas = split ? ceil_div(sg->n_chunks * 32, kSellBlock) : 0;
+        const int64_t head_ctas = ceil_div(t.slice[kTailW] * 32, kSellBlock);
+        const int64_t tail_ctas = ceil_div(sl.n_slices - t.slice[kTailW], (kSellBlock / 32) * kTailR);
+        cfg.gridDim = dim3(static_cast<unsigned>(split_ctas + head_ctas + tail_ctas));
+        const SplitArgs b = split ? split_args(*sg) : SplitArgs{};
+        const T *split_val = split ? static_cast<const T *>(sg->val) : nullptr;
+        if (split)
+            return cudaLaunchKernelEx(&cfg, k_sell_tail<T, K, true>, sell_args(sl, n), val, b, split_val, split_ctas,
+                                      head_ctas, t, x, y, ep);
+        return cudaLaunchKernelEx(&cfg, k_sell_tail<T, K, false>, sell_args(sl, n), val, b, split_val, split_ctas,
+                                  head_ctas, t, x, y, ep);
+    }
+    if (split) {
         const int64_t split_ctas = ceil_div(sg->n_chunks * 32, kSellBlock);
         cfg.gridDim = dim3(static_cast<unsigned>(split_ctas + sell_ctas));
         return cudaLaunchKernelEx(&cfg, k_sell_split<T, CS, K>, sell_args(sl, n), val, split_args(*sg),
                                   static_cast<const T *>(sg->val), split_ctas, x, y, ep);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
-    if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax) {
-        cfg.blockDim = dim3(kShortBlock);
-        cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(sl.n_pos, kShortBlock)));
+    if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax)
         return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K>, sell_args(sl, n), val, x, y, ep);
-    }
     return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y, ep);
 }
 
@@ -284,6 +391,11 @@ cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segm
     if (dtype == SPMV_F64)
         return sell_dispatch<double>(sl, n, split, static_cast<const double *>(x), static_cast<double *>(y), s, ep);
     return sell_dispatch<float>(sl, n, split, static_cast<const float *>(x), static_cast<float *>(y), s, ep);
+}
+
+int64_t sell_tail_positions(const Sliced &sl) {
+    if (!sl.present || !sl.has_tail || sl.C != 32 || sl.tail_slice[kTailW] >= sl.n_slices) return 0;
+    return (sl.n_slices - sl.tail_slice[kTailW]) * 32;
 }
 
 cudaError_t launch_rowsplit(int dtype, const Segmented &sg, const void *x, void *y, cudaStream_t s) {

@@ -26,10 +26,11 @@ constexpr int kMergeItems = kMergeThreads * kMergeIpt;
 constexpr int kHistCap = 4096;              // row-length histogram: buckets 0..kHistCap-1, last = ">= kHistCap"
 constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows are sorted in one CTA
 constexpr int kShortRow = 8;                 // rows this short on a small matrix: whole-row loads
-constexpr int kShortBlock = 64;              // threads per CTA of that short-row kernel
 constexpr int64_t kShortRowsMax = 152 * 2048;  // "small": fewer row positions than one wave of threads
-constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows
+constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows (float32)
+constexpr int kSplitChunk64 = 4096;         // the same for float64 (128 sequential terms a lane)
 constexpr int kMaxHostBlocks = 1024;         // row blocks of the spmv_apply_host pipeline, at most
+constexpr int kTailMaxW = 4;                 // narrow-tail table: slice widths 0..kTailMaxW
 
 // ----------------------------------------------------------------------------
 // format parts
@@ -61,8 +62,16 @@ struct Sliced {
     bool vec = false;              // one thread per row reading 16-byte vectors of its row
     int log2k_col = 0;             // interleaved slots: index groups of 2^log2k_col
     int log2k_val = 0;             //                    value groups of 2^log2k_val
+    bool staged = false;           // apply by sellb.cu's bulk-staged kernel
     bool pdl = true;               // launch with programmatic dependent launch (off for views
                                    // whose start waits on an event of another stream)
+    // Narrow tail of a globally sorted SELL-32 layout (sigma >= n, one thread per row,
+    // column-major slots), where slice widths never increase: for w = 0..kTailMaxW the
+    // slices of width <= w are those from tail_slice[w] on (n_slices if none), and the
+    // first of them starts at slot tail_slot[w].  has_tail is false for other layouts.
+    bool has_tail = false;
+    int64_t tail_slice[kTailMaxW + 1] = {};
+    int64_t tail_slot[kTailMaxW + 1] = {};
     int64_t *slice_ptr = nullptr;  // [n_slices + 1]
     int32_t *width = nullptr;      // [n_slices]
     int32_t *len = nullptr;        // [n_pos] entries stored at each position
@@ -101,7 +110,8 @@ struct Segmented {
     int32_t *carry_row = nullptr;  // [n_cta] row left open at the end of each CTA (-1 = none)
     double *carry_val = nullptr;   // [n_cta] its partial sum
     int32_t *part = nullptr;       // [n_cta + 1] merge-path split of every CTA boundary (kind 1)
-    int64_t n_chunks = 0;          // kind 3: chunks of at most kSplitChunk entries, none crossing a row
+    int64_t n_chunks = 0;          // kind 3: chunks of at most `chunk` entries, none crossing a row
+    int32_t chunk = 0;             // kind 3: kSplitChunk64 (float64) or kSplitChunk (float32)
     int32_t *chunk_begin = nullptr;    // [n_chunks] first entry of each chunk (compact CSR index)
     int32_t *chunk_end = nullptr;      // [n_chunks] one past its last entry
     int32_t *row_chunk_ptr = nullptr;  // [n_rows + 1] chunks of compact row i
@@ -187,6 +197,7 @@ struct spmv_handle_s {
     int32_t *basis_perm = nullptr;
     int ordering = SPMV_ORDER_NATURAL;
 
+    int *dev_err = nullptr;  // device flag: a bounded wait of an apply kernel ran out
     std::vector<std::string> kernels;  // launch sequence of one apply
     std::vector<void *> allocations;
 };
@@ -287,9 +298,9 @@ cudaError_t launch_compact_copy(int dtype, int64_t m, const int32_t *rows, const
                                 const int64_t *cptr, int32_t *col_out, void *val_out,
                                 int32_t *coo_row, cudaStream_t s);
 
-// row chunks of a compact CSR: count[i] = ceil(len_i / kSplitChunk) (at least 1)
-cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int64_t *count, cudaStream_t s);
-cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, const int64_t *cptr, int32_t *row_chunk_ptr,
+// row chunks of a compact CSR: count[i] = ceil(len_i / chunk) (at least 1)
+cudaError_t launch_chunk_counts(int64_t m, const int32_t *ptr, int32_t chunk, int64_t *count, cudaStream_t s);
+cudaError_t launch_chunk_fill(int64_t m, const int32_t *ptr, int32_t chunk, const int64_t *cptr, int32_t *row_chunk_ptr,
                               int32_t *chunk_begin, int32_t *chunk_end, int32_t *chunk_row, cudaStream_t s);
 
 
@@ -311,6 +322,13 @@ struct Scale {
 // scale: nullptr for y = A x
 cudaError_t launch_sell_apply(int dtype, const Sliced &sl, int64_t n, const Segmented *split, const void *x, void *y,
                               cudaStream_t s, const Scale *scale = nullptr);
+// bulk-staged SELL-32 apply (sellb.cu): one thread per row, column-major slots; err is
+// the handle's device flag, set when a bounded wait runs out
+bool sell_staged_supported(const Sliced &sl);
+cudaError_t launch_sell_staged(int dtype, const Sliced &sl, int64_t n, const void *x, void *y, int *err,
+                               cudaStream_t s, const Scale *scale = nullptr);
+// row positions the sliced apply hands to its narrow-tail path (0 = none) -- sell.cu
+int64_t sell_tail_positions(const Sliced &sl);
 cudaError_t launch_csr_vector(int dtype, int g, int64_t count, const int32_t *rows,
                               const int32_t *row_ptr, const int32_t *col, const void *val,
                               const void *x, void *y, cudaStream_t s);

@@ -88,6 +88,10 @@ FORMAT_CASES = [
     ("sell", {"C": 64, "sigma": 1 << 30, "vector_loads": 1, "long_row_threshold": 8}),
     ("ell_r", {"vector_loads": 1}),
     ("hyb", {"vector_loads": 1, "K": 5}),
+    # slots staged in shared memory by bulk copies
+    ("sell", {"staged": 1}),
+    ("sell", {"sigma": 1 << 30, "staged": 1}),
+    ("sell", {"staged": 1, "long_row_threshold": 8}),
 ]
 
 
