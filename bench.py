@@ -688,6 +688,16 @@ SWEEP_FORMATS = [
 ]
 
 
+def mode_dtypes(args):
+    """Value types a single-workload mode runs: --dtypes, else float64 and float32 for the
+    Laplacians and the workload's own type for the others."""
+    import numpy as np
+
+    if args.dtypes:
+        return [np.float64 if t == "f64" else np.float32 for t in args.dtypes.split(",")]
+    return [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+
+
 def run_multi(args):
     """Multi-vector apply Y = A X with k = --nrhs right-hand sides (AUTO format): one JSON line per k."""
     import numpy as np
@@ -698,7 +708,7 @@ def run_multi(args):
 
     torch.cuda.set_device(0)
     peak, peak_kind = load_peaks()
-    dtypes = [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+    dtypes = mode_dtypes(args)
     for dt in dtypes:
         csr, x_np = make_workload(args.workload, dtype=dt)
         sv = csr.vals.dtype.itemsize
@@ -857,7 +867,7 @@ def run_graph(args):
 
     torch.cuda.set_device(0)
     peak, peak_kind = load_peaks()
-    dtypes = [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+    dtypes = mode_dtypes(args)
     per_graph = 100
     for dt in dtypes:
         csr, x_np = make_workload(args.workload, dtype=dt)
@@ -918,7 +928,7 @@ def run_sweep(args):
 
     torch.cuda.set_device(0)
     peak, peak_kind = load_peaks()
-    dtypes = [np.float64, np.float32] if args.workload.startswith("lap") else [None]
+    dtypes = mode_dtypes(args)
     for dt in dtypes:
         csr, x_np = make_workload(args.workload, dtype=dt)
         sv = csr.vals.dtype.itemsize
@@ -968,6 +978,7 @@ def main(argv=None):
                     help="all = every configuration (headline: uniform16_16m); or one workload name")
     ap.add_argument("--format", default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtypes", default="", help="with --sweep / --graph / --nrhs: value types to run, e.g. f64,f32")
     ap.add_argument("--sweep", action="store_true", help="one JSON line per storage format instead of the bench line")
     ap.add_argument("--nrhs", type=int, default=0,
                     help="with --sweep: time the multi-vector apply with this many right-hand sides instead")

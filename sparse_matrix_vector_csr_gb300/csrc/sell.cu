@@ -176,13 +176,18 @@ __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
 // Short rows on a small matrix (fewer row positions than one wave of threads, every row
 // at most kShortRow entries): each thread loads its whole row before grid_wait(), so
 // between back-to-back applies the matrix read overlaps the previous apply entirely.
-// With less than a wave there is no occupancy to protect, hence 64 registers.
-template <typename T, int CS, bool K>
+// With less than a wave there is no occupancy to protect, hence 64 registers.  W is the
+// matrix's longest row: back to back, only the gathers, the multiply-adds and the store
+// remain after the wait, and on this GPU a warp's float64 multiply-add holds the FP64 pipe
+// for about 19 cycles (1.7 lanes a clock per SM), so a 5-entry stencil row compiled for 8
+// multiply-adds spent 3/8 of that critical path on padding (predicated-off multiply-adds
+// still take their turn in the pipe).
+template <typename T, int CS, bool K, int W>
 __global__ void __launch_bounds__(kSellBlock, 4)
     k_sell_short(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     allow_dependents();
     const int64_t p = gtid();
-    if (p < a.n_pos) sell_row<T, CS, K, kShortRow>(p, a, val, x, y, ep);
+    if (p < a.n_pos) sell_row<T, CS, K, W>(p, a, val, x, y, ep);
 }
 
 // Sliced rows and row-split chunks in one launch: the first split_ctas CTAs take
@@ -312,6 +317,24 @@ __global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__re
     if (c < b.n_chunks) split_chunk<T, true>(c, threadIdx.x & 31, b, val, x, y, Epi{1.0, 0.0, 0});
 }
 
+// k_sell_short compiled for the matrix's longest row (1 .. kShortRow entries)
+template <typename T, int CS, bool K>
+cudaError_t short_launch(cudaLaunchConfig_t &cfg, const Sliced &sl, int64_t n, const T *x, T *y, const Epi &ep) {
+    const T *val = static_cast<const T *>(sl.val);
+    static_assert(kShortRow == 8, "one case per row width");
+    switch (sl.max_width) {
+        case 0:
+        case 1: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 1>, sell_args(sl, n), val, x, y, ep);
+        case 2: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 2>, sell_args(sl, n), val, x, y, ep);
+        case 3: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 3>, sell_args(sl, n), val, x, y, ep);
+        case 4: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 4>, sell_args(sl, n), val, x, y, ep);
+        case 5: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 5>, sell_args(sl, n), val, x, y, ep);
+        case 6: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 6>, sell_args(sl, n), val, x, y, ep);
+        case 7: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 7>, sell_args(sl, n), val, x, y, ep);
+        default: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 8>, sell_args(sl, n), val, x, y, ep);
+    }
+}
+
 template <typename T, int CS, bool K>
 cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const T *x, T *y, cudaStream_t s,
                         const Epi &ep) {
@@ -354,7 +377,7 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
     }
     cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
     if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax)
-        return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K>, sell_args(sl, n), val, x, y, ep);
+        return short_launch<T, CS, K>(cfg, sl, n, x, y, ep);
     return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y, ep);
 }
 
