@@ -174,7 +174,7 @@ class ClockSampler:
         self.samples = []
         self.marks = []
         self.proc = None
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
         if gpu_id:
             cmd += ["-i", gpu_id]
         try:
