@@ -221,7 +221,10 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * different streams may run concurrently, and so may applies of different handles.
  * The sets are keyed by the stream handle and live until spmv_destroy; a graph
  * captured on a stream keeps using that stream's set, so replaying it concurrently
- * with other work on the same stream races.  Empty rows give +0.
+ * with other work on the same stream races.  A stream created after another was
+ * destroyed may get the same handle value and so the same set: destroy a stream only
+ * once its applies have finished (cudaStreamDestroy returns before they do).
+ * Empty rows give +0.
  */
 SPMV_API int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream);
 
