@@ -77,9 +77,9 @@ typedef enum { SPMV_F64 = 0, SPMV_F32 = 1 } spmv_dtype;
  *      kernels of the scite report's abstract).  Suited to irregular matrices.
  *  SPMV_FMT_AUTO        the builder picks one of the above from the row lengths.
  * In SELL, ELLPACK-R and CSR-vector, rows longer than the long-row threshold are
- * taken out and handled by a row-split pass: each is cut into chunks of 4096 entries
- * (float64) or 2048 (float32), one warp per chunk, and the chunk sums of a row combine
- * in a tree (the class of the
+ * taken out and handled by a row-split pass: each is cut into chunks of 2048 entries
+ * (4096 in float64 when the chunks run in the same launch as one-thread-per-row
+ * slices), one warp per chunk, and the chunk sums of a row combine in a tree (the class of the
  * longest rows in the Trilinos issue, processed in pieces).  So no single thread walks
  * a very long row.
  */

@@ -299,9 +299,13 @@ int build_row_chunks(BuildCtx &c, Segmented &sg) {
     SPMV_TRY(c.temp.get(&cptr, m + 1));
     SPMV_TRY(c.temp.get(&scan_tmp, scan_temp_elems(m)));
     // chunk length: no lane sums more than chunk / 32 terms of a row in sequence (64 in
-    // float32, whose rounding bound is the tighter; 128 in float64, where longer chunks
-    // halve the per-chunk overhead on rows of up to a million entries)
-    sg.chunk = h->dtype == SPMV_F64 ? kSplitChunk64 : kSplitChunk;
+    // float32, whose rounding bound is the tighter).  In float64, when the chunks share a
+    // launch with the sliced rows (one thread per row, element loads, not staged), chunks
+    // of 4096 halve the chunk warps the fused launch schedules first (power-law 163.0 ->
+    // 158.1 us); a row-split launch of its own keeps 2048, whose extra warps it needs for
+    // parallelism (the CSR-vector plan: 301 against 318 us).
+    const bool fused = h->sliced.present && h->sliced.group == 1 && !h->sliced.vec && h->params.staged != 1;
+    sg.chunk = (h->dtype == SPMV_F64 && fused) ? kSplitChunk64 : kSplitChunk;
     SPMV_TRY_CUDA(launch_chunk_counts(m, sg.ptr, sg.chunk, count, c.s));
     SPMV_TRY_CUDA(launch_exclusive_scan(count, m, cptr, scan_tmp, c.s));
     int64_t total = 0;
@@ -1643,6 +1647,7 @@ int spmv_describe(spmv_handle_t h, char *json, size_t cap) {
     append(o, "\"segment\":\"%s\",\"segment_rows\":%lld,\"segment_nnz\":%lld,\"segment_ctas\":%lld,",
            sg.kind == 0 ? "none" : sg.kind == 1 ? "csr_merge_path" : sg.kind == 2 ? "coo" : "row_split",
            (long long)sg.n_rows, (long long)sg.nnz, (long long)(sg.kind == 3 ? sg.n_chunks : sg.n_cta));
+    append(o, "\"split_chunk\":%d,", sg.kind == 3 ? sg.chunk : 0);
     o += "\"bins\":[";
     for (size_t i = 0; i < h->bins.size(); ++i)
         append(o, "%s[%d,%lld]", i ? "," : "", h->bins[i].g, (long long)h->bins[i].count);

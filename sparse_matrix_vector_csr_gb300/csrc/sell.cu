@@ -7,12 +7,12 @@
 // Long rows leave the sliced layout for the row-split pass (the Trilinos issue on
 // unpackAndCombine treats its longest class of rows with three levels of parallelism:
 // rows, pieces of a row, and the entries of a piece): every long row is cut into
-// chunks of at most 4096 (float64) or 2048 (float32) entries and one warp reduces one
-// chunk.  A row with a single chunk is written at once; for longer rows the warp that completes
-// the last chunk sums the row's partials (in double, in chunk order) -- it learns it
-// is last from a per-row integer counter.  Work per warp is bounded whatever the
-// row lengths; values are never accumulated atomically, and the summation order is
-// fixed.  The sliced rows and the chunks write disjoint rows of y, so both run in
+// chunks of at most 2048 entries (4096 in float64 in the fused launch below) and one
+// warp reduces one chunk.  A row with a single chunk is written at once; for longer
+// rows the warp that completes the last chunk sums the row's partials (in double, in
+// chunk order) -- it learns it is last from a per-row integer counter.  Work per warp
+// is bounded whatever the row lengths; values are never accumulated atomically, and
+// the summation order is fixed.  The sliced rows and the chunks write disjoint rows of y, so both run in
 // one launch.
 #include <cuda_runtime.h>
 

@@ -28,7 +28,7 @@ constexpr int kWindowSortMax = 2048;        // SELL windows up to this many rows
 constexpr int kShortRow = 8;                 // rows this short on a small matrix: whole-row loads
 constexpr int64_t kShortRowsMax = 152 * 2048;  // "small": fewer row positions than one wave of threads
 constexpr int kSplitChunk = 2048;           // entries per warp in the row-split pass for long rows (float32)
-constexpr int kSplitChunk64 = 4096;         // the same for float64 (128 sequential terms a lane)
+constexpr int kSplitChunk64 = 4096;         // float64 chunks fused with one-thread-per-row slices
 constexpr int kMaxHostBlocks = 1024;         // row blocks of the spmv_apply_host pipeline, at most
 constexpr int kTailMaxW = 4;                 // narrow-tail table: slice widths 0..kTailMaxW
 
@@ -111,7 +111,7 @@ struct Segmented {
     double *carry_val = nullptr;   // [n_cta] its partial sum
     int32_t *part = nullptr;       // [n_cta + 1] merge-path split of every CTA boundary (kind 1)
     int64_t n_chunks = 0;          // kind 3: chunks of at most `chunk` entries, none crossing a row
-    int32_t chunk = 0;             // kind 3: kSplitChunk64 (float64) or kSplitChunk (float32)
+    int32_t chunk = 0;             // kind 3: kSplitChunk64 or kSplitChunk entries per chunk
     int32_t *chunk_begin = nullptr;    // [n_chunks] first entry of each chunk (compact CSR index)
     int32_t *chunk_end = nullptr;      // [n_chunks] one past its last entry
     int32_t *row_chunk_ptr = nullptr;  // [n_rows + 1] chunks of compact row i
