@@ -320,7 +320,8 @@ def probe_gather_rate(torch, spmv, x) -> float:
     return max(rates)
 
 
-def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, sampler, peak, peak_kind, keep=False):
+def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, sampler, peak, peak_kind, keep=False,
+                   cpu=False):
     """Build one workload with AUTO, then time REPEATS regions of `steps` back-to-back
     applies (barrier + synchronize on both sides of each), an L2-flushed apply, the
     per-kernel split and, for L2-resident matrices, applies captured in a CUDA graph."""
@@ -465,6 +466,9 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
                         "note": "not HBM-bound: the matrix fits in L2; launch and latency figures"}
     if gather:
         rec["gather_roofline"] = gather
+    if cpu:  # context per configuration: the oracle on a short row sample, the OpenMP product on all of it
+        rec["cpu_oracle"] = cpu_baseline(csr, x_np, budget_s=1.5)
+        rec["cpu_openmp"] = cpu_openmp_baseline(csr, x_np, "dynamic" if name.startswith("powerlaw") else "static")
     if keep:
         rec["_csr"], rec["_x"] = csr, x_np
     return rec
@@ -572,8 +576,10 @@ def run_ours(args):
     records = {}
     try:
         for name, tag in configs:
-            records[(name, tag)] = measure_config(torch, spmv, name, tag, args.steps, args.warmup, world, dev_index,
-                                                  sampler, peak, peak_kind, keep=(name, tag) == headline)
+            records[(name, tag)] = measure_config(
+                torch, spmv, name, tag, args.steps, args.warmup, world, dev_index, sampler, peak, peak_kind,
+                keep=(name, tag) == headline,
+                cpu=rank == 0 and world == 1 and not args.no_cpu_baseline and (name, tag) != headline)
     finally:
         if sampler:
             sampler.stop()
