@@ -411,8 +411,9 @@ SPMV_API int spmv_get_permutation(spmv_handle_t h, int32_t *perm, void *stream);
 SPMV_API int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int direction, void *stream);
 
 /*
- * Synchronise `stream` and report whether an apply kernel of this handle gave up a
- * bounded wait on the device since the last report: SPMV_ERR_TIMEOUT (results of the
+ * None of the pages has a counterpart to this entry point: it reports the library's own
+ * bounded device waits.  Synchronise `stream` and report whether an apply kernel of this
+ * handle gave up a bounded wait on the device since the last report: SPMV_ERR_TIMEOUT (results of the
  * applies since then are invalid; the flag is cleared) or SPMV_OK.  Only the
  * bulk-staged apply (parameter `staged`) waits on the device, for its own bulk copies,
  * each wait bounded by about a second.  spmv_apply_host, spmv_apply_mapped and
