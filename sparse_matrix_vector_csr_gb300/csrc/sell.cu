@@ -181,9 +181,13 @@ __global__ void __launch_bounds__(kSellBlock, CS > 0 ? 8 : 6)
 // remain after the wait, and on this GPU a warp's float64 multiply-add holds the FP64 pipe
 // for about 19 cycles (1.7 lanes a clock per SM), so a 5-entry stencil row compiled for 8
 // multiply-adds spent 3/8 of that critical path on padding (predicated-off multiply-adds
-// still take their turn in the pipe).
-template <typename T, int CS, bool K, int W>
-__global__ void __launch_bounds__(kSellBlock, 4)
+// still take their turn in the pipe).  MINB = 4 (64 registers) below a wave; float64
+// matrices whose longest row is 1-3 or 5-7 entries take the same kernel above a wave at
+// MINB = 6 (40 registers): 7 multiply-adds for the 3D Laplacian's 7-entry rows instead of
+// 8 measured 29.6 against 30.9 us per apply (float32, whose multiply-adds are cheap, stays
+// with k_sell: 18.0 against 17.8; widths 4 and 8 are whole groups of k_sell's four).
+template <typename T, int CS, bool K, int W, int MINB>
+__global__ void __launch_bounds__(kSellBlock, MINB)
     k_sell_short(SellArgs a, const T *__restrict__ val, const T *__restrict__ x, T *__restrict__ y, Epi ep) {
     allow_dependents();
     const int64_t p = gtid();
@@ -318,20 +322,20 @@ __global__ void __launch_bounds__(256) k_split_chunks(SplitArgs b, const T *__re
 }
 
 // k_sell_short compiled for the matrix's longest row (1 .. kShortRow entries)
-template <typename T, int CS, bool K>
+template <typename T, int CS, bool K, int MINB>
 cudaError_t short_launch(cudaLaunchConfig_t &cfg, const Sliced &sl, int64_t n, const T *x, T *y, const Epi &ep) {
     const T *val = static_cast<const T *>(sl.val);
     static_assert(kShortRow == 8, "one case per row width");
     switch (sl.max_width) {
         case 0:
-        case 1: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 1>, sell_args(sl, n), val, x, y, ep);
-        case 2: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 2>, sell_args(sl, n), val, x, y, ep);
-        case 3: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 3>, sell_args(sl, n), val, x, y, ep);
-        case 4: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 4>, sell_args(sl, n), val, x, y, ep);
-        case 5: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 5>, sell_args(sl, n), val, x, y, ep);
-        case 6: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 6>, sell_args(sl, n), val, x, y, ep);
-        case 7: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 7>, sell_args(sl, n), val, x, y, ep);
-        default: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 8>, sell_args(sl, n), val, x, y, ep);
+        case 1: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 1, MINB>, sell_args(sl, n), val, x, y, ep);
+        case 2: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 2, MINB>, sell_args(sl, n), val, x, y, ep);
+        case 3: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 3, MINB>, sell_args(sl, n), val, x, y, ep);
+        case 4: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 4, MINB>, sell_args(sl, n), val, x, y, ep);
+        case 5: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 5, MINB>, sell_args(sl, n), val, x, y, ep);
+        case 6: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 6, MINB>, sell_args(sl, n), val, x, y, ep);
+        case 7: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 7, MINB>, sell_args(sl, n), val, x, y, ep);
+        default: return cudaLaunchKernelEx(&cfg, k_sell_short<T, CS, K, 8, MINB>, sell_args(sl, n), val, x, y, ep);
     }
 }
 
@@ -377,7 +381,10 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
     }
     cfg.gridDim = dim3(static_cast<unsigned>(sell_ctas));
     if (sl.max_width <= kShortRow && sl.n_pos <= kShortRowsMax)
-        return short_launch<T, CS, K>(cfg, sl, n, x, y, ep);
+        return short_launch<T, CS, K, 4>(cfg, sl, n, x, y, ep);
+    if constexpr (sizeof(T) == 8) {  // widths 4 and 8 are whole groups of k_sell's four
+        if (sl.max_width < kShortRow && (sl.max_width & 3)) return short_launch<T, CS, K, 6>(cfg, sl, n, x, y, ep);
+    }
     return cudaLaunchKernelEx(&cfg, k_sell<T, CS, K>, sell_args(sl, n), val, x, y, ep);
 }
 

@@ -117,3 +117,20 @@ def test_device_status_after_staged_applies():
             y = run(A, x)
         spmv.spmv_device_status(A._h)  # raises SPMV_ERR_TIMEOUT if a bounded wait ran out
         assert_parity(y, oracle.spmv(csr, x), np.float64, exact=True, label="staged")
+
+
+@pytest.mark.parametrize("shape", ["1d", "2d"])
+def test_width_exact_kernel_above_a_wave(shape):
+    """Float64 matrices whose longest row is 3 or 5 entries, with more row positions than
+    one wave of threads (152 x 2048), take the width-exact kernel at 6 CTAs per SM."""
+    from workloads import integer_x, laplacian_1d, laplacian_2d
+
+    csr = laplacian_1d(400_003) if shape == "1d" else laplacian_2d(601, 599)
+    assert csr.n > 152 * 2048
+    for integer in (True, False):
+        x = integer_x(csr.n) if integer else uniform_x(csr.n)
+        with build(csr, "auto") as A:
+            d = A.describe()
+            assert d["format"] == "sell" and d["max_width"] in (3, 5) and d["sigma"] == 1
+            y = run(A, x)
+            assert_parity(y, oracle.spmv(csr, x), np.float64, exact=integer, label=f"{shape} integer={integer}")
