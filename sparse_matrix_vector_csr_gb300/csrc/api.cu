@@ -928,7 +928,9 @@ struct Recorder {
 
 // Formats whose kernels write y exactly once per row (so alpha/beta fold into that write).
 bool fused_epilogue(spmv_handle_t h) {
-    if (h->sliced.group > 1 || h->sliced.vec || h->sliced.staged) return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
+    // kernels whose long rows run in a launch of their own (whose chunks store plain sums)
+    if (h->sliced.group > 1 || h->sliced.vec || h->sliced.staged)
+        return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && h->seg.kind == 0;
     return (h->format == SPMV_FMT_SELL || h->format == SPMV_FMT_ELL_R) && (h->seg.kind == 0 || h->seg.kind == 3);
 }
 

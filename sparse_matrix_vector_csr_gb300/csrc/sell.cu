@@ -12,8 +12,8 @@
 // rows the warp that completes the last chunk sums the row's partials (in double, in
 // chunk order) -- it learns it is last from a per-row integer counter.  Work per warp
 // is bounded whatever the row lengths; values are never accumulated atomically, and
-// the summation order is fixed.  The sliced rows and the chunks write disjoint rows of y, so both run in
-// one launch.
+// the summation order is fixed.  The sliced rows and the chunks write disjoint rows of
+// y, so both run in one launch.
 #include <cuda_runtime.h>
 
 #include <cstdint>
