@@ -277,43 +277,52 @@ def percentile(values, q):
     return v[lo] + (v[hi] - v[lo]) * (k - lo)
 
 
-def random_gather_sectors(csr, threshold: int = 128) -> dict:
-    """x sectors (32 bytes) a warp instruction of the AUTO plan touches, summed over one apply.
-    Rows of at most `threshold` entries sit in the sliced layout, where a warp instruction
-    covers one entry of 32 different rows: with random columns every such gather is a
-    sector of its own.  Longer rows go to the row-split pass, whose warp instruction covers
-    32 consecutive entries of one row: their distinct sectors are counted exactly (columns
-    sorted within a row, so a new sector starts where col // (32 / value bytes) changes)."""
+def random_gather_footprint(csr, threshold: int = 128) -> dict:
+    """x lines (128 bytes) and sectors (32 bytes) the warp instructions of the AUTO plan
+    read, summed over one apply.  Rows of at most `threshold` entries sit in the sliced
+    layout, where a warp instruction covers one entry of 32 different rows: with random
+    columns every such gather is a line and a sector of its own.  Longer rows go to the
+    row-split pass, whose warp instruction covers 32 consecutive entries of one row:
+    their distinct lines and sectors are counted exactly (columns sorted within a row, so
+    a new line or sector starts where col // (values per line or sector) changes)."""
     import numpy as np
 
     lens = np.diff(csr.row_ptr.astype(np.int64))
     per_sector = 32 // csr.vals.dtype.itemsize
     short = int(lens[lens <= threshold].sum())
-    long_sectors = 0
+    counts = {"long_row_sectors": 0, "long_row_lines": 0}
     for r in np.nonzero(lens > threshold)[0]:
         a, b = int(csr.row_ptr[r]), int(csr.row_ptr[r + 1])
-        sec = csr.col_idx[a:b].astype(np.int64) // per_sector
-        new = np.ones(sec.size, dtype=bool)
-        new[1:] = sec[1:] != sec[:-1]
-        new[::32] = True  # each warp instruction starts afresh (chunks are multiples of 32)
-        long_sectors += int(new.sum())
-    return {"short_row_gathers": short, "long_row_sectors": long_sectors, "sectors": short + long_sectors,
-            "model": "sliced rows: one sector per entry; row-split chunks: distinct sectors per 32 consecutive "
-                     "entries"}
+        col = csr.col_idx[a:b].astype(np.int64)
+        for key, per in (("long_row_sectors", per_sector), ("long_row_lines", 4 * per_sector)):
+            unit = col // per
+            new = np.ones(unit.size, dtype=bool)
+            new[1:] = unit[1:] != unit[:-1]
+            new[::32] = True  # each warp instruction starts afresh (chunks are multiples of 32)
+            counts[key] += int(new.sum())
+    return {"short_row_gathers": short, **counts, "sectors": short + counts["long_row_sectors"],
+            "lines": short + counts["long_row_lines"],
+            "model": "sliced rows: one line and one sector per entry; row-split chunks: distinct lines and sectors "
+                     "per 32 consecutive entries; bound = max(lines / request rate, sectors / sector rate)"}
 
 
-def probe_gather_rate(torch, spmv, x) -> float:
-    """Random gathers per second from x (spmv_probe_gather), best of 5 launches."""
+def gather_bound_ms(footprint: dict, line_rate: float, sector_rate: float) -> float:
+    """The gather floor of one apply: requests and returned sectors are separate limits."""
+    return max(footprint["lines"] / line_rate, footprint["sectors"] / sector_rate) * 1e3
+
+
+def probe_gather_rate(torch, spmv, x, sectors_per_line: int = 1) -> float:
+    """Lane loads (sectors) per second from x (spmv_probe_gather), best of 5 launches."""
     dev = x.device
     out = torch.zeros(1, dtype=torch.float64, device=dev)
     code = 0 if x.dtype == torch.float64 else 1
     stream = torch.cuda.current_stream()
-    spmv.spmv_probe_gather(x, x.numel(), code, PROBE_GATHERS, out, stream)  # warm-up
+    spmv.spmv_probe_gather(x, x.numel(), code, sectors_per_line, PROBE_GATHERS, out, stream)  # warm-up
     rates = []
     for _ in range(5):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        done = spmv.spmv_probe_gather(x, x.numel(), code, PROBE_GATHERS, out, stream)
+        done = spmv.spmv_probe_gather(x, x.numel(), code, sectors_per_line, PROBE_GATHERS, out, stream)
         e1.record(stream)
         e1.synchronize()
         rates.append(done / (e0.elapsed_time(e1) / 1e3))
@@ -412,14 +421,16 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
         del g
     gather = None
     if name.startswith(("powerlaw", "uniform")):
-        sectors = random_gather_sectors(csr)
-        rate = probe_gather_rate(torch, spmv, x)
-        bound_ms = sectors["sectors"] / rate * 1e3
-        gather = {"probe_gathers_per_s": rate, **sectors, "bound_ms": bound_ms,
+        foot = random_gather_footprint(csr)
+        line_rate = probe_gather_rate(torch, spmv, x, 1)
+        sector_rate = probe_gather_rate(torch, spmv, x, 4)
+        bound_ms = gather_bound_ms(foot, line_rate, sector_rate)
+        gather = {"probe_gathers_per_s": line_rate, "probe_sectors_per_s": sector_rate, **foot, "bound_ms": bound_ms,
                   "frac_of_gather_bound": bound_ms / (region_ms / steps),
                   "hbm_frac_at_gather_bound": effective_bytes(n, nnz, sv) / (bound_ms / 1e3) / 1e9 / peak,
-                  "probe": "spmv_probe_gather on this x: random indices, 8 gathers in flight per thread, a full "
-                           "wave of threads, best of 5 launches of 2^28 gathers"}
+                  "probe": "spmv_probe_gather on this x, 8 gathers in flight per thread, a full wave of threads, "
+                           "best of 5 launches of 2^28 lane loads: random elements (the request rate, one line "
+                           "each) and groups of 4 lanes reading the 4 sectors of a random line (the sector rate)"}
     A.close()
     del rp, ci, vv, x, y
     torch.cuda.empty_cache()

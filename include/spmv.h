@@ -470,24 +470,34 @@ SPMV_API int spmv_get_layout(spmv_handle_t h, int32_t *perm, int64_t *slice_ptr,
 SPMV_API int spmv_get_slots(spmv_handle_t h, int32_t *col, void *val, void *stream);
 
 /*
- * Measurement aid: the device's rate of gathers from x at random positions, the ceiling
+ * Measurement aid: the device's rates of gathers from x at random positions, the ceiling
  * of the matrices whose column indices have no locality.  The GPGPU spMVM paper's
  * code-balance model (performance-model section) charges x by its reuse factor; with
- * random columns nothing is reused and every x access of a warp touches a sector of its
- * own, so the time of the product cannot fall below (random gathers) / (this rate),
+ * random columns nothing is reused and the x accesses are scattered.  An SM sends its
+ * L1 misses to L2 as one request per 128-byte line (carrying the sectors of that line a
+ * warp instruction needs), and two limits apply at once: requests per second and
+ * sectors per second.  So the time of a product cannot fall below
+ *   max(lines / rate(sectors_per_line = 1), sectors / rate(sectors_per_line = 4)),
+ * counting, per warp instruction, the distinct lines and 32-byte sectors of x it reads,
  * however much HBM bandwidth the streamed matrix leaves unused.
- *   x        device array of n values of `dtype` (n < 2^31), only read.
- *   gathers  gathers to perform, rounded up to whole rounds of 8 per thread of a full
- *            wave (2048 threads per SM); the count done is written to *gathers_done
- *            (host pointer, may be NULL).
+ *   x        device array of n values of `dtype` (n < 2^31), only read.  Lines are
+ *            counted from x, which should start on a 128-byte boundary (as memory from
+ *            cudaMalloc does).
+ *   sectors_per_line  1: every lane gathers a random element of its own (one request
+ *            per gather); 2 or 4: groups of that many consecutive lanes read distinct
+ *            32-byte sectors of one random 128-byte line of x (needs n >= 128 bytes of
+ *            values).  Any other value is SPMV_ERR_INVALID_ARG.
+ *   gathers  lane loads to perform (one sector each), rounded up to whole rounds of 8
+ *            per thread of a full wave (2048 threads per SM); the count done is written
+ *            to *gathers_done (host pointer, may be NULL).
  *   out_sum  device double: the sum of the gathered values is ADDED to it (so no load
  *            can be dropped); its value has no other meaning.
- * Column indices come from a per-thread linear congruential sequence mapped onto
- * [0, n), so no index array is read.  One kernel launch on `stream`; time it with
- * events around the call.  Returns an spmv_status.
+ * Positions come from a per-thread (per-group) linear congruential sequence mapped onto
+ * [0, n) or onto the whole lines of x, so no index array is read.  One kernel launch on
+ * `stream`; time it with events around the call.  Returns an spmv_status.
  */
-SPMV_API int spmv_probe_gather(const void *x, int64_t n, int dtype, int64_t gathers, void *out_sum, void *stream,
-                               int64_t *gathers_done);
+SPMV_API int spmv_probe_gather(const void *x, int64_t n, int dtype, int sectors_per_line, int64_t gathers,
+                               void *out_sum, void *stream, int64_t *gathers_done);
 
 /*
  * y = A x computed directly from a CSR matrix in the caller's device memory, with

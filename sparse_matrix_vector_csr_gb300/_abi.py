@@ -97,7 +97,7 @@ def _load():
     lib.spmv_get_slots.restype = c_int
     lib.spmv_csr_apply_noalloc.argtypes = [i64, i64, vp, vp, vp, c_int, vp, vp, vp]
     lib.spmv_csr_apply_noalloc.restype = c_int
-    lib.spmv_probe_gather.argtypes = [vp, i64, c_int, i64, vp, vp, ctypes.POINTER(i64)]
+    lib.spmv_probe_gather.argtypes = [vp, i64, c_int, c_int, i64, vp, vp, ctypes.POINTER(i64)]
     lib.spmv_probe_gather.restype = c_int
     lib.spmv_device_status.argtypes = [vp, vp]
     lib.spmv_device_status.restype = c_int
@@ -300,11 +300,12 @@ def spmv_device_status(h, stream=None) -> None:
     _check(lib.spmv_device_status(h, _stream(stream)))
 
 
-def spmv_probe_gather(x, n, dtype, gathers, out_sum, stream=None) -> int:
-    """Random gathers from x (measurement aid, see spmv.h); returns the gathers launched."""
+def spmv_probe_gather(x, n, dtype, sectors_per_line, gathers, out_sum, stream=None) -> int:
+    """Random gathers from x, `sectors_per_line` lanes to a random 128-byte line
+    (measurement aid, see spmv.h); returns the lane loads launched."""
     done = ctypes.c_int64(0)
-    _check(lib.spmv_probe_gather(_ptr(x), int(n), int(dtype), int(gathers), _ptr(out_sum), _stream(stream),
-                                 ctypes.byref(done)))
+    _check(lib.spmv_probe_gather(_ptr(x), int(n), int(dtype), int(sectors_per_line), int(gathers), _ptr(out_sum),
+                                 _stream(stream), ctypes.byref(done)))
     return int(done.value)
 
 

@@ -30,20 +30,24 @@ def test_percentile_and_config_selection():
     assert bench.selected_configs("lap3d_128") == ([("lap3d_128", "f64"), ("lap3d_128", "f32")], ("lap3d_128", "f64"))
 
 
-def test_random_gather_sector_model():
-    """Short rows: one sector per entry.  A long row of sorted columns 0..199 in float64
-    (4 values per 32-byte sector): six warp instructions of 32 entries touch 8 sectors
-    each, the seventh (8 entries) 2."""
+def test_random_gather_footprint_model():
+    """Short rows: one line and one sector per entry.  A long row of sorted columns 0..199
+    in float64 (4 values per 32-byte sector, 16 per 128-byte line): six warp instructions
+    of 32 entries touch 8 sectors in 2 lines each, the seventh (8 entries) 2 sectors in 1
+    line.  The bound is the larger of the request time and the sector time."""
     import numpy as np
 
     from workloads import CSR
 
     cols = np.concatenate([[5, 900, 4000], np.arange(200)]).astype(np.int32)
     csr = CSR(5000, np.array([0, 3] + [203] * 4999, dtype=np.int32), cols, np.ones(203))
-    m = bench.random_gather_sectors(csr)
+    m = bench.random_gather_footprint(csr)
     assert m["short_row_gathers"] == 3 and m["long_row_sectors"] == 6 * 8 + 2 and m["sectors"] == 53
-    m32 = bench.random_gather_sectors(csr.astype(np.float32))  # 8 values per sector
-    assert m32["long_row_sectors"] == 6 * 4 + 1
+    assert m["long_row_lines"] == 6 * 2 + 1 and m["lines"] == 16
+    m32 = bench.random_gather_footprint(csr.astype(np.float32))  # 8 values per sector, 32 per line
+    assert m32["long_row_sectors"] == 6 * 4 + 1 and m32["long_row_lines"] == 6 + 1
+    assert bench.gather_bound_ms(m, 16e3, 53e3 / 2) == pytest.approx(2.0)  # sectors dominate
+    assert bench.gather_bound_ms(m, 4e3, 1e9) == pytest.approx(4.0)  # requests dominate
 
 
 def _free_port():

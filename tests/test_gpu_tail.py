@@ -89,20 +89,32 @@ def test_tail_of_only_empty_and_unit_rows():
         assert not np.signbit(y[~has]).any() and np.all(y[~has] == 0)
 
 
+@pytest.mark.parametrize("spl", [1, 2, 4])
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
-def test_gather_probe(dtype):
+def test_gather_probe(dtype, spl):
     import sparse_matrix_vector_csr_gb300 as spmv
 
     torch = torch_cuda()
     tdt = torch.float64 if dtype == np.float64 else torch.float32
+    code = 0 if dtype == np.float64 else 1
     x = torch.ones(1 << 20, dtype=tdt, device="cuda")
     out = torch.zeros(1, dtype=torch.float64, device="cuda")
-    done = spmv.spmv_probe_gather(x, x.numel(), 0 if dtype == np.float64 else 1, 1 << 22, out)
+    done = spmv.spmv_probe_gather(x, x.numel(), code, spl, 1 << 22, out)
     torch.cuda.synchronize()
     assert done >= 1 << 22
-    assert out.item() == done  # every gathered value is 1, so the sum counts the gathers
+    assert out.item() == done  # every gathered value is 1, so the sum counts the lane loads
+    if spl > 1:  # x of exactly one line: every lane load stays inside it
+        one = torch.ones(128 // x.element_size(), dtype=tdt, device="cuda")
+        out.zero_()
+        done = spmv.spmv_probe_gather(one, one.numel(), code, spl, 1 << 20, out)
+        torch.cuda.synchronize()
+        assert out.item() == done
+        with pytest.raises(spmv.SpmvError):  # less than one line
+            spmv.spmv_probe_gather(one, one.numel() - 1, code, spl, 10, out)
     with pytest.raises(spmv.SpmvError):
-        spmv.spmv_probe_gather(x, 0, 0, 10, out)
+        spmv.spmv_probe_gather(x, 0, code, spl, 10, out)
+    with pytest.raises(spmv.SpmvError):
+        spmv.spmv_probe_gather(x, x.numel(), code, 3, 10, out)
 
 
 def test_device_status_after_staged_applies():
