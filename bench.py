@@ -278,17 +278,20 @@ def percentile(values, q):
 
 
 def random_gather_footprint(csr, threshold: int = 128) -> dict:
-    """x lines (128 bytes) and sectors (32 bytes) the warp instructions of the AUTO plan
-    read, summed over one apply.  Rows of at most `threshold` entries sit in the sliced
-    layout, where a warp instruction covers one entry of 32 different rows: with random
-    columns every such gather is a line and a sector of its own.  Longer rows go to the
-    row-split pass, whose warp instruction covers 32 consecutive entries of one row:
-    their distinct lines and sectors are counted exactly (columns sorted within a row, so
-    a new line or sector starts where col // (values per line or sector) changes)."""
+    """Requests (128-byte lines) and sectors (32 bytes) an SM must send to L2 in one apply.
+    x gathers: rows of at most `threshold` entries sit in the sliced layout, where a warp
+    instruction covers one entry of 32 different rows, so with random columns every such
+    gather is a line and a sector of its own; longer rows go to the row-split pass, whose
+    warp instruction covers 32 consecutive entries of one row: their distinct lines and
+    sectors are counted exactly (columns sorted within a row, so a new line or sector
+    starts where col // (values per line or sector) changes).  The stream: the matrix,
+    its row pointers and y at their algorithmic size (the B_eff terms other than x), in
+    whole lines and sectors -- the least any layout reads and writes."""
     import numpy as np
 
     lens = np.diff(csr.row_ptr.astype(np.int64))
-    per_sector = 32 // csr.vals.dtype.itemsize
+    sv = csr.vals.dtype.itemsize
+    per_sector = 32 // sv
     short = int(lens[lens <= threshold].sum())
     counts = {"long_row_sectors": 0, "long_row_lines": 0}
     for r in np.nonzero(lens > threshold)[0]:
@@ -300,10 +303,16 @@ def random_gather_footprint(csr, threshold: int = 128) -> dict:
             new[1:] = unit[1:] != unit[:-1]
             new[::32] = True  # each warp instruction starts afresh (chunks are multiples of 32)
             counts[key] += int(new.sum())
-    return {"short_row_gathers": short, **counts, "sectors": short + counts["long_row_sectors"],
-            "lines": short + counts["long_row_lines"],
-            "model": "sliced rows: one line and one sector per entry; row-split chunks: distinct lines and sectors "
-                     "per 32 consecutive entries; bound = max(lines / request rate, sectors / sector rate)"}
+    n, nnz = int(csr.n), int(lens.sum())
+    stream = nnz * (sv + 4) + (n + 1) * 4 + n * sv
+    g_lines, g_sectors = short + counts["long_row_lines"], short + counts["long_row_sectors"]
+    return {"short_row_gathers": short, **counts, "gather_lines": g_lines, "gather_sectors": g_sectors,
+            "stream_bytes": stream, "stream_lines": -(-stream // 128), "stream_sectors": -(-stream // 32),
+            "lines": g_lines - (-stream // 128), "sectors": g_sectors - (-stream // 32),
+            "model": "x gathers: sliced rows one line and one sector per entry, row-split chunks the distinct lines "
+                     "and sectors per 32 consecutive entries; stream: matrix, row pointers and y at their "
+                     "algorithmic bytes in whole lines and sectors; bound = max(lines / request rate, sectors / "
+                     "sector rate)"}
 
 
 def gather_bound_ms(footprint: dict, line_rate: float, sector_rate: float) -> float:

@@ -34,7 +34,8 @@ def test_random_gather_footprint_model():
     """Short rows: one line and one sector per entry.  A long row of sorted columns 0..199
     in float64 (4 values per 32-byte sector, 16 per 128-byte line): six warp instructions
     of 32 entries touch 8 sectors in 2 lines each, the seventh (8 entries) 2 sectors in 1
-    line.  The bound is the larger of the request time and the sector time."""
+    line.  The stream adds the matrix, row pointers and y in whole lines and sectors.  The
+    bound is the larger of the request time and the sector time."""
     import numpy as np
 
     from workloads import CSR
@@ -42,12 +43,15 @@ def test_random_gather_footprint_model():
     cols = np.concatenate([[5, 900, 4000], np.arange(200)]).astype(np.int32)
     csr = CSR(5000, np.array([0, 3] + [203] * 4999, dtype=np.int32), cols, np.ones(203))
     m = bench.random_gather_footprint(csr)
-    assert m["short_row_gathers"] == 3 and m["long_row_sectors"] == 6 * 8 + 2 and m["sectors"] == 53
-    assert m["long_row_lines"] == 6 * 2 + 1 and m["lines"] == 16
+    assert m["short_row_gathers"] == 3 and m["long_row_sectors"] == 6 * 8 + 2 and m["gather_sectors"] == 53
+    assert m["long_row_lines"] == 6 * 2 + 1 and m["gather_lines"] == 16
+    stream = 203 * (8 + 4) + 5001 * 4 + 5000 * 8  # 62,440 bytes: 487.8 lines, 1951.25 sectors
+    assert m["stream_bytes"] == stream and m["stream_lines"] == 488 and m["stream_sectors"] == 1952
+    assert m["lines"] == 16 + 488 and m["sectors"] == 53 + 1952
     m32 = bench.random_gather_footprint(csr.astype(np.float32))  # 8 values per sector, 32 per line
     assert m32["long_row_sectors"] == 6 * 4 + 1 and m32["long_row_lines"] == 6 + 1
-    assert bench.gather_bound_ms(m, 16e3, 53e3 / 2) == pytest.approx(2.0)  # sectors dominate
-    assert bench.gather_bound_ms(m, 4e3, 1e9) == pytest.approx(4.0)  # requests dominate
+    assert bench.gather_bound_ms(m, 504e3, 2005e3 / 2) == pytest.approx(2.0)  # sectors dominate
+    assert bench.gather_bound_ms(m, 504e3 / 4, 1e9) == pytest.approx(4.0)  # requests dominate
 
 
 def _free_port():
