@@ -217,7 +217,9 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * pass) the handle keeps once per stream: the first apply of a handle on a stream
  * allocates that stream's set (a few bytes per long row or per chunk of the
  * segmented part; the build's own stream gets its set during the build), and later
- * applies on the stream reuse it in stream order.  So applies of one handle on
+ * applies on the stream reuse it in stream order.  A first apply inside a stream
+ * capture allocates and initialises the set at once, outside the graph, so the graph
+ * and applies enqueued on that stream outside it both find the set ready.  So applies of one handle on
  * different streams may run concurrently, and so may applies of different handles.
  * The sets are keyed by the stream handle and live until spmv_destroy; a graph
  * captured on a stream keeps using that stream's set, so replaying it concurrently

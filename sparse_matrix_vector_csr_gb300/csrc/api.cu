@@ -136,10 +136,32 @@ struct RelaxedCapture {
     ~RelaxedCapture() { (void)cudaThreadExchangeStreamCaptureMode(&mode); }
 };
 
+// The row-split counters of a new scratch set must read zero before the first pass that
+// uses them.  Cleared on s itself when s is not being captured (ordered before the
+// apply's kernels).  On a stream being captured a memset enqueued there would only be a
+// node of the graph, run when (and if) the graph is launched, while an apply enqueued
+// on s outside the graph would find the counters uncleared; so they are cleared at once
+// on a private stream instead (the caller is in the relaxed capture mode).
+int clear_counters(int32_t *done, int64_t count, cudaStream_t s) {
+    const size_t bytes = sizeof(int32_t) * static_cast<size_t>(count);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    SPMV_TRY_CUDA(cudaStreamIsCapturing(s, &cs));
+    if (cs == cudaStreamCaptureStatusNone) {
+        SPMV_TRY_CUDA(cudaMemsetAsync(done, 0, bytes, s));
+        return SPMV_OK;
+    }
+    cudaStream_t z = nullptr;
+    SPMV_TRY_CUDA(cudaStreamCreateWithFlags(&z, cudaStreamNonBlocking));
+    cudaError_t e = cudaMemsetAsync(done, 0, bytes, z);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(z);
+    (void)cudaStreamDestroy(z);
+    SPMV_TRY_CUDA(e);
+    return SPMV_OK;
+}
+
 // The apply scratch of stream s: found, or allocated on the first apply of the handle
-// on s.  The row-split counters start at zero: cleared on s itself, so the clearing is
-// ordered before the apply's kernels (and, under stream capture, becomes part of the
-// graph).  The column and staging buffers are allocated later, on first need.
+// on s, with its row-split counters at zero.  The column and staging buffers are
+// allocated later, on first need.
 int acquire_scratch(spmv_handle_t h, cudaStream_t s, ApplyScratch **out) {
     std::lock_guard<std::mutex> lock(h->scratch_mutex);
     for (auto &p : h->scratch)
@@ -158,7 +180,7 @@ int acquire_scratch(spmv_handle_t h, cudaStream_t s, ApplyScratch **out) {
     if (sg.kind == 3 && sg.n_rows > 0) {
         SPMV_TRY(dev_alloc_n(h, &sc->partial, std::max<int64_t>(sg.n_chunks, 1) * 8));  // up to 8 right-hand sides
         SPMV_TRY(dev_alloc_n(h, &sc->done, sg.n_rows));
-        SPMV_TRY_CUDA(cudaMemsetAsync(sc->done, 0, sizeof(int32_t) * sg.n_rows, s));
+        SPMV_TRY(clear_counters(sc->done, sg.n_rows, s));
     }
     *out = sc.get();
     h->scratch.push_back(std::move(sc));

@@ -1,19 +1,18 @@
 // Bulk-staged SELL-32 apply: the matrix slots reach shared memory through the bulk
 // copy engine (cp.async.bulk, completion counted on an mbarrier), and the threads
-// gather x with plain loads at the column indices they read there.
+// gather x with plain loads at the column indices they read there.  This is the staging
+// the SELL layout invites: a slice of C rows is one contiguous block of C * width slots
+// (GPGPU spMVM paper, pJDS section, Fig. 1), and eight consecutive slices are one
+// contiguous block too.  The copies carry an L2 evict-first hint, so the once-read
+// stream does not push x out of L2, and a thread that reads its indices from shared
+// memory keeps eight gathers in flight without waiting on a global load.
 //
-// Why: on matrices whose x accesses have no locality every gather of a warp is 32
-// separate sectors, and the L1/texture unit's tag stage sets the pace.  In the
-// register kernel (sell.cu) the streamed column indices and values go through that
-// same unit -- one more line per warp load, 32 extra lines per 512 gathers on the
-// random uniform matrix, which measured 93 % of the pure random-gather rate.  Bulk
-// copies bypass it: the stream goes from L2 to shared memory on its own engine, the
-// unit serves only the gathers, and since a thread reads its indices from shared
-// memory it can keep eight gathers in flight without waiting on a global load.  The
-// copies carry an L2 evict-first hint, so the once-read stream does not push x out of
-// L2.  This is the staging the SELL layout invites: a slice of C rows is one
-// contiguous block of C * width slots (GPGPU spMVM paper, pJDS section, Fig. 1), and
-// eight consecutive slices are one contiguous block too.
+// Measured on GB300, it is slower than the register kernel (sell.cu) and is only built
+// on request (format parameter `staged`): the matrices it was meant for, those whose x
+// gathers have no locality, are bound by the requests an SM sends to L2 (one per
+// 128-byte line a warp instruction touches, about one per clock), and the bulk copies'
+// requests go through that same path, so moving the stream off the load pipe frees
+// none of it; each CTA also waits for its first copy with nothing else to do.
 //
 // Work: one CTA of 256 threads per group of 8 consecutive slices (256 row positions,
 // one per thread).  A group whose slices are at most kChunkCols wide is copied whole
@@ -154,6 +153,7 @@ __global__ void __launch_bounds__(kSellBlock) k_sell_staged(SellArgs a, const T 
     __shared__ uint64_t bar[2];
     __shared__ int64_t base[kGroupSlices];
     __shared__ int32_t width[kGroupSlices];
+    __shared__ int armed[2];  // phases armed on each stage's mbarrier (thread 0 only)
     allow_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kGroupSlices;
@@ -184,7 +184,12 @@ __global__ void __launch_bounds__(kSellBlock) k_sell_staged(SellArgs a, const T 
     const uint64_t pol = evict_first_policy();
     if (threadIdx.x == 0) {
         issue_chunk<T>(smem, bar, st, 0, 0, whole, base, width, nsl, a.col, val, pol);
-        if (nk > 1) issue_chunk<T>(smem, bar, st, 1, 1, whole, base, width, nsl, a.col, val, pol);
+        armed[0] = 1;
+        armed[1] = 0;
+        if (nk > 1) {
+            issue_chunk<T>(smem, bar, st, 1, 1, whole, base, width, nsl, a.col, val, pol);
+            armed[1] = 1;
+        }
     }
     grid_wait();  // x and y only after the previous kernel of the stream
     const int my_w = have ? width[warp] : 0;
@@ -218,13 +223,19 @@ __global__ void __launch_bounds__(kSellBlock) k_sell_staged(SellArgs a, const T 
             if (threadIdx.x == 0 && ok) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue_chunk<T>(smem, bar, st, b, k + 2, whole, base, width, nsl, a.col, val, pol);
+                ++armed[b];
             }
         }
     }
     if (!ok) {
         if (lane == 0) atomicOr(st.err, 1);
-        // let the copies already issued land before the CTA's shared memory goes away
-        for (int k = 0; k < nk && k < 2; ++k) (void)mbar_wait_bounded(bar + k, 0u);
+        // Let the copies already issued land before the CTA's shared memory goes away
+        // (the CTA lives until its last thread returns).  Thread 0 arms a stage again
+        // only after its own wait for the stage's previous phase succeeded, so at most
+        // the last armed phase of each stage is in flight: wait for that one.
+        if (threadIdx.x == 0)
+            for (int b = 0; b < 2; ++b)
+                if (armed[b] > 0) (void)mbar_wait_bounded(bar + b, static_cast<uint32_t>((armed[b] - 1) & 1));
         return;
     }
     if (w >= 0 && r >= 0 && r < a.n) store_y(y, r, acc, ep);

@@ -130,3 +130,41 @@ def test_two_host_threads_apply_host(plan):
     assert not errors, errors
     for i in range(2):
         assert_parity(results[i], oracle.spmv(csr, xs[i]), np.float64, exact=True, label=f"{label} thread {i}")
+
+
+@pytest.mark.parametrize("plan", PLANS, ids=[p[2] for p in PLANS])
+def test_first_apply_inside_a_capture(plan):
+    """The first apply of a handle on a stream is captured into a graph, so the stream's
+    scratch set is allocated then.  An apply enqueued on that stream outside the graph
+    before the graph has ever run, then replays of the graph, then another apply outside
+    it, all match the oracle bit for bit."""
+    torch = torch_cuda()
+    fmt, params, label = plan
+    csr = _matrix(True)
+    xa_np, xb_np = _vectors(csr.n, True)
+    want_a, want_b = oracle.spmv(csr, xa_np), oracle.spmv(csr, xb_np)
+    with build(csr, fmt, **params) as A:
+        _uses_scratch(A.describe(), label)
+        xa, xb = torch.from_numpy(xa_np).cuda(), torch.from_numpy(xb_np).cuda()
+        ya, yb = torch.full_like(xa, float("nan")), torch.full_like(xb, float("nan"))
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            A.apply(xa, ya, stream=s)
+        with torch.cuda.stream(s):
+            A.apply(xb, yb, stream=s)  # the graph has not run yet
+        s.synchronize()
+        assert_parity(yb.cpu().numpy(), want_b, np.float64, exact=True, label=f"{label} outside the graph")
+        for _ in range(3):
+            ya.fill_(float("nan"))
+            with torch.cuda.stream(s):
+                g.replay()
+            s.synchronize()
+            assert_parity(ya.cpu().numpy(), want_a, np.float64, exact=True, label=f"{label} graph replay")
+        yb.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            A.apply(xb, yb, stream=s)
+        s.synchronize()
+        assert_parity(yb.cpu().numpy(), want_b, np.float64, exact=True, label=f"{label} after the replays")
+        del g
