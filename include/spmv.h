@@ -27,6 +27,9 @@
  *    and spmv_last_error_message() describe the failure for the calling thread.
  *    No entry point traps or aborts on bad input; every entry point except
  *    spmv_csr_apply_noalloc validates its matrix.
+ *  - Environment: SPMV_LOG set to anything but "" or "0" makes every successful build
+ *    write its plan (the spmv_describe JSON) to stderr as one line "spmv: built {...}";
+ *    SPMV_FAIL_ALLOC injects a device allocation failure (see spmv_device_memory).
  */
 #ifndef SPMV_GB300_H
 #define SPMV_GB300_H
@@ -182,6 +185,23 @@ typedef enum {
 
 /* Fill *p with "all automatic" values.  Returns SPMV_OK or SPMV_ERR_INVALID_ARG. */
 SPMV_API int spmv_default_params(spmv_format_params *p);
+
+/*
+ * The device memory this library holds right now, over all handles and all calls in
+ * progress: the number of its live device allocations and their total size in bytes
+ * (build temporaries, handle arrays, per-stream scratch, solver workspaces; not the
+ * fixed scratch array of spmv_csr_apply_noalloc, which is part of the library's device
+ * image).  No page has a counterpart: it lets a caller account for the library's share
+ * of device memory, and tests check with it that failed calls release what they took.
+ * Either pointer (host memory) may be NULL.  Always returns SPMV_OK.
+ *
+ * Fault injection (host side, for tests): when the environment variable SPMV_FAIL_ALLOC
+ * holds a positive integer k, the k-th device allocation the library attempts after the
+ * variable took that value fails as if the device were out of memory -- once; the count
+ * restarts whenever the value changes, unset included.  The call that made it returns
+ * SPMV_ERR_OOM after releasing what it had allocated.
+ */
+SPMV_API int spmv_device_memory(int64_t *allocations, int64_t *bytes);
 
 /*
  * Build a handle from a device CSR matrix.

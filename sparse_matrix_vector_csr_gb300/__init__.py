@@ -36,6 +36,7 @@ from ._abi import (  # noqa: F401
     spmv_gmres,
     spmv_permute_vector,
     spmv_probe_gather,
+    spmv_device_memory,
     spmv_device_status,
     spmv_get_slots,
     spmv_last_error,

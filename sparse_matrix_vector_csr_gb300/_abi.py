@@ -28,7 +28,7 @@ EXPORTS = (
     "spmv_last_error_message", "spmv_error_string", "spmv_to_csr", "spmv_describe", "spmv_get_layout",
     "spmv_csr_apply_noalloc", "spmv_apply_ex", "spmv_apply_multi", "spmv_cg", "spmv_get_slots",
     "spmv_build_permuted", "spmv_get_permutation", "spmv_permute_vector", "spmv_apply_mapped", "spmv_bicgstab",
-    "spmv_gmres", "spmv_probe_gather", "spmv_device_status",
+    "spmv_gmres", "spmv_probe_gather", "spmv_device_status", "spmv_device_memory",
 )
 
 #: spmv_ordering codes
@@ -99,6 +99,8 @@ def _load():
     lib.spmv_csr_apply_noalloc.restype = c_int
     lib.spmv_probe_gather.argtypes = [vp, i64, c_int, c_int, i64, vp, vp, ctypes.POINTER(i64)]
     lib.spmv_probe_gather.restype = c_int
+    lib.spmv_device_memory.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.spmv_device_memory.restype = c_int
     lib.spmv_device_status.argtypes = [vp, vp]
     lib.spmv_device_status.restype = c_int
     f64 = ctypes.c_double
@@ -298,6 +300,13 @@ def spmv_csr_apply_noalloc(n, nnz, row_ptr, col_idx, vals, dtype, x, y, stream=N
 def spmv_device_status(h, stream=None) -> None:
     """Synchronise the stream; raise SPMV_ERR_TIMEOUT if an apply kernel gave up a wait."""
     _check(lib.spmv_device_status(h, _stream(stream)))
+
+
+def spmv_device_memory() -> tuple:
+    """(live device allocations, their bytes) held by the library right now."""
+    count, size = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib.spmv_device_memory(ctypes.byref(count), ctypes.byref(size)))
+    return int(count.value), int(size.value)
 
 
 def spmv_probe_gather(x, n, dtype, sectors_per_line, gathers, out_sum, stream=None) -> int:

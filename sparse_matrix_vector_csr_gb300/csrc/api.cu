@@ -7,8 +7,10 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "spmv_internal.cuh"
@@ -30,6 +32,88 @@ int set_cuda_error(cudaError_t err, const char *what) {
     const int st = (err == cudaErrorMemoryAllocation) ? SPMV_ERR_OOM : SPMV_ERR_CUDA;
     (void)cudaGetLastError();  // clear a non-sticky error so later calls start clean
     return set_error(st, std::string(what) + ": " + cudaGetErrorString(err));
+}
+
+// ---------------------------------------------------------------------------
+// device memory of the library
+// ---------------------------------------------------------------------------
+namespace {
+std::mutex g_mem_mutex;
+std::unordered_map<void *, size_t> g_mem_live;  // every device allocation held, with its size
+int64_t g_mem_bytes = 0;
+std::string g_fail_value;  // SPMV_FAIL_ALLOC as last seen
+long g_fail_seen = 0;      // allocations since it took that value
+
+// SPMV_FAIL_ALLOC=k: the k-th device allocation after the variable took its current
+// value fails as if the device were out of memory (once; the count restarts whenever
+// the value changes, unset included).  Called with g_mem_mutex held.
+bool injected_failure() {
+    const char *v = std::getenv("SPMV_FAIL_ALLOC");
+    const std::string cur = v ? v : "";
+    if (cur != g_fail_value) {
+        g_fail_value = cur;
+        g_fail_seen = 0;
+    }
+    if (cur.empty()) return false;
+    char *end = nullptr;
+    const long k = std::strtol(cur.c_str(), &end, 10);
+    if (end == cur.c_str() || k <= 0) return false;
+    return ++g_fail_seen == k;
+}
+
+void track(void *p, size_t bytes) {
+    g_mem_live[p] = bytes;
+    g_mem_bytes += static_cast<int64_t>(bytes);
+}
+
+void untrack(void *p) {
+    auto it = g_mem_live.find(p);
+    if (it == g_mem_live.end()) return;
+    g_mem_bytes -= static_cast<int64_t>(it->second);
+    g_mem_live.erase(it);
+}
+}  // namespace
+
+cudaError_t lib_malloc(void **p, size_t bytes) {
+    std::lock_guard<std::mutex> lock(g_mem_mutex);
+    *p = nullptr;
+    if (injected_failure()) return cudaErrorMemoryAllocation;
+    const cudaError_t e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess) track(*p, bytes);
+    return e;
+}
+
+cudaError_t lib_malloc_async(void **p, size_t bytes, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_mem_mutex);
+    *p = nullptr;
+    if (injected_failure()) return cudaErrorMemoryAllocation;
+    const cudaError_t e = cudaMallocAsync(p, bytes, s);
+    if (e == cudaSuccess) track(*p, bytes);
+    return e;
+}
+
+void lib_free(void *p) {
+    if (!p) return;
+    {
+        std::lock_guard<std::mutex> lock(g_mem_mutex);
+        untrack(p);
+    }
+    (void)cudaFree(p);
+}
+
+void lib_free_async(void *p, cudaStream_t s) {
+    if (!p) return;
+    {
+        std::lock_guard<std::mutex> lock(g_mem_mutex);
+        untrack(p);
+    }
+    (void)cudaFreeAsync(p, s);
+}
+
+void memory_held(int64_t *allocations, int64_t *bytes) {
+    std::lock_guard<std::mutex> lock(g_mem_mutex);
+    if (allocations) *allocations = static_cast<int64_t>(g_mem_live.size());
+    if (bytes) *bytes = g_mem_bytes;
 }
 
 bool device_memory_here(const void *p) {
@@ -61,7 +145,7 @@ void clear_error() {
 int dev_alloc(spmv_handle_t h, void **p, size_t bytes) {
     *p = nullptr;
     if (bytes == 0) return SPMV_OK;
-    cudaError_t e = cudaMalloc(p, bytes);
+    cudaError_t e = lib_malloc(p, bytes);
     if (e != cudaSuccess) {
         *p = nullptr;
         return set_cuda_error(e, "cudaMalloc");
@@ -83,14 +167,14 @@ int dev_alloc_n(spmv_handle_t h, T **p, int64_t count) {
 struct Temp {
     std::vector<void *> ptrs;
     ~Temp() {
-        for (void *p : ptrs) cudaFree(p);
+        for (void *p : ptrs) lib_free(p);
     }
     template <class T>
     int get(T **p, int64_t count) {
         *p = nullptr;
         if (count <= 0) count = 1;
         void *q = nullptr;
-        cudaError_t e = cudaMalloc(&q, static_cast<size_t>(count) * sizeof(T));
+        cudaError_t e = lib_malloc(&q, static_cast<size_t>(count) * sizeof(T));
         if (e != cudaSuccess) return set_cuda_error(e, "cudaMalloc (build temporary)");
         ptrs.push_back(q);
         *p = static_cast<T *>(q);
@@ -927,7 +1011,7 @@ void free_handle(spmv_handle_t h) {
     for (cudaEvent_t e : h->host_events) cudaEventDestroy(e);
     if (h->host_in) cudaStreamDestroy(h->host_in);
     if (h->host_out) cudaStreamDestroy(h->host_out);
-    for (void *p : h->allocations) cudaFree(p);
+    for (void *p : h->allocations) lib_free(p);
     delete h;
 }
 
@@ -1034,6 +1118,22 @@ int check_current_device(spmv_handle_t h) {
     return SPMV_OK;
 }
 
+// SPMV_LOG set to anything but "" or "0": every successful build writes its plan (the
+// spmv_describe JSON) to stderr, one line.
+void log_plan(spmv_handle_t h) {
+    const char *v = std::getenv("SPMV_LOG");
+    if (!v || !*v || (v[0] == '0' && !v[1])) return;
+    std::vector<char> buf(1 << 16);
+    if (spmv_describe(h, buf.data(), buf.size()) != SPMV_OK) {
+        buf.assign(1 << 22, 0);
+        if (spmv_describe(h, buf.data(), buf.size()) != SPMV_OK) {
+            clear_error();
+            return;
+        }
+    }
+    std::fprintf(stderr, "spmv: built %s\n", buf.data());
+}
+
 spmv_handle_t build_impl(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t *col_idx, const void *vals,
                          int dtype, int format, const spmv_format_params *params, cudaStream_t s) {
     clear_error();
@@ -1090,6 +1190,7 @@ spmv_handle_t build_impl(int64_t n, int64_t nnz, const int32_t *row_ptr, const i
         set_error(keep != SPMV_OK ? keep : st, msg);
         return nullptr;
     }
+    log_plan(h);
     return h;
 }
 
@@ -1258,6 +1359,11 @@ int apply_host_pipelined(spmv_handle_t h, const ApplyScratch &sc, const void *x_
 using namespace spmv;
 
 extern "C" {
+
+int spmv_device_memory(int64_t *allocations, int64_t *bytes) {
+    memory_held(allocations, bytes);
+    return SPMV_OK;
+}
 
 int spmv_default_params(spmv_format_params *p) {
     if (!p) return set_error(SPMV_ERR_INVALID_ARG, "NULL params");

@@ -57,12 +57,12 @@ struct Scratch {
     std::vector<void *> ptrs;
     explicit Scratch(cudaStream_t st) : s(st) {}
     ~Scratch() {
-        for (void *p : ptrs) cudaFreeAsync(p, s);
+        for (void *p : ptrs) lib_free_async(p, s);
     }
     template <class T>
     int get(T **p, int64_t count) {
         void *q = nullptr;
-        cudaError_t e = cudaMallocAsync(&q, static_cast<size_t>(std::max<int64_t>(count, 1)) * sizeof(T), s);
+        cudaError_t e = lib_malloc_async(&q, static_cast<size_t>(std::max<int64_t>(count, 1)) * sizeof(T), s);
         if (e != cudaSuccess) return set_cuda_error(e, "cudaMallocAsync (ordering scratch)");
         ptrs.push_back(q);
         *p = static_cast<T *>(q);

@@ -454,7 +454,7 @@ struct StreamBuffer {
     void *ptr = nullptr;
     cudaStream_t s = nullptr;
     ~StreamBuffer() {
-        if (ptr) cudaFreeAsync(ptr, s);
+        if (ptr) lib_free_async(ptr, s);
     }
 };
 
@@ -524,7 +524,7 @@ int cg(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, cudaStr
     StreamBuffer ws;
     ws.s = s;
     const size_t bytes = 4 * vec_pad + kRedBlocks * sizeof(double) + sizeof(Scalars) + sizeof(Control);
-    SPMV_TRY_CUDA(cudaMallocAsync(&ws.ptr, bytes, s));
+    SPMV_TRY_CUDA(lib_malloc_async(&ws.ptr, bytes, s));
     SPMV_TRY_CUDA(cudaMemsetAsync(ws.ptr, 0, bytes, s));
     char *base = static_cast<char *>(ws.ptr);
     P *r = reinterpret_cast<P *>(base);
@@ -592,7 +592,7 @@ int bicgstab(spmv_handle_t h, const T *b, T *x, double rtol, int32_t max_iter, c
     StreamBuffer ws;
     ws.s = s;
     const size_t bytes = 7 * vec_pad + 2 * kRedBlocks * sizeof(double) + sizeof(BiScalars) + sizeof(Control);
-    SPMV_TRY_CUDA(cudaMallocAsync(&ws.ptr, bytes, s));
+    SPMV_TRY_CUDA(lib_malloc_async(&ws.ptr, bytes, s));
     SPMV_TRY_CUDA(cudaMemsetAsync(ws.ptr, 0, bytes, s));
     char *base = static_cast<char *>(ws.ptr);
     P *r = reinterpret_cast<P *>(base);
@@ -912,7 +912,7 @@ int gmres(spmv_handle_t h, const T *b, T *x, int32_t m, double rtol, int32_t max
     ws.s = s;
     const size_t bytes = static_cast<size_t>(m + 2) * vec_pad + static_cast<size_t>(kGmMax + 1) * kRedBlocks * sizeof(double) +
                          sizeof(GmScalars) + sizeof(Control);
-    SPMV_TRY_CUDA(cudaMallocAsync(&ws.ptr, bytes, s));
+    SPMV_TRY_CUDA(lib_malloc_async(&ws.ptr, bytes, s));
     SPMV_TRY_CUDA(cudaMemsetAsync(ws.ptr, 0, bytes, s));
     char *base = static_cast<char *>(ws.ptr);
     P *V = reinterpret_cast<P *>(base);

@@ -210,6 +210,17 @@ namespace spmv {
 int set_error(int status, const std::string &msg);
 int set_cuda_error(cudaError_t err, const char *what);
 
+// ----------------------------------------------------------------------------
+// device memory of the library -- api.cu
+// ----------------------------------------------------------------------------
+// Every device allocation of the library goes through these: they keep the count and
+// size of what it holds (spmv_device_memory) and fail an allocation on request (the
+// SPMV_FAIL_ALLOC environment variable, a host-side fault injector for tests).
+cudaError_t lib_malloc(void **p, size_t bytes);
+cudaError_t lib_malloc_async(void **p, size_t bytes, cudaStream_t s);
+void lib_free(void *p);
+void lib_free_async(void *p, cudaStream_t s);
+
 #define SPMV_TRY_CUDA(expr)                                              \
     do {                                                                 \
         cudaError_t spmv_err__ = (expr);                                 \
