@@ -441,6 +441,7 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
                            "best of 5 launches of 2^28 lane loads: random elements (the request rate, one line "
                            "each) and groups of 4 lanes reading the 4 sectors of a random line (the sector rate)"}
     A.close()
+    y_host = y.cpu().numpy() if (cpu or keep) else None  # A x, for the parity check of the CPU leg
     del rp, ci, vv, x, y
     torch.cuda.empty_cache()
 
@@ -487,10 +488,10 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
     if gather:
         rec["gather_roofline"] = gather
     if cpu:  # context per configuration: the oracle on a short row sample, the OpenMP product on all of it
-        rec["cpu_oracle"] = cpu_baseline(csr, x_np, budget_s=1.5)
+        rec["cpu_oracle"] = cpu_baseline(csr, x_np, budget_s=1.5, y_gpu=y_host)
         rec["cpu_openmp"] = cpu_openmp_baseline(csr, x_np, "dynamic" if name.startswith("powerlaw") else "static")
     if keep:
-        rec["_csr"], rec["_x"] = csr, x_np
+        rec["_csr"], rec["_x"], rec["_y"] = csr, x_np, y_host
     return rec
 
 
@@ -516,8 +517,10 @@ def measure_e2e(torch, spmv, csr, x_np, steps):
     return statistics.median(times)
 
 
-def cpu_baseline(csr, x_np, budget_s=10.0):
-    """The oracle as it stands (single thread, long double) on a row prefix sized to the budget."""
+def cpu_baseline(csr, x_np, budget_s=10.0, y_gpu=None):
+    """The oracle as it stands (single thread, long double) on a row prefix sized to the
+    budget.  With y_gpu (the GPU's A x for the same x) the rows the oracle computed are
+    also checked against it: the worst |y - y_ref| / (tau * sum |a_ij x_j|) over them."""
     import numpy as np
 
     import oracle
@@ -528,13 +531,20 @@ def cpu_baseline(csr, x_np, budget_s=10.0):
     dt = max(time.perf_counter() - t0, 1e-6)
     rows = int(min(csr.n, max(probe, probe * budget_s / dt)))
     t0 = time.perf_counter()
-    oracle.spmv(csr, x_np, rows=np.arange(rows))
+    ref = oracle.spmv(csr, x_np, rows=np.arange(rows))
     dt = time.perf_counter() - t0
     nnz = int(csr.row_ptr[rows])
-    return {"value": 2.0 * nnz / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of the workload ({nnz} nonzeros), one pass, "
-                      f"single-threaded long double (LDBL_MANT_DIG={oracle.ldbl_mant_dig()})",
-            "seconds": dt}
+    out = {"value": 2.0 * nnz / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"rows 0..{rows - 1} of the workload ({nnz} nonzeros), one pass, "
+                     f"single-threaded long double (LDBL_MANT_DIG={oracle.ldbl_mant_dig()})",
+           "seconds": dt}
+    if y_gpu is not None:
+        dtype = csr.vals.dtype
+        ok, worst, at = oracle.check_rows(np.asarray(y_gpu)[:rows], ref, dtype)
+        out["parity"] = {"rows": rows, "within_tolerance": ok, "max_error_ratio": worst, "worst_row": at,
+                         "tau": oracle.TAU[np.dtype(dtype)],
+                         "rule": "|y - y_ref| <= tau * sum |a_ij x_j| per row (1.0 = at the tolerance)"}
+    return out
 
 
 def cpu_model() -> str:
@@ -604,7 +614,7 @@ def run_ours(args):
         if sampler:
             sampler.stop()
     head = records[headline]
-    csr, x_np = head.pop("_csr"), head.pop("_x")
+    csr, x_np, y_host = head.pop("_csr"), head.pop("_x"), head.pop("_y")
     e2e_steps = max(args.steps, 3)
     e2e_t = reduce_max(measure_e2e(torch, spmv, csr, x_np, e2e_steps), world,
                        device=torch.device("cuda", dev_index))
@@ -646,7 +656,7 @@ def run_ours(args):
     if "gather_roofline" in head:
         line["gather_roofline"] = head["gather_roofline"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(csr, x_np)
+        line["cpu_baseline"] = cpu_baseline(csr, x_np, y_gpu=y_host)
         line["cpu_openmp"] = cpu_openmp_baseline(csr, x_np,
                                                  "dynamic" if headline[0].startswith("powerlaw") else "static")
     print(json.dumps(line), flush=True)
@@ -997,8 +1007,8 @@ def run_sweep(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="all",
                     help="all = every configuration (headline: uniform16_16m); or one workload name")

@@ -54,6 +54,29 @@ def test_random_gather_footprint_model():
     assert bench.gather_bound_ms(m, 504e3 / 4, 1e9) == pytest.approx(4.0)  # requests dominate
 
 
+def test_cpu_leg_parity_field():
+    """The CPU leg checks a given y on the rows the oracle computed: the oracle's own
+    result (rounded once to double) passes far inside the tolerance; one planted error
+    far above the tolerance fails there."""
+    import numpy as np
+
+    from workloads import laplacian_2d, uniform_x
+
+    csr = laplacian_2d(40, 30)
+    x = uniform_x(csr.n, seed=3)
+    import oracle
+
+    y = oracle.spmv(csr, x)["y"]
+    rec = bench.cpu_baseline(csr, x, budget_s=0.01, y_gpu=y)
+    assert rec["parity"]["within_tolerance"] and rec["parity"]["max_error_ratio"] < 1e-3
+    assert rec["parity"]["rows"] == csr.n  # the sample never falls below 20,000 rows (or n)
+    bad = y.copy()
+    bad[77] += 1e-6
+    rec = bench.cpu_baseline(csr, x, budget_s=0.01, y_gpu=bad)
+    assert not rec["parity"]["within_tolerance"] and rec["parity"]["worst_row"] == 77
+    assert rec["parity"]["max_error_ratio"] > 1.0
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))

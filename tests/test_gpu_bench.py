@@ -45,6 +45,8 @@ def test_bench_line_contract():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == n * 8 == e["d2h_bytes_per_step"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    par = d["cpu_baseline"]["parity"]  # the GPU result on the rows the oracle computed
+    assert par["within_tolerance"] is True and 0 <= par["max_error_ratio"] <= 1.0 and par["rows"] > 0
     assert d["cpu_openmp"]["cores"] >= 1
     g = d["gather_roofline"]  # the power-law shape carries the random-gather roofline
     assert g["probe_gathers_per_s"] > 0 and g["probe_sectors_per_s"] > 0 and 0 < g["frac_of_gather_bound"]
