@@ -124,3 +124,38 @@ def test_params_struct_layout_matches_header(tmp_path):
         assert int(got[f]) == getattr(spmv._abi.FormatParams, f).offset, f
     p = spmv.spmv_default_params()
     assert all(getattr(p, f) == -1 for f in fields), {f: getattr(p, f) for f in fields}
+
+
+def test_size_and_argument_limits_refused_before_any_cuda_call(libpath):
+    """n and nnz must lie in [0, 2^31), dtype must be F64 or F32, the probe takes 1, 2 or 4
+    sectors per line, and the allocation-free call refuses sizes past its fixed scratch:
+    each refusal comes before the library touches CUDA or dereferences a pointer, so
+    host arrays stand in for device ones here and nothing runs on a device."""
+    import numpy as np
+
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    dummy = np.zeros(4, np.int32)  # never read
+    for n, nnz in ((1 << 31, 0), (4, 1 << 31), (-1, 0), (4, -1)):
+        with pytest.raises(spmv.SpmvError) as ei:
+            spmv.spmv_build_from_csr(n, nnz, dummy, dummy, dummy, 0, "auto")
+        assert ei.value.status == -1, (n, nnz)
+        with pytest.raises(spmv.SpmvError) as ei:
+            spmv.spmv_csr_apply_noalloc(n, nnz, dummy, dummy, dummy, 0, dummy, dummy, 0)
+        assert ei.value.status == -1, (n, nnz)
+    with pytest.raises(spmv.SpmvError) as ei:
+        spmv.spmv_build_from_csr(4, 0, dummy, None, None, 7, "auto")  # no such value type
+    assert ei.value.status == -1
+    with pytest.raises(spmv.SpmvError) as ei:
+        spmv.spmv_build_from_csr(4, 0, dummy, None, None, 0, 9)  # no such format
+    assert ei.value.status == -1
+    # n + nnz above the allocation-free limit (134,217,728 path items)
+    with pytest.raises(spmv.SpmvError) as ei:
+        spmv.spmv_csr_apply_noalloc(100_000_000, 100_000_000, dummy, dummy, dummy, 0, dummy, dummy, 0)
+    assert ei.value.status == -5
+    spmv.spmv_csr_apply_noalloc(0, 0, None, None, None, 0, None, None, 0)  # n = 0: nothing to do
+    for spl in (0, 3, 8):
+        with pytest.raises(spmv.SpmvError) as ei:
+            spmv.spmv_probe_gather(dummy, 4, 0, spl, 10, dummy, 0)
+        assert ei.value.status == -1
+    assert spmv.spmv_device_memory() == (0, 0)  # nothing allocated in this process
