@@ -229,7 +229,10 @@ SPMV_API spmv_handle_t spmv_build_from_csr_ex(int64_t n, int64_t nnz, const int3
  * y = A x, overwriting y (no scaling, no accumulation into the old y).
  * x and y are device arrays of n elements of the handle's value type, in the
  * caller's original row order (any row permutation of the format is internal);
- * overlapping x and y are refused with SPMV_ERR_INVALID_ARG.
+ * overlapping x and y, and an x or y that is not memory of the current device (host
+ * memory, pinned or not, or another device's), are refused with SPMV_ERR_INVALID_ARG
+ * before anything is enqueued.  The same holds for the vectors of spmv_apply_ex,
+ * spmv_apply_multi, spmv_apply_profiled, spmv_permute_vector and the solvers.
  * Asynchronous on `stream`: returns after enqueueing 1 to 6 kernel launches (one for the
  * SELL / ELLPACK-R plans AUTO picks; CSR-vector: one per row-length bin and the row-split).
  * The apply only reads the handle's matrix data.  What it writes besides y (the carries

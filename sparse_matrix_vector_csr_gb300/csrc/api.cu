@@ -1109,6 +1109,13 @@ int check_device_flag(spmv_handle_t h) {
     return set_error(SPMV_ERR_TIMEOUT, "an apply kernel gave up waiting for its bulk copies (results invalid)");
 }
 
+// The vector arguments of an apply: device memory of the current device (a host or
+// another device's pointer is refused before anything is enqueued).
+int check_vectors(const void *a, const char *an, const void *b, const char *bn) {
+    SPMV_TRY(check_device_pointer(a, an));
+    return check_device_pointer(b, bn);
+}
+
 int check_current_device(spmv_handle_t h) {
     int dev = -1;
     SPMV_TRY_CUDA(cudaGetDevice(&dev));
@@ -1473,6 +1480,7 @@ int spmv_permute_vector(spmv_handle_t h, const void *src, void *dst, int directi
     if (!src || !dst) return set_error(SPMV_ERR_INVALID_ARG, "NULL src or dst");
     if (vectors_alias(h, src, dst)) return set_error(SPMV_ERR_INVALID_ARG, "src and dst must not overlap");
     SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_vectors(src, "src", dst, "dst"));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!h->basis_perm) {
         SPMV_TRY_CUDA(cudaMemcpyAsync(dst, src, value_bytes(h->dtype) * h->n, cudaMemcpyDeviceToDevice, s));
@@ -1488,6 +1496,7 @@ int spmv_apply(spmv_handle_t h, const void *x, void *y, void *stream) {
     if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
     if (vectors_alias(h, x, y)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
     SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_vectors(x, "x", y, "y"));
     return enqueue(h, x, y, static_cast<cudaStream_t>(stream), nullptr);
 }
 
@@ -1568,6 +1577,7 @@ int spmv_apply_profiled(spmv_handle_t h, const void *x, void *y, void *stream, f
     if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
     if (vectors_alias(h, x, y)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
     SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_vectors(x, "x", y, "y"));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Recorder rec;
     SPMV_TRY(enqueue(h, x, y, s, &rec));
@@ -1588,6 +1598,7 @@ int spmv_apply_ex(spmv_handle_t h, double alpha, const void *x, double beta, voi
     if (!x || !y) return set_error(SPMV_ERR_INVALID_ARG, "NULL x or y");
     if (vectors_alias(h, x, y)) return set_error(SPMV_ERR_INVALID_ARG, "x and y overlap");
     SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_vectors(x, "x", y, "y"));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (alpha == 1.0 && beta == 0.0) return enqueue(h, x, y, s, nullptr);
     const Scale scale{alpha, beta};
@@ -1607,6 +1618,7 @@ int spmv_apply_multi(spmv_handle_t h, int64_t k, double alpha, const void *X, in
         if (spans_overlap(X, xspan, Y, yspan)) return set_error(SPMV_ERR_INVALID_ARG, "X and Y overlap");
     }
     SPMV_TRY(check_current_device(h));
+    SPMV_TRY(check_vectors(X, "X", Y, "Y"));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (k == 1 && ldx == 1 && ldy == 1) return spmv_apply_ex(h, alpha, X, beta, Y, stream);  // contiguous vectors
     const size_t vb = value_bytes(h->dtype);

@@ -997,6 +997,18 @@ int gmres(spmv_handle_t h, const T *b, T *x, int32_t m, double rtol, int32_t max
 using namespace spmv;
 
 namespace {
+// b and x: device memory of the current device, which must be the handle's
+int check_solve_vectors(spmv_handle_t h, const void *b, const void *x) {
+    int dev = -1;
+    SPMV_TRY_CUDA(cudaGetDevice(&dev));
+    if (dev != h->device)
+        return set_error(SPMV_ERR_INVALID_ARG, "the handle belongs to CUDA device " + std::to_string(h->device) +
+                                                   " but device " + std::to_string(dev) + " is current");
+    if (!device_memory_here(b) || !device_memory_here(x))
+        return set_error(SPMV_ERR_INVALID_ARG, "b and x must be device memory of the current device");
+    return SPMV_OK;
+}
+
 // two vectors of the handle's n values share a byte
 bool overlapping(spmv_handle_t h, const void *a, const void *b) {
     const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
@@ -1014,6 +1026,7 @@ extern "C" SPMV_API int spmv_cg(spmv_handle_t h, const void *b, void *x, double 
     if (h->n == 0) return SPMV_OK;
     if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
     if (overlapping(h, b, x)) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not overlap");
+    SPMV_TRY(check_solve_vectors(h, b, x));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->dtype == SPMV_F64)
         return cg<double>(h, static_cast<const double *>(b), static_cast<double *>(x), rtol, max_iter, s, iterations,
@@ -1031,6 +1044,7 @@ extern "C" SPMV_API int spmv_bicgstab(spmv_handle_t h, const void *b, void *x, d
     if (h->n == 0) return SPMV_OK;
     if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
     if (overlapping(h, b, x)) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not overlap");
+    SPMV_TRY(check_solve_vectors(h, b, x));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->dtype == SPMV_F64)
         return bicgstab<double>(h, static_cast<const double *>(b), static_cast<double *>(x), rtol, max_iter, s,
@@ -1050,6 +1064,7 @@ extern "C" SPMV_API int spmv_gmres(spmv_handle_t h, const void *b, void *x, int3
     if (h->n == 0) return SPMV_OK;
     if (!b || !x) return set_error(SPMV_ERR_INVALID_ARG, "NULL b or x");
     if (overlapping(h, b, x)) return set_error(SPMV_ERR_INVALID_ARG, "b and x must not overlap");
+    SPMV_TRY(check_solve_vectors(h, b, x));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->dtype == SPMV_F64)
         return gmres<double>(h, static_cast<const double *>(b), static_cast<double *>(x), restart, rtol, max_iter, s,

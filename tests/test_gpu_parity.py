@@ -315,6 +315,40 @@ def test_host_pointers_are_rejected():
     assert ei.value.status == -1
 
 
+def test_host_vectors_are_refused_by_the_applies():
+    """Vectors that are not device memory of the current device (a pageable numpy array,
+    a pinned tensor) are refused before anything is enqueued; device vectors still work."""
+    import sparse_matrix_vector_csr_gb300 as spmv
+
+    torch = torch_cuda()
+    csr = random_csr(300, 0.05, seed=4)
+    x_np = uniform_x(csr.n)
+    xd = torch.from_numpy(x_np).cuda()
+    yd = torch.full_like(xd, float("nan"))
+    pinned = torch.from_numpy(x_np.copy()).pin_memory()
+    with build(csr, "auto") as A:
+        h = A._h
+        for bad_x, bad_y in ((x_np, yd), (xd, np.empty(csr.n)), (pinned, yd), (xd, pinned)):
+            for call in (lambda: spmv.spmv_apply(h, bad_x, bad_y, 0),
+                         lambda: spmv.spmv_apply_ex(h, 2.0, bad_x, 0.5, bad_y, 0),
+                         lambda: spmv.spmv_permute_vector(h, bad_x, bad_y, 0, 0)):
+                with pytest.raises(spmv.SpmvError) as ei:
+                    call()
+                assert ei.value.status == -1
+        X = np.zeros((csr.n, 2))
+        with pytest.raises(spmv.SpmvError) as ei:
+            spmv.spmv_apply_multi(h, 2, 1.0, X, 2, 0.0, torch.zeros(csr.n, 2, dtype=torch.float64, device="cuda"), 2, 0)
+        assert ei.value.status == -1
+        with pytest.raises(spmv.SpmvError) as ei:
+            spmv.spmv_cg(h, x_np, yd, 1e-8, 10, 0)
+        assert ei.value.status == -1
+        torch.cuda.synchronize()
+        assert torch.isnan(yd).all()  # nothing ran
+        A.apply(xd, yd)
+        torch.cuda.synchronize()
+        assert_parity(yd.cpu().numpy(), oracle.spmv(csr, x_np), np.float64)
+
+
 def test_too_large_layout_is_refused():
     import sparse_matrix_vector_csr_gb300 as spmv
 
