@@ -621,6 +621,12 @@ int plan_sliced(BuildCtx &c, const int32_t *lens, int32_t C, int64_t sigma, int6
             for (int64_t s = 1; s < sl.n_slices && monotone; ++s) monotone = widths[s] <= widths[s - 1];
             if (monotone) {
                 sl.has_tail = true;
+                int sms = 0;
+                if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c.h->device) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    sms = 152;
+                }
+                sl.tail_cap = 12 * static_cast<int64_t>(sms);
                 int64_t s = 0, slot = 0;
                 for (int w = kTailMaxW; w >= 0; --w) {  // first slice of width <= w, and its slot
                     while (s < sl.n_slices && widths[s] > w) slot += static_cast<int64_t>(widths[s++]) * sl.C;

@@ -16,6 +16,7 @@
 // y, so both run in one launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "device_util.cuh"
@@ -291,7 +292,9 @@ __device__ __forceinline__ void sell_tail(int64_t warp, int lane, const SellArgs
 
 // A globally sorted layout with a narrow tail: the first split_ctas CTAs take the long
 // rows' chunks (one per warp, as in k_sell_split; none without long rows), the next
-// head_ctas the positions before the tail (one per thread), the rest the tail.
+// head_ctas the positions before the tail (one per thread), the rest the tail -- one
+// group of 2 x 32 rows per warp with chunks in the launch (the tail CTAs then fill the
+// slots the chunks leave), or, without chunks, at most Sliced::tail_cap CTAs that loop.
 template <typename T, bool K, bool SPLIT>
 __global__ void __launch_bounds__(kSellBlock, SPLIT ? 6 : 8)
     k_sell_tail(SellArgs a, const T *__restrict__ val, SplitArgs b, const T *__restrict__ split_val,
@@ -309,8 +312,18 @@ __global__ void __launch_bounds__(kSellBlock, SPLIT ? 6 : 8)
         if (p < t.slice[kTailW] * 32) sell_row<T, 32, K>(p, a, val, x, y, ep);
         return;
     }
-    const int64_t warp = (hb - head_ctas) * (kSellBlock / 32) + (threadIdx.x >> 5);
-    sell_tail<T, K>(warp, threadIdx.x & 31, a, t, val, x, y, ep);
+    const int64_t first = (hb - head_ctas) * (kSellBlock / 32) + (threadIdx.x >> 5);
+    if constexpr (SPLIT) {
+        sell_tail<T, K>(first, threadIdx.x & 31, a, t, val, x, y, ep);
+    } else {
+        // no chunks in the launch: the tail CTAs are capped and each loops over the tail
+        // (a CTA of two rows a thread lives a few microseconds; launching one per 512 rows
+        // left the SMs' slots idle between CTAs)
+        const int64_t stride = (static_cast<int64_t>(gridDim.x) - head_ctas) * (kSellBlock / 32);
+        const int64_t n_warps = (t.n_slices - t.slice[kTailW] + kTailR - 1) / kTailR;
+        for (int64_t warp = first; warp < n_warps; warp += stride)
+            sell_tail<T, K>(warp, threadIdx.x & 31, a, t, val, x, y, ep);
+    }
 }
 
 // Row-split chunks alone (long rows next to the CSR-vector bins).
@@ -363,7 +376,8 @@ cudaError_t sell_launch(const Sliced &sl, int64_t n, const Segmented *sg, const 
         }
         const int64_t split_ctas = split ? ceil_div(sg->n_chunks * 32, kSellBlock) : 0;
         const int64_t head_ctas = ceil_div(t.slice[kTailW] * 32, kSellBlock);
-        const int64_t tail_ctas = ceil_div(sl.n_slices - t.slice[kTailW], (kSellBlock / 32) * kTailR);
+        int64_t tail_ctas = ceil_div(sl.n_slices - t.slice[kTailW], (kSellBlock / 32) * kTailR);
+        if (!split && sl.tail_cap > 0) tail_ctas = std::min(tail_ctas, sl.tail_cap);
         cfg.gridDim = dim3(static_cast<unsigned>(split_ctas + head_ctas + tail_ctas));
         const SplitArgs b = split ? split_args(*sg) : SplitArgs{};
         const T *split_val = split ? static_cast<const T *>(sg->val) : nullptr;

@@ -72,6 +72,9 @@ struct Sliced {
     bool has_tail = false;
     int64_t tail_slice[kTailMaxW + 1] = {};
     int64_t tail_slot[kTailMaxW + 1] = {};
+    // CTAs for the narrow tail when no long-row chunks share the launch (12 per SM): each
+    // loops over the tail instead of a short-lived CTA per 512 rows
+    int64_t tail_cap = 0;
     int64_t *slice_ptr = nullptr;  // [n_slices + 1]
     int32_t *width = nullptr;      // [n_slices]
     int32_t *len = nullptr;        // [n_pos] entries stored at each position

@@ -146,3 +146,28 @@ def test_width_exact_kernel_above_a_wave(shape):
             assert d["format"] == "sell" and d["max_width"] in (3, 5) and d["sigma"] == 1
             y = run(A, x)
             assert_parity(y, oracle.spmv(csr, x), np.float64, exact=integer, label=f"{shape} integer={integer}")
+
+
+@pytest.mark.parametrize("integer", [True, False], ids=["integer", "real"])
+def test_capped_tail_loops_without_long_rows(integer):
+    """No row longer than the threshold, so no chunks share the launch: the tail runs on
+    at most 12 CTAs per SM, each looping over groups of 64 rows.  2.5 M rows, three in
+    four of at most 2 entries, give over two groups per warp."""
+    from workloads import CSR
+
+    rng = np.random.default_rng(31)
+    n = 2_500_000
+    lens = rng.choice([0, 1, 2, 3, 7], size=n, p=[0.15, 0.45, 0.25, 0.1, 0.05])
+    rp = np.zeros(n + 1, np.int64)
+    np.cumsum(lens, out=rp[1:])
+    col = rng.integers(2, n, size=int(rp[-1])).astype(np.int32)  # unsorted, duplicates allowed
+    vals = (rng.integers(-8, 9, col.size) if integer else rng.standard_normal(col.size)).astype(np.float64)
+    csr = CSR(n, rp.astype(np.int32), col, vals)
+    x = (rng.integers(-8, 9, n) if integer else uniform_x(n, seed=32)).astype(np.float64)
+    x[0], x[1] = np.inf, np.nan  # referenced by no stored entry
+    with build(csr, "sell", C=32, sigma=1 << 30) as A:
+        d = A.describe()
+        assert d["n_long_rows"] == 0 and d["tail_positions"] > 12 * 152 * 8 * 64, d
+        y = run(A, x)
+        assert np.all(np.isfinite(y))
+        assert_parity(y, oracle.spmv(csr, x), np.float64, exact=integer, label="capped tail")
