@@ -332,8 +332,8 @@ int cuthill_mckee(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t 
     const int vbits = bits(static_cast<uint64_t>(n));  // keys up to n (the diagonal sentinel)
     // graph of A + A^T: sorted, distinct adjacency lists without self loops
     const int64_t m = 2 * nnz;
-    uint32_t *u0, *u1;
-    int32_t *v0, *v1;
+    uint32_t *u0 = nullptr, *u1 = nullptr;
+    int32_t *v0 = nullptr, *v1 = nullptr;
     SPMV_TRY(sc.get(&u0, m));
     SPMV_TRY(sc.get(&u1, m));
     SPMV_TRY(sc.get(&v0, m));
@@ -352,9 +352,9 @@ int cuthill_mckee(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t 
     SPMV_TRY(radix_sort(kc, vc, kd, vd, m, vbits, rt, s));  // kc: rows, vc: columns
     u0 = kc;
     v0 = vc;
-    int64_t *flag, *epos, *scan_tmp, *gptr, *deg64;
+    int64_t *flag = nullptr, *epos = nullptr, *scan_tmp = nullptr, *gptr = nullptr, *deg64 = nullptr;
     unsigned long long *deg;
-    int32_t *adj;
+    int32_t *adj = nullptr;
     SPMV_TRY(sc.get(&flag, m));
     SPMV_TRY(sc.get(&epos, m + 1));
     SPMV_TRY(sc.get(&scan_tmp, scan_temp_elems(std::max<int64_t>(m, n))));
@@ -376,8 +376,8 @@ int cuthill_mckee(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t 
     SPMV_TRY_CUDA(cudaGetLastError());
 
     // (degree, index) order: stable sort of the indices by degree
-    uint32_t *dk0, *dk1;
-    int32_t *by_rank, *r1, *rank, *pos, *claim, *cand;
+    uint32_t *dk0 = nullptr, *dk1 = nullptr;
+    int32_t *by_rank = nullptr, *r1 = nullptr, *rank = nullptr, *pos = nullptr, *claim = nullptr, *cand = nullptr;
     SPMV_TRY(sc.get(&dk0, n));
     SPMV_TRY(sc.get(&dk1, n));
     SPMV_TRY(sc.get(&by_rank, n));
@@ -405,8 +405,8 @@ int cuthill_mckee(int64_t n, int64_t nnz, const int32_t *row_ptr, const int32_t 
     SPMV_TRY_CUDA(cudaGetLastError());
 
     // sort buffers for large levels
-    uint32_t *lk0, *lk1;
-    int32_t *lv0, *lv1;
+    uint32_t *lk0 = nullptr, *lk1 = nullptr;
+    int32_t *lv0 = nullptr, *lv1 = nullptr;
     SPMV_TRY(sc.get(&lk0, n));
     SPMV_TRY(sc.get(&lk1, n));
     SPMV_TRY(sc.get(&lv0, n));
@@ -471,8 +471,8 @@ int compute_ordering(int ordering, int64_t n, int64_t nnz, const int32_t *row_pt
             Scratch sc(s);
             RadixTemp rt;
             SPMV_TRY(rt.init(sc, n));
-            uint32_t *k0, *k1;
-            int32_t *v1;
+            uint32_t *k0 = nullptr, *k1 = nullptr;
+            int32_t *v1 = nullptr;
             SPMV_TRY(sc.get(&k0, n));
             SPMV_TRY(sc.get(&k1, n));
             SPMV_TRY(sc.get(&v1, n));
@@ -487,7 +487,7 @@ int compute_ordering(int ordering, int64_t n, int64_t nnz, const int32_t *row_pt
         }
         case SPMV_ORDER_RCM: {
             Scratch sc(s);
-            int32_t *order;
+            int32_t *order = nullptr;
             SPMV_TRY(sc.get(&order, n));
             SPMV_TRY(cuthill_mckee(n, nnz, row_ptr, col, order, s));
             k_reverse<<<grid(n), kThreads, 0, s>>>(n, order, perm);
@@ -498,7 +498,7 @@ int compute_ordering(int ordering, int64_t n, int64_t nnz, const int32_t *row_pt
         case SPMV_ORDER_USER: {
             if (!user_perm) return set_error(SPMV_ERR_INVALID_ARG, "ordering USER needs a permutation");
             Scratch sc(s);
-            int32_t *seen, *status;
+            int32_t *seen = nullptr, *status = nullptr;
             SPMV_TRY(sc.get(&seen, n));
             SPMV_TRY(sc.get(&status, 2));
             SPMV_TRY_CUDA(cudaMemsetAsync(seen, 0, sizeof(int32_t) * n, s));
@@ -525,8 +525,8 @@ int permute_csr(int dtype, int64_t n, int64_t nnz, const int32_t *row_ptr, const
         return SPMV_OK;
     }
     Scratch sc(s);
-    int32_t *inv;
-    int64_t *len, *ptr64, *scan_tmp;
+    int32_t *inv = nullptr;
+    int64_t *len = nullptr, *ptr64 = nullptr, *scan_tmp = nullptr;
     SPMV_TRY(sc.get(&inv, n));
     SPMV_TRY(sc.get(&len, n));
     SPMV_TRY(sc.get(&ptr64, n + 1));
