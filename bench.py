@@ -487,6 +487,10 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
                         "note": "not HBM-bound: the matrix fits in L2; launch and latency figures"}
     if gather:
         rec["gather_roofline"] = gather
+        # the limit that binds here: the requests an SM sends to L2, not HBM bandwidth
+        rec["roofline"]["binding_limit"] = {"kind": "L1-to-L2 requests of the x gathers and the stream",
+                                            "frac": gather["frac_of_gather_bound"],
+                                            "bound_ms": gather["bound_ms"], "see": "gather_roofline"}
     if cpu:  # context per configuration: the oracle on a short row sample, the OpenMP product on all of it
         rec["cpu_oracle"] = cpu_baseline(csr, x_np, budget_s=1.5, y_gpu=y_host)
         rec["cpu_openmp"] = cpu_openmp_baseline(csr, x_np, "dynamic" if name.startswith("powerlaw") else "static")

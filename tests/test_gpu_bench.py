@@ -50,6 +50,7 @@ def test_bench_line_contract():
     assert d["cpu_openmp"]["cores"] >= 1
     g = d["gather_roofline"]  # the power-law shape carries the random-gather roofline
     assert g["probe_gathers_per_s"] > 0 and g["probe_sectors_per_s"] > 0 and 0 < g["frac_of_gather_bound"]
+    assert d["roofline"]["binding_limit"]["frac"] == g["frac_of_gather_bound"]
     assert 0 < g["lines"] <= g["sectors"] and g["bound_ms"] == pytest.approx(
         max(g["lines"] / g["probe_gathers_per_s"], g["sectors"] / g["probe_sectors_per_s"]) * 1e3)
     assert d["configs"] == []  # one workload asked for: the headline alone
