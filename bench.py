@@ -254,6 +254,16 @@ BENCH_CONFIGS = [
 HEADLINE = ("uniform16_16m", "f32")
 #: timed regions of K applies each; the line reports their median and spread
 REPEATS = 11
+MIN_REPEATS = 3
+TIMED_BUDGET_MS = 30000.0  # timed work per configuration: fewer regions when K applies take long
+E2E_BUDGET_S = 10.0  # each of the three end-to-end runs
+
+
+def region_count(first_region_ms: float) -> int:
+    """Timed regions for a configuration whose first region took first_region_ms (max
+    over ranks): REPEATS, or as many as fit TIMED_BUDGET_MS, but at least MIN_REPEATS."""
+    fit = int(TIMED_BUDGET_MS // max(first_region_ms, 1e-6))
+    return max(MIN_REPEATS, min(REPEATS, fit))
 #: matrices small enough to sit in L2: timed under a CUDA graph, flagged "not HBM-bound"
 GRAPH_TIMED = ("lap2d_256",)
 #: applies captured per CUDA graph for the launch-bound configurations
@@ -368,7 +378,8 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
         rc |= apply_c(*args)
     torch.cuda.synchronize()
     regions, t0, t1 = [], None, None
-    for _ in range(REPEATS):
+    n_regions = REPEATS
+    while len(regions) < n_regions:
         barrier(world, dev_index)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -381,6 +392,8 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
         torch.cuda.synchronize()
         barrier(world, dev_index)
         regions.append(e0.elapsed_time(e1))
+        if len(regions) == 1:  # every rank takes the same count, from the slowest first region
+            n_regions = region_count(reduce_max(regions[0], world, device=dev))
     t1 = time.time()
     if rc:
         raise RuntimeError(f"spmv_apply failed on {name}: {spmv.spmv_last_error_message()}")
@@ -463,7 +476,7 @@ def measure_config(torch, spmv, name, tag, steps, warmup, world, dev_index, samp
         "workload": name, "dtype": tag, "desc": WORKLOADS[name]["desc"], "n": n, "nnz": nnz,
         "value": 2.0 * nnz * world / (ms / 1e3) / 1e9, "unit": UNIT,
         "ms_per_step": ms, "ms_per_step_p10": percentile(regions, 0.1) / steps,
-        "ms_per_step_p90": percentile(regions, 0.9) / steps, "regions": REPEATS, "steps_per_region": steps,
+        "ms_per_step_p90": percentile(regions, 0.9) / steps, "regions": len(regions), "steps_per_region": steps,
         "effective_gbs": beff / (ms / 1e3) / 1e9,
         "cold_ms_per_step": cold_ms, "cold_effective_gbs": beff / (cold_ms / 1e3) / 1e9,
         "build_ms": build_ms, "generate_s": gen_s,
@@ -619,7 +632,11 @@ def run_ours(args):
             sampler.stop()
     head = records[headline]
     csr, x_np, y_host = head.pop("_csr"), head.pop("_x"), head.pop("_y")
-    e2e_steps = max(args.steps, 3)
+    # as many host-buffer calls as fit E2E_BUDGET_S a run (three runs), at least 3: the
+    # estimate (the headline apply, max over ranks, plus x in and y out at 150 GB/s) is
+    # the same on every rank
+    call_s = head["ms_per_step"] / 1e3 + 2.0 * csr.n * csr.vals.dtype.itemsize / 150e9
+    e2e_steps = max(3, min(args.steps, int(E2E_BUDGET_S / call_s)))
     e2e_t = reduce_max(measure_e2e(torch, spmv, csr, x_np, e2e_steps), world,
                        device=torch.device("cuda", dev_index))
     if rank != 0:
@@ -635,9 +652,10 @@ def run_ours(args):
             "workload": f"{WORKLOADS[headline[0]]['desc']} (nnz={csr.nnz}), {'float64' if sv == 8 else 'float32'}",
             "n": csr.n, "nnz": csr.nnz, "format": head["format"]["format"],
             "parallelism": "replicas" if world > 1 else "single",
-            "timing": (f"{REPEATS} timed regions of {args.steps} back-to-back applies after {args.warmup} warm-up "
-                       "applies, barrier + synchronize around each region; value and ms_per_step from the median "
-                       "region (max over ranks), p10/p90 beside it"),
+            "timing": (f"{head['regions']} timed regions of {args.steps} back-to-back applies after {args.warmup} "
+                       "warm-up applies, barrier + synchronize around each region; value and ms_per_step from the "
+                       f"median region (max over ranks), p10/p90 beside it; up to {REPEATS} regions, fewer (at least "
+                       f"{MIN_REPEATS}) where {REPEATS} would exceed {TIMED_BUDGET_MS / 1e3:.0f} s of timed work"),
             "l2": (f"inputs larger than L2: one apply streams {beff / 1e6:.0f} MB > {l2_bytes / 1e6:.0f} MB L2"
                    if beff > l2_bytes else f"stream of {beff / 1e6:.0f} MB fits in the {l2_bytes / 1e6:.0f} MB L2; "
                                            "cold_* fields flush L2 before every apply"),

@@ -30,6 +30,14 @@ def test_percentile_and_config_selection():
     assert bench.selected_configs("lap3d_128") == ([("lap3d_128", "f64"), ("lap3d_128", "f32")], ("lap3d_128", "f64"))
 
 
+def test_region_count_fits_the_timed_budget():
+    """11 regions while they fit 30 s of timed work; fewer for long regions, never below 3."""
+    assert bench.region_count(1.0) == 11
+    assert bench.region_count(2700.0) == 11 and bench.region_count(2800.0) == 10
+    assert bench.region_count(5000.0) == 6
+    assert bench.region_count(20000.0) == 3 and bench.region_count(1e9) == 3
+
+
 def test_random_gather_footprint_model():
     """Short rows: one line and one sector per entry.  A long row of sorted columns 0..199
     in float64 (4 values per 32-byte sector, 16 per 128-byte line): six warp instructions
